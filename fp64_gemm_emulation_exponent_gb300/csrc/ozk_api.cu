@@ -1,0 +1,560 @@
+// C-ABI of libozk: argument checks, method constants, workspace layout and the
+// stage sequence of the Ozaki-II pipeline (the "Day 12" page, section
+// "Profile 不能只看 Tensor Core": scale / exponent scan, residue quantization,
+// INT8 GEMM, mod reduction, CRT reconstruction, undo scaling, write double).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "ozk_internal.h"
+
+namespace ozk {
+namespace {
+
+constexpr int kSplitSms = 152;  // SM count the split-K choice plans for (GB300)
+constexpr int64_t kMaxDim = INT32_MAX / 2;  // rows/columns the kernels index with int
+
+// ---- small unsigned multi-limb integers for the host-side constants -------
+struct Limbs {
+  uint32_t w[8];
+};
+
+void limbs_set(Limbs& a, uint32_t v) {
+  std::memset(a.w, 0, sizeof a.w);
+  a.w[0] = v;
+}
+
+void limbs_mul_small(Limbs& a, uint32_t m) {
+  uint64_t c = 0;
+  for (int l = 0; l < 8; ++l) {
+    c += static_cast<uint64_t>(a.w[l]) * m;
+    a.w[l] = static_cast<uint32_t>(c);
+    c >>= 32;
+  }
+}
+
+int limbs_msb(const Limbs& a) {
+  for (int l = 7; l >= 0; --l)
+    if (a.w[l]) return 32 * l + 31 - __builtin_clz(a.w[l]);
+  return -1;
+}
+
+int ceil_log2(int64_t K) {
+  int c = 0;
+  while (c < 62 && (int64_t{1} << c) < K) ++c;
+  return c;
+}
+
+CrtConst build_crt_const(int n) {
+  CrtConst K;
+  std::memset(&K, 0, sizeof K);
+  K.n = n;
+  Limbs P;
+  limbs_set(P, 1);
+  for (int k = 0; k < n; ++k) limbs_mul_small(P, modulus_at(k));
+  for (int l = 0; l < kMaxCrtLimbs; ++l) K.P[l] = P.w[l];
+  for (int k = 0; k < n; ++k) {
+    const uint32_t p = modulus_at(k);
+    K.p[k] = p;
+    K.magic[k] = magic_of(p);
+    K.bias[k] = bias_of(p);
+    K.r32[k] = static_cast<uint32_t>((0x100000000ull + p / 2) / p);
+    Limbs Mk;
+    limbs_set(Mk, 1);
+    uint32_t mk_mod_p = 1;
+    for (int j = 0; j < n; ++j) {
+      if (j == k) continue;
+      limbs_mul_small(Mk, modulus_at(j));
+      mk_mod_p = (mk_mod_p * (modulus_at(j) % p)) % p;
+    }
+    for (int l = 0; l < kMaxCrtLimbs; ++l) K.Mk[k][l] = Mk.w[l];
+    uint32_t inv = 0;
+    for (uint32_t x = 1; x < p; ++x)
+      if ((mk_mod_p * x) % p == 1u) {
+        inv = x;
+        break;
+      }
+    K.w[k] = inv;
+  }
+  return K;
+}
+
+CrtConst g_crt[kMaxModuli + 1];
+std::once_flag g_crt_once;
+
+// ---- per-device state -----------------------------------------------------
+std::mutex g_mutex;
+struct DevInfo {
+  int checked = 0;  // 0 unknown, 1 ok, -1 wrong architecture
+  int sms = 0;
+};
+std::map<int, DevInfo> g_dev;
+std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_ws;  // cached workspaces
+struct HostBufs {
+  double* A = nullptr;
+  double* B = nullptr;
+  double* C = nullptr;
+  size_t a = 0, b = 0, c = 0;
+};
+std::map<int, HostBufs> g_host;
+
+int check_device(int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DevInfo& d = g_dev[dev];
+  if (d.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return OZK_ERR_CUDA;
+    d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    d.sms = sms;
+  }
+  if (d.checked < 0) return OZK_ERR_DEVICE;
+  if (sms_out) *sms_out = d.sms;
+  return OZK_OK;
+}
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool ranges_overlap(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+size_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return sizeof(double) * static_cast<size_t>((rows - 1) * ld + cols);
+}
+
+int validate(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+             int64_t ldb, const double* C, int64_t ldc, int n) {
+  if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  if (n < 2 || n > kMaxModuli) return OZK_ERR_UNSUPPORTED;
+  if (K > OZK_MAX_K || M > kMaxDim || N > kMaxDim) return OZK_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return OZK_OK;
+  if (!C || ldc < N) return OZK_ERR_INVALID_ARG;
+  if (K == 0) return OZK_OK;
+  if (!A || !B || lda < K || ldb < N) return OZK_ERR_INVALID_ARG;
+  if (beta_for(K, n) < 1) return OZK_ERR_UNSUPPORTED;
+  const size_t cb = span_bytes(M, N, ldc);
+  if (ranges_overlap(C, cb, A, span_bytes(M, K, lda)) || ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
+    return OZK_ERR_INVALID_ARG;
+  return OZK_OK;
+}
+
+// Workspace layout (byte offsets), shared by ozk_workspace_size and the run.
+struct Layout {
+  size_t amax, s, t, a, b, out, total;
+  int64_t kpad, ldo;
+  int splits;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
+  Layout L;
+  L.kpad = ozk_kpad(K);
+  L.splits = choose_splits(M, N, L.kpad, n, kSplitSms);
+  L.ldo = L.splits == 1 ? round_up(N, 16) : round_up(N, 4);
+  size_t off = 0;
+  L.amax = off;
+  off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(M + N), 256);
+  L.s = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(M), 256);
+  L.t = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(N), 1024);
+  L.a = off;
+  off = align_up(off + 2u * static_cast<size_t>(n) * M * L.kpad, 1024);
+  L.b = off;
+  off = align_up(off + 2u * static_cast<size_t>(n) * N * L.kpad, 1024);
+  L.out = off;
+  const size_t per = L.splits == 1 ? 1 : 4 * static_cast<size_t>(L.splits);
+  off = align_up(off + per * static_cast<size_t>(n) * M * L.ldo, 256);
+  L.total = off;
+  return L;
+}
+
+int record(ozk_event_t* ev, int idx, cudaStream_t stream) {
+  if (!ev) return OZK_OK;
+  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[idx]), stream) == cudaSuccess ? OZK_OK
+                                                                                          : OZK_ERR_CUDA;
+}
+
+#define OZK_CUDA(expr)                   \
+  do {                                   \
+    if ((expr) != cudaSuccess) return OZK_ERR_CUDA; \
+  } while (0)
+
+int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+              int64_t ldb, double* C, int64_t ldc, int n, void* ws, size_t ws_bytes,
+              cudaStream_t stream, ozk_event_t* ev) {
+  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return OZK_OK;
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
+  if (K == 0) {
+    OZK_CUDA(cudaMemset2DAsync(C, sizeof(double) * ldc, 0, sizeof(double) * N, M, stream));
+    return OZK_OK;
+  }
+  const Layout L = layout_for(M, N, K, n);
+  if (!ws || ws_bytes < L.total || reinterpret_cast<uintptr_t>(ws) % 256) return OZK_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
+  int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
+  int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
+  uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
+  uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
+  void* out = base + L.out;
+  const int beta = beta_for(K, n);
+
+  if ((rc = record(ev, 0, stream))) return rc;
+  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
+  if ((rc = record(ev, 1, stream))) return rc;
+  OZK_CUDA(launch_quantize_a(M, K, L.kpad, A, lda, s, n, as, stream));
+  OZK_CUDA(launch_quantize_b(K, N, L.kpad, B, ldb, t, n, bs, stream));
+  if ((rc = record(ev, 2, stream))) return rc;
+  OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, bs, n, L.splits == 1 ? 0 : 1, out, L.ldo, L.splits,
+                               sms, stream));
+  if ((rc = record(ev, 3, stream))) return rc;
+  OZK_CUDA(launch_crt(M, N, n, out, L.splits == 1 ? 0 : 1, L.ldo, L.splits, s, t, C, ldc, nullptr,
+                      stream));
+  if ((rc = record(ev, 4, stream))) return rc;
+  return OZK_OK;
+}
+
+}  // namespace
+
+int beta_for(int64_t K, int n) {
+  if (n < 2 || n > kMaxModuli) return -1;
+  if (K < 1) K = 1;
+  Limbs P;
+  limbs_set(P, 1);
+  for (int k = 0; k < n; ++k) limbs_mul_small(P, modulus_at(k));
+  const int num = limbs_msb(P) - 1 - ceil_log2(K);
+  const int beta = num >= 0 ? num / 2 : -((-num + 1) / 2);
+  return beta >= 1 ? beta : -1;
+}
+
+const CrtConst& crt_const(int n) {
+  std::call_once(g_crt_once, [] {
+    for (int k = 2; k <= kMaxModuli; ++k) g_crt[k] = build_crt_const(k);
+  });
+  return g_crt[n];
+}
+
+}  // namespace ozk
+
+using namespace ozk;
+
+extern "C" {
+
+const char* ozk_status_string(int status) {
+  switch (status) {
+    case OZK_OK: return "ok";
+    case OZK_ERR_INVALID_ARG: return "invalid argument";
+    case OZK_ERR_UNSUPPORTED: return "unsupported size or moduli count";
+    case OZK_ERR_WORKSPACE: return "workspace missing, too small, misaligned or not allocatable";
+    case OZK_ERR_CUDA: return "CUDA runtime error";
+    case OZK_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    case OZK_ERR_DEVICE: return "device is not sm_103 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+int ozk_moduli(int n_moduli, int32_t* out) {
+  if (n_moduli < 1 || n_moduli > kMaxModuli || !out) return OZK_ERR_INVALID_ARG;
+  for (int k = 0; k < n_moduli; ++k) out[k] = static_cast<int32_t>(modulus_at(k));
+  return OZK_OK;
+}
+
+int ozk_beta(int64_t K, int n_moduli) {
+  const int b = beta_for(K, n_moduli);
+  return b >= 1 ? b : -OZK_ERR_UNSUPPORTED;
+}
+
+int64_t ozk_kpad(int64_t K) { return K <= 0 ? 0 : (K + kKBlock - 1) / kKBlock * kKBlock; }
+
+size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli) {
+  if (M <= 0 || N <= 0 || K <= 0 || K > OZK_MAX_K) return 0;
+  if (M > kMaxDim || N > kMaxDim || beta_for(K, n_moduli) < 1) return 0;
+  return layout_for(M, N, K, n_moduli).total;
+}
+
+int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, double* C, int64_t ldc, int n_moduli,
+                       void* workspace, size_t workspace_bytes, ozk_stream_t stream,
+                       ozk_event_t* events) {
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+int ozk_dgemm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                 int64_t ldb, double* C, int64_t ldc, int n_moduli, void* workspace,
+                 size_t workspace_bytes, ozk_stream_t stream) {
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int ozk_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+              int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return OZK_OK;
+  if ((rc = check_device(nullptr))) return rc;
+  const size_t need = K > 0 ? layout_for(M, N, K, n_moduli).total : 0;
+  void* ws = nullptr;
+  if (need) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto& slot = g_ws[{dev, st}];
+    if (slot.second < need) {
+      if (slot.first) {
+        if (cudaStreamSynchronize(st) != cudaSuccess) return OZK_ERR_CUDA;
+        cudaFree(slot.first);
+        slot = {nullptr, 0};
+      }
+      if (cudaMalloc(&slot.first, need) != cudaSuccess) {
+        slot = {nullptr, 0};
+        return OZK_ERR_WORKSPACE;
+      }
+      slot.second = need;
+    }
+    ws = slot.first;
+  }
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, ws, need,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                   int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return OZK_OK;
+  if ((rc = check_device(nullptr))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+  double *dA, *dB, *dC;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    HostBufs& h = g_host[dev];
+    auto grow = [&](double*& p, size_t& have, size_t need) -> bool {
+      if (have >= need) return true;
+      if (p) {
+        cudaDeviceSynchronize();
+        cudaFree(p);
+      }
+      p = nullptr;
+      have = 0;
+      if (need && cudaMalloc(&p, need) != cudaSuccess) return false;
+      have = need;
+      return true;
+    };
+    if (!grow(h.A, h.a, sizeof(double) * static_cast<size_t>(M * K)) ||
+        !grow(h.B, h.b, sizeof(double) * static_cast<size_t>(K * N)) ||
+        !grow(h.C, h.c, sizeof(double) * static_cast<size_t>(M * N)))
+      return OZK_ERR_WORKSPACE;
+    dA = h.A;
+    dB = h.B;
+    dC = h.C;
+  }
+  if (K > 0) {
+    OZK_CUDA(cudaMemcpy2DAsync(dA, sizeof(double) * K, A, sizeof(double) * lda, sizeof(double) * K, M,
+                               cudaMemcpyHostToDevice, st));
+    OZK_CUDA(cudaMemcpy2DAsync(dB, sizeof(double) * N, B, sizeof(double) * ldb, sizeof(double) * N, K,
+                               cudaMemcpyHostToDevice, st));
+  }
+  rc = ozk_dgemm(M, N, K, dA, K > 0 ? K : 1, dB, N, dC, N, n_moduli, stream);
+  if (rc) return rc;
+  OZK_CUDA(cudaMemcpy2DAsync(C, sizeof(double) * ldc, dC, sizeof(double) * N, sizeof(double) * N, M,
+                             cudaMemcpyDeviceToHost, st));
+  OZK_CUDA(cudaStreamSynchronize(st));
+  return OZK_OK;
+}
+
+int ozk_stream_status(ozk_stream_t stream) {
+  int status = 0;
+  const int rc = take_device_status(reinterpret_cast<cudaStream_t>(stream), &status);
+  if (rc) return rc;
+  return status ? OZK_ERR_TIMEOUT : OZK_OK;
+}
+
+int ozk_release_cached(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (cudaDeviceSynchronize() != cudaSuccess) return OZK_ERR_CUDA;
+  for (auto it = g_ws.begin(); it != g_ws.end();) {
+    if (it->first.first == dev) {
+      cudaFree(it->second.first);
+      it = g_ws.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  auto h = g_host.find(dev);
+  if (h != g_host.end()) {
+    cudaFree(h->second.A);
+    cudaFree(h->second.B);
+    cudaFree(h->second.C);
+    g_host.erase(h);
+  }
+  return OZK_OK;
+}
+
+int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+              int64_t ldb, int n_moduli, int32_t* s, int32_t* t, uint64_t* scratch,
+              ozk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  const int beta = beta_for(K, n_moduli);
+  if (beta < 1 || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (M + N == 0) return OZK_OK;
+  if (!scratch || (M && !s) || (N && !t)) return OZK_ERR_INVALID_ARG;
+  if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, scratch,
+                        reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda, const int32_t* s, int n_moduli,
+                   uint16_t* a_slices, ozk_stream_t stream) {
+  if (M < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  if (n_moduli < 2 || n_moduli > kMaxModuli || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return OZK_OK;
+  if (!A || lda < K || !s || !a_slices || reinterpret_cast<uintptr_t>(a_slices) % 16)
+    return OZK_ERR_INVALID_ARG;
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  OZK_CUDA(launch_quantize_a(M, K, ozk_kpad(K), A, lda, s, n_moduli, a_slices,
+                             reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb, const int32_t* t, int n_moduli,
+                   uint16_t* b_slices, ozk_stream_t stream) {
+  if (N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  if (n_moduli < 2 || n_moduli > kMaxModuli || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (N == 0 || K == 0) return OZK_OK;
+  if (!B || ldb < N || !t || !b_slices || reinterpret_cast<uintptr_t>(b_slices) % 16)
+    return OZK_ERR_INVALID_ARG;
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  OZK_CUDA(launch_quantize_b(K, N, ozk_kpad(K), B, ldb, t, n_moduli, b_slices,
+                             reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
+                     const uint16_t* b_slices, int n_moduli, int out_kind, void* out, int64_t ldo,
+                     int splits, ozk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  if (n_moduli < 2 || n_moduli > kMaxModuli || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (M > kMaxDim || N > kMaxDim) return OZK_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0 || K == 0) return OZK_OK;
+  const int64_t kpad = ozk_kpad(K);
+  if (!a_slices || !b_slices || !out) return OZK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a_slices) % 16 || reinterpret_cast<uintptr_t>(b_slices) % 16 ||
+      reinterpret_cast<uintptr_t>(out) % 16)
+    return OZK_ERR_INVALID_ARG;
+  if (out_kind == 0) {
+    if (splits != 1 || ldo < N || ldo % 16) return OZK_ERR_INVALID_ARG;
+  } else if (out_kind == 1) {
+    if (splits < 1 || splits > 64 || splits > kpad / kKBlock || ldo < N || ldo % 4)
+      return OZK_ERR_INVALID_ARG;
+  } else {
+    return OZK_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  OZK_CUDA(launch_residue_gemm(M, N, kpad, a_slices, b_slices, n_moduli, out_kind, out, ldo, splits,
+                               sms, reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+static int check_crt_args(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind,
+                          int64_t ldi, int splits) {
+  if (M < 0 || N < 0) return OZK_ERR_INVALID_ARG;
+  if (n_moduli < 2 || n_moduli > kMaxModuli) return OZK_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return OZK_OK;
+  if (!in || reinterpret_cast<uintptr_t>(in) % 16) return OZK_ERR_INVALID_ARG;
+  if (in_kind == 0) {
+    if (splits != 1 || ldi < N || ldi % 16) return OZK_ERR_INVALID_ARG;
+  } else if (in_kind == 1) {
+    if (splits < 1 || splits > 64 || ldi < N || ldi % 4) return OZK_ERR_INVALID_ARG;
+  } else {
+    return OZK_ERR_INVALID_ARG;
+  }
+  return OZK_OK;
+}
+
+int ozk_crt_combine(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind, int64_t ldi,
+                    int splits, const int32_t* s, const int32_t* t, double* C, int64_t ldc,
+                    ozk_stream_t stream) {
+  int rc = check_crt_args(M, N, n_moduli, in, in_kind, ldi, splits);
+  if (rc || M == 0 || N == 0) return rc;
+  if (!s || !t || !C || ldc < N) return OZK_ERR_INVALID_ARG;
+  if ((rc = check_device(nullptr))) return rc;
+  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, splits, s, t, C, ldc, nullptr,
+                      reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_crt_lift(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind, int64_t ldi,
+                 int splits, uint32_t* X, ozk_stream_t stream) {
+  int rc = check_crt_args(M, N, n_moduli, in, in_kind, ldi, splits);
+  if (rc || M == 0 || N == 0) return rc;
+  if (!X) return OZK_ERR_INVALID_ARG;
+  if ((rc = check_device(nullptr))) return rc;
+  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, splits, nullptr, nullptr, nullptr, 0, X,
+                      reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_event_create(ozk_event_t* ev) {
+  if (!ev) return OZK_ERR_INVALID_ARG;
+  cudaEvent_t e;
+  if (cudaEventCreate(&e) != cudaSuccess) return OZK_ERR_CUDA;
+  *ev = reinterpret_cast<ozk_event_t>(e);
+  return OZK_OK;
+}
+
+int ozk_event_destroy(ozk_event_t ev) {
+  return cudaEventDestroy(reinterpret_cast<cudaEvent_t>(ev)) == cudaSuccess ? OZK_OK : OZK_ERR_CUDA;
+}
+
+int ozk_event_record(ozk_event_t ev, ozk_stream_t stream) {
+  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? OZK_OK
+             : OZK_ERR_CUDA;
+}
+
+int ozk_event_elapsed(ozk_event_t start, ozk_event_t stop, float* ms) {
+  if (!ms) return OZK_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(reinterpret_cast<cudaEvent_t>(stop)) != cudaSuccess) return OZK_ERR_CUDA;
+  return cudaEventElapsedTime(ms, reinterpret_cast<cudaEvent_t>(start),
+                              reinterpret_cast<cudaEvent_t>(stop)) == cudaSuccess
+             ? OZK_OK
+             : OZK_ERR_CUDA;
+}
+
+int ozk_device_sm_count(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return sms;
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// Internal declarations shared by the CUDA translation units of libozk.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "ozk.h"
+
+namespace ozk {
+
+constexpr int kMaxModuli = 20;
+constexpr int kKBlock = 64;  // K elements (bf16) per smem row: 128 bytes, one swizzle row
+constexpr int kNumSmsFallback = 148;
+
+// Moduli in the order they are consumed: pairwise coprime integers <= 256,
+// so every balanced residue lies in [-128, 127].
+__host__ __device__ constexpr uint32_t modulus_at(int k) {
+  constexpr uint32_t t[kMaxModuli] = {256, 255, 253, 251, 247, 241, 239, 233, 229, 227,
+                                      223, 217, 211, 199, 197, 193, 191, 181, 179, 173};
+  return t[k];
+}
+
+// q = __umulhi(u, magic) is floor(u/p) or floor(u/p)+1 for every u < 2^32,
+// because magic*p = 2^32 + e with 1 <= e <= p.  One conditional add fixes r.
+__host__ __device__ constexpr uint32_t magic_of(uint32_t p) {
+  return static_cast<uint32_t>(0x100000000ull / p) + 1u;
+}
+
+// A multiple of p in [2^31, 2^31 + p): x + bias maps every int32 |x| < 2^31 - 2^14
+// to [0, 2^32) without changing its class mod p.
+__host__ __device__ constexpr uint32_t bias_of(uint32_t p) {
+  return static_cast<uint32_t>(((0x80000000ull + p - 1) / p) * p);
+}
+
+__host__ __device__ constexpr uint32_t pow2_mod(int e, uint32_t p) {
+  uint32_t r = 1u % p;
+  for (int i = 0; i < e; ++i) r = (r * 2u) % p;
+  return r;
+}
+
+template <int I, int N, typename F>
+__host__ __device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<I + 1, N>(f);
+  }
+}
+
+// Limb count of the CRT accumulator for n moduli: S = sum_k y_k P/p_k with
+// y_k < 2^16 stays below 2^(8n + 14) (log2 P <= 8n, n <= 20).  At least 3.
+__host__ __device__ constexpr int crt_limbs(int n) {
+  return (8 * n + 14 + 31) / 32 < 3 ? 3 : (8 * n + 14 + 31) / 32;
+}
+constexpr int kMaxCrtLimbs = 6;
+
+// Constants of the CRT combine for one moduli count (built on the host).
+struct CrtConst {
+  uint32_t p[kMaxModuli];
+  uint32_t magic[kMaxModuli];
+  uint32_t bias[kMaxModuli];
+  uint32_t w[kMaxModuli];    // (P/p_k)^-1 mod p_k
+  uint32_t r32[kMaxModuli];  // round(2^32 / p_k)
+  uint32_t Mk[kMaxModuli][kMaxCrtLimbs];  // P/p_k, little-endian 32-bit limbs
+  uint32_t P[kMaxCrtLimbs];
+  int n;
+};
+
+// Host-side method constants (ozk_api.cu).
+int beta_for(int64_t K, int n);  // -1 when unsupported
+const CrtConst& crt_const(int n);
+
+// Launchers; each returns the first CUDA error it meets.
+cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                         const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
+                         uint64_t* amax, cudaStream_t stream);
+cudaError_t launch_quantize_a(int64_t M, int64_t K, int64_t kpad, const double* A,
+                              int64_t lda, const int32_t* s, int n, uint16_t* out,
+                              cudaStream_t stream);
+cudaError_t launch_quantize_b(int64_t K, int64_t N, int64_t kpad, const double* B,
+                              int64_t ldb, const int32_t* t, int n, uint16_t* out,
+                              cudaStream_t stream);
+cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
+                                const uint16_t* b_slices, int n, int out_kind, void* out,
+                                int64_t ldo, int splits, int num_sms, cudaStream_t stream);
+cudaError_t launch_crt(int64_t M, int64_t N, int n, const void* in, int in_kind, int64_t ldi,
+                       int splits, const int32_t* s, const int32_t* t, double* C, int64_t ldc,
+                       uint32_t* X, cudaStream_t stream);
+
+// Device status word latched by kernels (residue_gemm.cu).
+int take_device_status(cudaStream_t stream, int* status);
+
+// Tile sizes of the residue GEMM, exposed for the host's split-K choice.
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms);
+
+}  // namespace ozk

@@ -1,0 +1,601 @@
+// One integer GEMM per modulus with the mod reduction fused into the epilogue
+// (the "INT8 GEMM" and "mod reduction" stages of the Ozaki-II pipeline on the
+// "Day 12" page, section "Profile 不能只看 Tensor Core"; its section
+// "一次 NCU 結果怎麼解讀" shows a register-starved mma.sync kernel, 218
+// registers per thread and the Tensor pipe at 7.5%).
+//
+// GB300 (sm_103a) has no tcgen05 kind::i8, so the residues (integers in
+// [-128, 127]) are fed to the bf16 tensor cores, where they are exact: every
+// product is an integer below 2^14 in magnitude and every fp32 partial sum of
+// one 256-term chunk stays below 2^22, so the fp32 accumulator in TMEM holds
+// the chunk's exact integer sum.  The epilogue warps read each chunk out of
+// TMEM and add it into int32 registers (exact for K < 2^17), then reduce mod p
+// once per tile.
+//
+// Structure: persistent CTAs (one per SM), warp-specialised.
+//   warp 0      TMA producer: A and B slice tiles into a 4-stage smem ring
+//               (128-byte swizzle), one mbarrier pair per stage.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and issues tcgen05.mma (M=128, N=256, K=16) from one lane.
+//   warps 2, 3  idle (they complete warpgroup 0, which hands its registers
+//               to the epilogue through setmaxnreg).
+//   warps 4..11 epilogue: TMEM -> registers -> int32 sums -> mod p -> HBM.
+// Every mbarrier wait is bounded (2 s); a wait that runs out latches
+// OZK_ERR_TIMEOUT on the device, makes all roles stop, drains in-flight copies
+// and MMAs, frees TMEM and returns.
+#include <cuda.h>
+
+#include "ozk_internal.h"
+
+namespace ozk {
+
+__device__ int g_status;  // latched device-side faults, read by ozk_stream_status
+
+namespace {
+
+constexpr int BM = kTileM, BN = kTileN, BK = kKBlock;
+constexpr int kStages = 4;
+constexpr int kChunkKB = 4;  // k-blocks per exact fp32 chunk: 256 products, |sum| <= 2^22
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0: control, 1-2: epilogue
+// Register split between the warpgroups (setmaxnreg).  The kernel launches
+// with kLaunchRegs per thread; warpgroup 0 gives registers back, the two
+// epilogue warpgroups take them: 128 * 56 + 256 * 224 = 384 * 168.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 56;
+constexpr int kEpiRegs = 224;
+static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split exceeds the pool");
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 50000000ull;
+
+// fp32 bits of 1.5 * 2^23: x + 1.5*2^23 for an integer |x| <= 2^22 has the
+// integer x in its low mantissa bits, exactly.
+constexpr float kMagic = 12582912.0f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+struct ModTable {
+  uint32_t p[kMaxModuli], magic[kMaxModuli], bias[kMaxModuli];
+};
+
+__host__ __device__ constexpr ModTable make_mod_table() {
+  ModTable t{};
+  for (int k = 0; k < kMaxModuli; ++k) {
+    t.p[k] = modulus_at(k);
+    t.magic[k] = magic_of(t.p[k]);
+    t.bias[k] = bias_of(t.p[k]);
+  }
+  return t;
+}
+
+__constant__ ModTable c_mod = make_mod_table();
+
+struct GemmParams {
+  int M, N, n, kblocks, tiles_m, tiles_n, splits, kb_per_split, out_kind;
+  int64_t ldo;
+  void* out;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of the given parity to complete.  Returns false when
+// another role has aborted, or after kTimeoutNs (then latches the fault and
+// tells the other roles to stop).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(&g_status, 1);
+        return false;
+      }
+    }
+  }
+}
+
+// Every lane of the warp waits; the outcome is made warp-uniform so that the
+// .sync.aligned tcgen05 instructions after it see a converged warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool got = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, got);
+}
+
+// Bounded wait used only while shutting down after an abort.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_test(bar, parity))
+    if (globaltimer() - t0 > kDrainNs) return;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
+// start address >> 4 (bits 0-13), leading byte offset 16 B (unused for this
+// layout), stride byte offset 1024 B between 8-row groups (bits 32-45),
+// descriptor version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the mbarrier when every tcgen05.mma issued so far by this
+// thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+struct Unit {
+  int p, sk, mt, nt, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
+  Unit r;
+  r.nt = u % prm.tiles_n;
+  u /= prm.tiles_n;
+  r.mt = u % prm.tiles_m;
+  u /= prm.tiles_m;
+  r.sk = u % prm.splits;
+  r.p = u / prm.splits;
+  r.kb0 = r.sk * prm.kb_per_split;
+  r.kb1 = min(prm.kblocks, r.kb0 + prm.kb_per_split);
+  if (r.kb1 < r.kb0) r.kb1 = r.kb0;
+  return r;
+}
+
+// x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
+__device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic, uint32_t bias) {
+  const uint32_t u = static_cast<uint32_t>(x) + bias;
+  const uint32_t q = __umulhi(u, magic);
+  int32_t r = static_cast<int32_t>(u - q * p);
+  r += r < 0 ? static_cast<int32_t>(p) : 0;
+  return static_cast<uint32_t>(r);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // 1024-aligned tiles
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t accf0 = empty0 + 8 * kStages;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const int units = prm.n * prm.splits * prm.tiles_m * prm.tiles_n;
+
+  if (warp < 4) regs_dec<kCtrlRegs>();
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    // The whole warp walks the schedule and waits; lane 0 issues the copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued_parity[kStages];
+    for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(u, prm);
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(full0 + 8 * stage, kStageBytes);
+          tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p,
+                      full0 + 8 * stage);
+          tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, kb * BK, w.nt * BN, w.p,
+                      full0 + 8 * stage);
+        }
+        __syncwarp();
+        issued_parity[stage] = static_cast<int>(phase);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {  // let copies still in flight land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (issued_parity[s] >= 0)
+          mbar_wait_drain(full0 + 8 * s, static_cast<uint32_t>(issued_parity[s]));
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    // The whole warp walks the schedule and waits; lane 0 issues the MMAs.
+    int stage = 0;
+    uint32_t phase = 0;
+    int ab = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(u, prm);
+      for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
+        const int c1 = min(w.kb1, c0 + kChunkKB);
+        if (!warp_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
+        for (int kb = c0; kb < c1; ++kb) {
+          if (!warp_wait(full0 + 8 * stage, phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * kABytes));
+            const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
+              mma_bf16(d, da + 2ull * kk, db + 2ull * kk, kIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
+            mma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs are done
+          }
+          __syncwarp();
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(accf0 + 8 * ab);  // chunk sum ready in TMEM buffer ab
+        __syncwarp();
+        ab ^= 1;
+        if (ab == 0) aphase ^= 1u;
+      }
+    }
+    if (lane == 0) {
+      mma_commit(drain);  // every issued MMA has finished before TMEM is freed
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------ epilogue ------------------------------
+    regs_inc<kEpiRegs>();
+    const int ew = warp - 4;
+    const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
+    const int half = ew >> 2;   // which 128 of the 256 tile columns
+    const int row_in_tile = quad * 32 + lane;
+    int ab = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit w = decode_unit(u, prm);
+      const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
+      int32_t acc[128];
+#pragma unroll
+      for (int e = 0; e < 128; ++e) acc[e] = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(ab * BN + half * 128);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t v[32];
+          tmem_ld32(taddr + 32 * q, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            acc[32 * q + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8 * ab);
+        ab ^= 1;
+        if (ab == 0) aphase ^= 1u;
+      }
+      if (!ok) break;
+      const uint32_t offset = static_cast<uint32_t>(nchunks) * kMagicBits;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
+
+      const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
+      const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * 128;
+      if (gi < prm.M) {
+        if (prm.out_kind == 0) {
+          const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
+          uint8_t* dst = static_cast<uint8_t*>(prm.out) +
+                         (static_cast<int64_t>(w.p) * prm.M + gi) * prm.ldo + gj0;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            if (gj0 + 16 * v < prm.ldo) {
+              uint32_t word[4];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                word[b] = mod_p(acc[16 * v + 4 * b], p, mg, bs) |
+                          (mod_p(acc[16 * v + 4 * b + 1], p, mg, bs) << 8) |
+                          (mod_p(acc[16 * v + 4 * b + 2], p, mg, bs) << 16) |
+                          (mod_p(acc[16 * v + 4 * b + 3], p, mg, bs) << 24);
+              }
+              *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+            }
+          }
+        } else {
+          int32_t* dst = static_cast<int32_t*>(prm.out) +
+                         ((static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.M + gi) * prm.ldo + gj0;
+#pragma unroll
+          for (int v = 0; v < 32; ++v)
+            if (gj0 + 4 * v < prm.ldo)
+              *reinterpret_cast<int4*>(dst + 4 * v) =
+                  make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 3-D view [n][rows][kpad] of bf16 slices, box 64 (k) x box_rows x 1.
+bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t kpad, int n,
+                    uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kpad), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(n)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kpad) * 2,
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(kpad) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
+  const int64_t tiles = static_cast<int64_t>(n) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t kblocks = kpad / BK;
+  if (tiles >= num_sms || kblocks < 32) return 1;
+  auto eff = [&](int64_t s) {
+    const int64_t units = tiles * s;
+    const int64_t waves = (units + num_sms - 1) / num_sms;
+    return static_cast<double>(units) / static_cast<double>(waves * num_sms);
+  };
+  int best = 1;
+  double best_eff = eff(1);
+  for (int64_t s = 2; s <= 64 && kblocks / s >= 16; ++s) {
+    const double e = eff(s);
+    if (e > best_eff + 0.02) {
+      best = static_cast<int>(s);
+      best_eff = e;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
+                                const uint16_t* b_slices, int n, int out_kind, void* out,
+                                int64_t ldo, int splits, int num_sms, cudaStream_t stream) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  CUtensorMap tmA, tmB;
+  if (!make_slice_map(&tmA, a_slices, M, kpad, n, BM) || !make_slice_map(&tmB, b_slices, N, kpad, n, BN))
+    return cudaErrorInvalidValue;
+  GemmParams prm;
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(N);
+  prm.n = n;
+  prm.kblocks = static_cast<int>(kpad / BK);
+  prm.tiles_m = static_cast<int>((M + BM - 1) / BM);
+  prm.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  prm.splits = splits;
+  prm.kb_per_split = (prm.kblocks + splits - 1) / splits;
+  prm.out_kind = out_kind;
+  prm.ldo = ldo;
+  prm.out = out;
+  const int64_t units = static_cast<int64_t>(n) * splits * prm.tiles_m * prm.tiles_n;
+  const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
+  cudaError_t e = cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the pool has the registers: refuse to launch
+  // unless the compiled launch register count covers the split exactly.
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, residue_gemm_kernel)) != cudaSuccess) return e;
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+  residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, prm);
+  return cudaGetLastError();
+}
+
+int take_device_status(cudaStream_t stream, int* status) {
+  *status = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return OZK_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return OZK_ERR_CUDA;
+  if (v) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return OZK_ERR_CUDA;
+  }
+  *status = v;
+  return OZK_OK;
+}
+
+}  // namespace ozk

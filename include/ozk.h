@@ -1,0 +1,201 @@
+/*
+ * ozk — FP64 GEMM emulated with exact integer residue GEMMs on GB300 tensor
+ * cores and Chinese-Remainder reconstruction (Ozaki scheme II).
+ *
+ * Method source: the "Day 12" page on ithelp.ithome.com.tw (Ozaki-II
+ * INT8/CRT FP64 GEMM emulation).  Its section "Profile 不能只看 Tensor Core"
+ * lists the pipeline this library implements, stage by stage:
+ *   scale / exponent scan -> residue quantization -> integer GEMM per modulus
+ *   -> mod reduction -> CRT reconstruction -> undo scaling -> write double.
+ * Its section "先定義公平比較" fixes the boundary: double in, double out.
+ *
+ * Conventions for every entry point:
+ *  - A is M x K, B is K x N, C is M x N, all row-major double, leading
+ *    dimensions in elements (lda >= K, ldb >= N, ldc >= N).  C = A * B.
+ *  - n_moduli (2..20) selects the first n of the moduli
+ *    {256,255,253,251,247,241,239,233,229,227,223,217,211,199,197,193,191,181,179,173}.
+ *    14 gives about a 53-bit product, 8 about 26 bits per operand.
+ *  - Device pointers belong to the caller; the library never frees them.
+ *  - ozk_stream_t is a cudaStream_t (NULL = legacy default stream).  Work is
+ *    stream-ordered and asynchronous unless stated otherwise.
+ *  - Argument errors are returned synchronously before anything is launched.
+ *    Launch failures return OZK_ERR_CUDA.  Faults detected inside a kernel
+ *    (a pipeline wait that ran out) are latched on the device and reported by
+ *    ozk_stream_status().
+ *  - Sizes M, N or K equal to 0 are valid: nothing is computed, and for K = 0
+ *    (with M, N > 0) C is filled with zeros.
+ *  - Requires a GB300-class GPU (sm_103a); other devices give OZK_ERR_DEVICE.
+ */
+#ifndef OZK_H
+#define OZK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ozk_stream_t; /* identical to cudaStream_t */
+typedef struct CUevent_st* ozk_event_t;   /* identical to cudaEvent_t */
+
+typedef enum {
+  OZK_OK = 0,
+  OZK_ERR_INVALID_ARG = 1, /* bad pointer, size, leading dimension or overlap */
+  OZK_ERR_UNSUPPORTED = 2, /* K >= 2^17, n_moduli outside 2..20, or too few moduli for K */
+  OZK_ERR_WORKSPACE = 3,   /* caller workspace too small, or allocation failed */
+  OZK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  OZK_ERR_TIMEOUT = 5,     /* a kernel's bounded pipeline wait ran out (device-side) */
+  OZK_ERR_DEVICE = 6       /* current device is not sm_103 */
+} ozk_status;
+
+#define OZK_MAX_MODULI 20
+#define OZK_MAX_K 131071           /* exact int32 sums need 2^14 * K < 2^31 */
+#define OZK_SCALE_NONFINITE INT32_MIN
+#define OZK_LIMBS 8                /* lifted integers: 8 x uint32, two's complement */
+
+/* ------------------------------------------------------------------ */
+/* Host-only helpers (no CUDA calls).                                  */
+/* ------------------------------------------------------------------ */
+
+/* Human-readable text for a status code.  Never NULL. */
+const char* ozk_status_string(int status);
+
+/* Writes the first n_moduli moduli to out[0..n-1].  Returns OZK_OK or
+ * OZK_ERR_INVALID_ARG. */
+int ozk_moduli(int n_moduli, int32_t* out);
+
+/* Bits per operand beta for inner dimension K: the largest even split of
+ * floor(log2 P) - 1 - ceil(log2 K) bits, P the product of the moduli, so that
+ * the symmetric CRT lift of sum_k a'_ik b'_kj is exact.  Returns beta >= 1,
+ * or -OZK_ERR_UNSUPPORTED when the moduli cannot cover K. */
+int ozk_beta(int64_t K, int n_moduli);
+
+/* Row length of the residue slices: K rounded up to a multiple of 64. */
+int64_t ozk_kpad(int64_t K);
+
+/* Bytes of device workspace ozk_dgemm_ws needs for this problem (0 when
+ * nothing is computed).  Returns 0 as well for unsupported arguments, which
+ * ozk_dgemm_ws then reports. */
+size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli);
+
+/* ------------------------------------------------------------------ */
+/* The GEMM.                                                           */
+/* ------------------------------------------------------------------ */
+
+/* C = A * B with n_moduli residue GEMMs.  A, B, C are device pointers.
+ * C must not overlap A or B (OZK_ERR_INVALID_ARG).  Rows of A or columns of
+ * B that hold an Inf or NaN give NaN rows/columns of C.  Uses a workspace the
+ * library allocates on first use and caches per (device, stream); calls on
+ * different streams therefore never share scratch memory. */
+int ozk_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+              const double* B, int64_t ldb, double* C, int64_t ldc,
+              int n_moduli, ozk_stream_t stream);
+
+/* As ozk_dgemm, with caller-provided device workspace of at least
+ * ozk_workspace_size(M, N, K, n_moduli) bytes (256-byte aligned).  The
+ * library allocates nothing.  Calls that share a workspace must be ordered
+ * on one stream. */
+int ozk_dgemm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                 const double* B, int64_t ldb, double* C, int64_t ldc,
+                 int n_moduli, void* workspace, size_t workspace_bytes,
+                 ozk_stream_t stream);
+
+/* As ozk_dgemm_ws, recording events[0..4] on the stream at the stage
+ * boundaries (before scan, before quantize, before the residue GEMM,
+ * before the CRT combine, after it) when events is not NULL.  The events are
+ * the caller's (create them with ozk_event_create). */
+int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A,
+                       int64_t lda, const double* B, int64_t ldb, double* C,
+                       int64_t ldc, int n_moduli, void* workspace,
+                       size_t workspace_bytes, ozk_stream_t stream,
+                       ozk_event_t* events);
+
+/* C = A * B for HOST matrices (pinned memory gives the fastest copies).
+ * Copies A and B to the device, runs ozk_dgemm on the stream, copies C back
+ * and synchronises the stream before returning.  Device buffers are cached
+ * per device and grow as needed. */
+int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                   const double* B, int64_t ldb, double* C, int64_t ldc,
+                   int n_moduli, ozk_stream_t stream);
+
+/* Synchronises the stream, then reports and clears a fault latched by a
+ * kernel (OZK_ERR_TIMEOUT), or OZK_ERR_CUDA if the stream reported an error. */
+int ozk_stream_status(ozk_stream_t stream);
+
+/* Releases the cached workspaces and host-copy buffers of the current device. */
+int ozk_release_cached(void);
+
+/* ------------------------------------------------------------------ */
+/* Stage entry points (the same kernels ozk_dgemm runs, one at a time). */
+/* All pointers are device pointers.                                   */
+/* ------------------------------------------------------------------ */
+
+/* Exponent scan ("scale / exponent scan").  s[i] = beta - E_i where
+ * max_k |a_ik| = f 2^E_i with f in [0.5, 1); t[j] likewise over the columns
+ * of B.  0 for an all-zero row/column, OZK_SCALE_NONFINITE when it holds an
+ * Inf or NaN.  scratch: (M + N) uint64 of device scratch memory, overwritten. */
+int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+              const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
+              uint64_t* scratch, ozk_stream_t stream);
+
+/* Residue quantisation of A ("double load, exponent scaling, round, mod,
+ * balanced int8 conversion").  For each modulus p and element:
+ * a'_ik = trunc(a_ik 2^s_i) and r = sym(a' mod p) in [-floor(p/2), ceil(p/2)-1],
+ * stored as bfloat16 (exact for these integers) at
+ * a_slices[(p * M + i) * kpad + k]; columns K..kpad-1 are zero.
+ * kpad = ozk_kpad(K).  Rows with s_i = OZK_SCALE_NONFINITE are zero. */
+int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda,
+                   const int32_t* s, int n_moduli, uint16_t* a_slices,
+                   ozk_stream_t stream);
+
+/* Residue quantisation of B, transposed to K-major: the residue of b'_kj is
+ * stored at b_slices[(p * N + j) * kpad + k]; rows K..kpad-1 are zero. */
+int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb,
+                   const int32_t* t, int n_moduli, uint16_t* b_slices,
+                   ozk_stream_t stream);
+
+/* One integer GEMM per modulus ("INT8 GEMM", run on bf16 tensor cores: every
+ * product and every partial sum of 256 terms is an exact fp32 integer) with
+ * the mod reduction fused into its epilogue.
+ *  out_kind 0: out is uint8 [n][M][ldo], c = (sum_k ra rb) mod p in [0, p);
+ *              ldo >= N, a multiple of 16; splits must be 1.
+ *  out_kind 1: out is int32 [splits][n][M][ldo], the exact partial sums over
+ *              the split'th share of K (their sum is the exact dot product);
+ *              ldo >= N, a multiple of 4.
+ * K is the inner dimension the slices were quantised with (kpad = ozk_kpad(K)).
+ * splits in 1..64 and at most kpad/64. */
+int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
+                     const uint16_t* b_slices, int n_moduli, int out_kind,
+                     void* out, int64_t ldo, int splits, ozk_stream_t stream);
+
+/* CRT reconstruction with symmetric lift, undo scaling, FP64 write:
+ * C_ij = RN-even(X_ij 2^-(s_i + t_j)) with X_ij the unique integer in
+ * [-P/2, P/2) congruent to the residues; NaN where s_i or t_j is
+ * OZK_SCALE_NONFINITE.  in / in_kind / ldi / splits as ozk_residue_gemm's out. */
+int ozk_crt_combine(int64_t M, int64_t N, int n_moduli, const void* in,
+                    int in_kind, int64_t ldi, int splits, const int32_t* s,
+                    const int32_t* t, double* C, int64_t ldc, ozk_stream_t stream);
+
+/* The lifted integers themselves, X[(i * N + j) * OZK_LIMBS + l] (limb l of
+ * a two's-complement 256-bit value, least significant first).  For checking
+ * the integer stage. */
+int ozk_crt_lift(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind,
+                 int64_t ldi, int splits, uint32_t* X, ozk_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Timing helpers (thin wrappers of the CUDA runtime).                 */
+/* ------------------------------------------------------------------ */
+int ozk_event_create(ozk_event_t* ev);
+int ozk_event_destroy(ozk_event_t ev);
+int ozk_event_record(ozk_event_t ev, ozk_stream_t stream);
+/* Milliseconds between two recorded events (synchronises on the second). */
+int ozk_event_elapsed(ozk_event_t start, ozk_event_t stop, float* ms);
+
+/* Number of SMs of the current device (for sizing), or -1 on error. */
+int ozk_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OZK_H */

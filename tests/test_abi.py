@@ -1,0 +1,88 @@
+"""The C-ABI library on the CPU: it loads, exports every entry point that
+include/ozk.h declares, and its host-side logic (moduli, bit budget, slice
+padding, workspace size, status text) agrees with the oracle and with itself.
+No compute call is made here (no GPU)."""
+import os
+import re
+
+import pytest
+
+import oracle
+from fp64_gemm_emulation_exponent_gb300 import build as ozk_build
+from fp64_gemm_emulation_exponent_gb300 import ozk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ozk.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    ozk_build.build()
+    yield
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ozk_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ["ozk_dgemm", "ozk_dgemm_ws", "ozk_workspace_size", "ozk_stream_status",
+                 "ozk_status_string", "ozk_scale", "ozk_quantize_a", "ozk_quantize_b",
+                 "ozk_residue_gemm", "ozk_crt_combine", "ozk_crt_lift"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ozk.lib()
+    missing = [name for name in declared_functions() if not hasattr(L, name)]
+    assert not missing
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(declared_functions()) == set(ozk.SIGNATURES)
+
+
+def test_moduli_match_the_oracle():
+    assert ozk.ozk_moduli(20) == [int(p) for p in oracle.moduli(20)]
+
+
+def test_beta_matches_the_oracle():
+    for n in range(2, 21):
+        for K in [1, 2, 3, 63, 64, 65, 255, 256, 512, 1000, 1024, 4096, 8192, 65536, 131071]:
+            try:
+                want = oracle.beta(K, n)
+            except oracle.OracleError:
+                want = -ozk.OZK_ERR_UNSUPPORTED
+            assert ozk.ozk_beta(K, n) == want, (K, n)
+
+
+def test_kpad():
+    assert [ozk.ozk_kpad(k) for k in [0, 1, 63, 64, 65, 128, 131071]] == [0, 64, 64, 64, 128, 128, 131072]
+
+
+def test_workspace_size():
+    assert ozk.ozk_workspace_size(0, 10, 10, 14) == 0
+    assert ozk.ozk_workspace_size(10, 10, 0, 14) == 0
+    assert ozk.ozk_workspace_size(10, 10, 10, 1) == 0
+    assert ozk.ozk_workspace_size(10, 10, 131072, 14) == 0
+    for (M, N, K, n) in [(1, 1, 1, 2), (256, 256, 256, 14), (4096, 4096, 4096, 14), (8192, 8192, 512, 20),
+                         (512, 512, 65536, 20)]:
+        ws = ozk.ozk_workspace_size(M, N, K, n)
+        kpad = ozk.ozk_kpad(K)
+        slices = 2 * n * (M + N) * kpad
+        assert ws >= slices + n * M * N
+        assert ws % 256 == 0
+    # grows with every dimension
+    base = ozk.ozk_workspace_size(300, 300, 300, 14)
+    assert ozk.ozk_workspace_size(301, 300, 300, 14) > base
+    assert ozk.ozk_workspace_size(300, 300, 400, 14) > base
+    assert ozk.ozk_workspace_size(300, 300, 300, 15) > base
+
+
+def test_status_strings():
+    for code in range(0, 7):
+        assert ozk.status_string(code)
+    assert ozk.status_string(99) == "unknown status"

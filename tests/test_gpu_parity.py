@@ -1,0 +1,301 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle.
+
+Integer stages (scales, residue slices, per-modulus int32 sums, reduced
+residues, lifted integers) must match bit for bit.  The final FP64 C is the
+correctly rounded value of an exact integer, so it must match bit for bit as
+well; the error against the compensated reference is checked on top (the
+tolerances of the precision contract: 1e-14 at 14+ moduli, 2^-30 at 11).
+
+Method: Ozaki scheme II on the "Day 12" page (ithelp.ithome.com.tw), section
+"Profile 不能只看 Tensor Core" (stage list).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp64_gemm_emulation_exponent_gb300 import ozk, workloads
+from gpu_helpers import (bf16_to_int, dev, dgemm, ld_of, run_combine, run_gemm, run_lift,
+                         run_quantize, run_scale, same_bits, strided)
+
+pytestmark = pytest.mark.gpu
+
+
+def inputs(M, N, K, seed, kind="normal"):
+    rng = np.random.default_rng(seed)
+    A = rng.standard_normal((M, K))
+    B = rng.standard_normal((K, N))
+    if kind == "special":
+        if M > 3:
+            A[0] = 0.0
+            A[1] = np.ldexp(rng.standard_normal(K), -1040)   # subnormal row
+            A[2] = np.ldexp(rng.standard_normal(K), 900)     # huge row
+            A[3] = np.ldexp(rng.standard_normal(K), rng.integers(-60, 60, K))  # wide row
+        if N > 2:
+            B[:, 0] = 0.0
+            B[:, 1] = np.ldexp(rng.standard_normal(K), -300)
+            B[:, 2] = -np.ldexp(np.ones(K), 5)
+    return A, B
+
+
+def check_stages(A, B, n, splits=1):
+    M, K = A.shape
+    _, N = B.shape
+    dA, dB = dev(A), dev(B)
+    # 1. exponent scan
+    s, t = run_scale(dA, dB, n)
+    so, to = oracle.scale(A, B, n)
+    assert np.array_equal(s.cpu().numpy(), so)
+    assert np.array_equal(t.cpu().numpy(), to)
+    # 2. residue slices
+    a_sl, b_sl = run_quantize(dA, dB, s, t, n)
+    Ap = oracle.truncate(A, so, True)
+    Bp = oracle.truncate(B, to, False)
+    ra = oracle.residues(Ap, n)  # n x M x K
+    rb = oracle.residues(Bp, n)  # n x K x N
+    ga = a_sl.cpu().numpy().view(np.uint16)
+    gb = b_sl.cpu().numpy().view(np.uint16)
+    assert np.array_equal(bf16_to_int(ga[:, :, :K]), ra.astype(np.int64))
+    assert np.array_equal(bf16_to_int(gb[:, :, :K]), rb.transpose(0, 2, 1).astype(np.int64))
+    assert np.all(ga[:, :, K:] == 0) and np.all(gb[:, :, K:] == 0)
+    # 3. per-modulus exact int32 sums, and their reduction mod p
+    raw, cmod = oracle.gemm_mod(ra, rb, n)
+    out32, ld32 = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=1, splits=splits)
+    g32 = out32.cpu().numpy()[:, :, :, :N].astype(np.int64).sum(axis=0)
+    assert np.array_equal(g32, raw.astype(np.int64))
+    out8, ld8 = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
+    assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    # 4. lifted integers, from either representation
+    Xo = oracle.crt(cmod, n)
+    X8 = run_lift(out8, 0, ld8, 1, M, N, n).cpu().numpy().view(np.uint32)
+    assert np.array_equal(X8, Xo)
+    X32 = run_lift(out32, 1, ld32, splits, M, N, n).cpu().numpy().view(np.uint32)
+    assert np.array_equal(X32, Xo)
+    # 5. undo scaling, write double
+    Co = oracle.dgemm(A, B, n)
+    C8 = run_combine(out8, 0, ld8, 1, s, t, M, N, n).cpu().numpy()
+    assert same_bits(C8, Co)
+    C32 = run_combine(out32, 1, ld32, splits, s, t, M, N, n).cpu().numpy()
+    assert same_bits(C32, Co)
+    return Co
+
+
+STAGE_SHAPES = [(1, 1, 1), (7, 5, 3), (128, 256, 64), (129, 257, 65), (256, 256, 256),
+                (300, 200, 1000), (33, 17, 2000), (64, 600, 129)]
+
+
+@pytest.mark.parametrize("M,N,K", STAGE_SHAPES)
+@pytest.mark.parametrize("n", [8, 14, 20])
+def test_stages_bit_exact(M, N, K, n):
+    A, B = inputs(M, N, K, seed=M * 7 + N * 3 + K + n, kind="special")
+    check_stages(A, B, n)
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 11, 17])
+def test_stages_other_moduli_counts(n):
+    K = 40 if n <= 3 else 300
+    if ozk.ozk_beta(K, n) < 1:
+        pytest.skip("too few moduli for K")
+    A, B = inputs(130, 270, K, seed=n, kind="special")
+    check_stages(A, B, n)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_split_k_partials_sum_to_the_exact_product(splits):
+    A, B = inputs(70, 300, 4000, seed=splits)
+    check_stages(A, B, 14, splits=splits)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 700, 3), (513, 1, 77), (256, 256, 256), (129, 257, 1025)])
+@pytest.mark.parametrize("n", [8, 11, 14, 17, 20])
+def test_dgemm_bit_exact(M, N, K, n):
+    A, B = inputs(M, N, K, seed=1 + n, kind="special")
+    assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
+
+
+def test_dgemm_square256_normal_n14():
+    w = workloads.WORKLOADS["square256_normal"]
+    A, B = workloads.workload_operands(w)
+    C = dgemm(A, B, 14)
+    assert same_bits(C, oracle.dgemm(A, B, 14))
+    R = oracle.dot2(A, B)
+    eta = np.max(np.abs(C - R) / (np.abs(A) @ np.abs(B)))
+    assert eta <= 1e-14
+
+
+@pytest.mark.parametrize("n", [14, 8, 11])
+def test_dgemm_square1024_wide(n):
+    w = workloads.WORKLOADS["square1024_wide"]
+    A, B = workloads.workload_operands(w)
+    C = dgemm(A, B, n)
+    assert same_bits(C, oracle.dgemm(A, B, n))
+    R = oracle.dot2(A, B)
+    eta = np.max(np.abs(C - R) / (np.abs(A) @ np.abs(B)))
+    if n >= 14:
+        assert eta <= 1e-14
+    elif n == 11:
+        assert eta <= 2.0**-30
+    else:  # 8 moduli: the a-priori truncation bound
+        s, t = oracle.scale(A, B, n)
+        bound = (np.abs(A).sum(1)[:, None] * np.ldexp(1.0, -t)[None, :]
+                 + np.ldexp(1.0, -s)[:, None] * np.abs(B).sum(0)[None, :]
+                 + w.K * np.ldexp(1.0, -(s[:, None] + t[None, :])))
+        assert np.all(np.abs(C - R) <= bound * (1 + 1e-12) + np.spacing(np.abs(C)))
+
+
+def sample_pairs(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    ii = list(rng.integers(0, M, count))
+    jj = list(rng.integers(0, N, count))
+    for i in {0, 127, 128, M - 1}:
+        for j in {0, 255, 256, N - 1}:
+            if i < M and j < N:
+                ii.append(i)
+                jj.append(j)
+    return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
+
+
+def check_sampled(name, n, count):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.workload_operands(w)
+    dA, dB = dev(A), dev(B)
+    C = ozk.dgemm(dA, dB, n)
+    torch.cuda.synchronize()
+    assert ozk.ozk_stream_status() == 0
+    ii, jj = sample_pairs(w.M, w.N, count, seed=n)
+    Cg = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().numpy()
+    Co, _, _, _ = oracle.sample(A, B, n, ii, jj)
+    assert same_bits(Cg, Co)
+    R, absAB = oracle.dot2_sample(A, B, ii, jj)
+    eta = float(np.max(np.abs(Cg - R) / absAB))
+    if n >= 14:
+        assert eta <= 1e-14
+    elif n == 11:
+        assert eta <= 2.0**-30
+    del dA, dB, C
+    torch.cuda.empty_cache()
+    return eta
+
+
+@pytest.mark.parametrize("n", [14, 8])
+def test_square4096_sampled(n):
+    check_sampled("square4096_normal", n, 384)
+
+
+def test_square8192_sampled():
+    check_sampled("square8192_uniform", 14, 192)
+
+
+@pytest.mark.parametrize("n", [8, 11, 14, 17, 20])
+def test_wide8192_k512_sampled(n):
+    check_sampled("wide8192_k512", n, 384)
+
+
+@pytest.mark.parametrize("n", [8, 11, 14, 17, 20])
+def test_tall512_k65536_sampled(n):
+    check_sampled("tall512_k65536", n, 96)
+
+
+# ----------------------------------------------------------------- edge cases
+def test_empty_and_k0():
+    for (M, N) in [(0, 5), (5, 0), (0, 0)]:
+        A = torch.zeros((M, 3), dtype=torch.float64, device="cuda")
+        B = torch.zeros((3, N), dtype=torch.float64, device="cuda")
+        C = ozk.dgemm(A, B, 14)
+        assert C.shape == (M, N)
+    A = torch.zeros((4, 0), dtype=torch.float64, device="cuda")
+    B = torch.zeros((0, 6), dtype=torch.float64, device="cuda")
+    C = torch.full((4, 6), 5.0, dtype=torch.float64, device="cuda")
+    ozk.ozk_dgemm(4, 6, 0, A, 1, B, 6, C, 6, 14)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+
+
+def test_rejected_arguments():
+    A = torch.ones((4, 8), dtype=torch.float64, device="cuda")
+    B = torch.ones((8, 5), dtype=torch.float64, device="cuda")
+    C = torch.empty((4, 5), dtype=torch.float64, device="cuda")
+    L = ozk.lib()
+    s = ozk._stream(None)
+    p = ctypes.c_void_p
+    call = lambda M, N, K, a, lda, b, ldb, c, ldc, n: L.ozk_dgemm(M, N, K, p(a), lda, p(b), ldb, p(c), ldc, n, s)
+    a, b, c = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    assert call(4, 5, 8, a, 8, b, 5, c, 5, 1) == ozk.OZK_ERR_UNSUPPORTED
+    assert call(4, 5, 8, a, 8, b, 5, c, 5, 21) == ozk.OZK_ERR_UNSUPPORTED
+    assert call(4, 5, 131072, a, 131072, b, 5, c, 5, 14) == ozk.OZK_ERR_UNSUPPORTED
+    assert call(4, 5, 8, a, 7, b, 5, c, 5, 14) == ozk.OZK_ERR_INVALID_ARG      # lda < K
+    assert call(4, 5, 8, a, 8, b, 5, c, 4, 14) == ozk.OZK_ERR_INVALID_ARG      # ldc < N
+    assert call(4, 5, 8, a, 8, b, 5, a, 5, 14) == ozk.OZK_ERR_INVALID_ARG      # C overlaps A
+    assert call(-1, 5, 8, a, 8, b, 5, c, 5, 14) == ozk.OZK_ERR_INVALID_ARG
+    assert call(4, 5, 8, 0, 8, b, 5, c, 5, 14) == ozk.OZK_ERR_INVALID_ARG      # null A
+    assert call(4, 5, 60000, a, 60000, b, 5, c, 5, 2) == ozk.OZK_ERR_UNSUPPORTED  # beta < 1
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    rc = L.ozk_dgemm_ws(4, 5, 8, p(a), 8, p(b), 5, p(c), 5, 14, p(ws.data_ptr()), 16, s)
+    assert rc == ozk.OZK_ERR_WORKSPACE
+    assert ozk.ozk_stream_status() == 0
+
+
+def test_nonfinite_rows_and_columns():
+    A, B = inputs(40, 50, 70, seed=3)
+    A[5, 9] = np.inf
+    A[17, 0] = np.nan
+    B[3, 44] = -np.inf
+    C = dgemm(A, B, 14)
+    Co = oracle.dgemm(A, B, 14)
+    assert same_bits(C, Co)
+    assert np.all(np.isnan(C[5])) and np.all(np.isnan(C[17])) and np.all(np.isnan(C[:, 44]))
+
+
+def test_subnormal_and_overflowing_results():
+    rng = np.random.default_rng(5)
+    A = rng.standard_normal((9, 33))
+    B = rng.standard_normal((33, 11))
+    A[0:3] *= 2.0**-560
+    B[:, 0:4] *= 2.0**-560        # products near 2^-1120: subnormal and underflow
+    A[4:6] *= 2.0**520
+    B[:, 6:8] *= 2.0**510         # products near 2^1030: overflow to inf
+    for n in (8, 14, 20):
+        assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
+
+
+@pytest.mark.parametrize("pad,offset", [(3, 1), (1, 0), (0, 1)])
+def test_strided_and_unaligned_operands(pad, offset):
+    A, B = inputs(65, 130, 97, seed=pad + offset, kind="special")
+    dA, _ba = strided(A, pad, offset)
+    dB, _bb = strided(B, pad + 1, offset)
+    C = torch.empty((65, 130), dtype=torch.float64, device="cuda")
+    ozk.ozk_dgemm(65, 130, 97, dA, ld_of(dA), dB, ld_of(dB), C, 130, 14)
+    torch.cuda.synchronize()
+    assert same_bits(C.cpu().numpy(), oracle.dgemm(A, B, 14))
+
+
+def test_caller_workspace_and_host_buffers_agree():
+    A, B = inputs(200, 300, 500, seed=9)
+    C0 = dgemm(A, B, 14)
+    dA, dB = dev(A), dev(B)
+    need = ozk.ozk_workspace_size(200, 300, 500, 14)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    C1 = torch.empty((200, 300), dtype=torch.float64, device="cuda")
+    ozk.ozk_dgemm_ws(200, 300, 500, dA, 500, dB, 300, C1, 300, 14, ws, need)
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((200, 300), dtype=torch.float64).pin_memory()
+    ozk.ozk_dgemm_host(200, 300, 500, hA, 500, hB, 300, hC, 300, 14)
+    torch.cuda.synchronize()
+    assert same_bits(C1.cpu().numpy(), C0)
+    assert same_bits(hC.numpy(), C0)
+    assert ozk.ozk_stream_status() == 0
+
+
+def test_deterministic_and_stream_ordered():
+    A, B = inputs(300, 700, 900, seed=4)
+    dA, dB = dev(A), dev(B)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        C1 = ozk.dgemm(dA, dB, 14, stream=st)
+        C2 = ozk.dgemm(dA, dB, 14, stream=st)
+    st.synchronize()
+    assert torch.equal(C1.view(torch.int64), C2.view(torch.int64))
+    assert ozk.ozk_stream_status(st) == 0
