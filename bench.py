@@ -218,20 +218,23 @@ def run_reference(args, ranks: Ranks):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config(w),
+        "data": "synthetic", "config": config(w, N_MODULI),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def config(w):
+def config(w, n):
     from fp64_gemm_emulation_exponent_gb300 import ozk
 
-    return {"workload": f"{w.name}: M=N=K={w.K}, A,B i.i.d. N(0,1) seeded 1002/2002, "
-                        f"{N_MODULI} moduli (beta={ozk.ozk_beta(w.K, N_MODULI)} bits per operand)",
-            "M": w.M, "N": w.N, "K": w.K, "n_moduli": N_MODULI,
-            "l2": "inputs larger than L2 (A+B = 268 MB fp64; residue slices 940 MB per step)",
+    ab = 8 * (w.M * w.K + w.K * w.N)
+    sl = 2 * n * (w.M + w.N) * ozk.ozk_kpad(w.K)
+    return {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K}, A,B i.i.d. {w.dist} seeded "
+                        f"{1000 + w.seed}/{2000 + w.seed}, {n} moduli "
+                        f"(beta={ozk.ozk_beta(w.K, n)} bits per operand)",
+            "M": w.M, "N": w.N, "K": w.K, "n_moduli": n,
+            "l2": f"inputs larger than L2 (A+B = {ab / 1e6:.0f} MB fp64; residue slices {sl / 1e6:.0f} MB per step)",
             "parallelism": "replicas (one independent GEMM per GPU)"}
 
 
@@ -241,8 +244,8 @@ def run_gpu(args, ranks: Ranks):
     from fp64_gemm_emulation_exponent_gb300 import ozk
 
     torch.cuda.set_device(ranks.local)
-    w = workloads.WORKLOADS[WORKLOAD]
-    M, N, K, n = w.M, w.N, w.K, N_MODULI
+    w = workloads.WORKLOADS[args.workload]
+    M, N, K, n = w.M, w.N, w.K, args.moduli
     A, B = workloads.workload_operands(w)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()
@@ -316,7 +319,7 @@ def run_gpu(args, ranks: Ranks):
         "bound": "tensor", "kernel": "residue_gemm (tcgen05 kind::f16, bf16-exact residues)",
         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
         "peak_source": f"bf16_tflops_sustained, {pk['source']}",
-        "traffic": committed_traffic(WORKLOAD),
+        "traffic": committed_traffic(f"{w.name}/n{n}"),
         "algorithmic": f"2*M*N*K*n = {algo_flops:.4g} flop per launch",
     }
     hbm = pk["hbm_gbs"]
@@ -330,12 +333,12 @@ def run_gpu(args, ranks: Ranks):
 
     line = None
     if ranks.rank == 0:
-        cpu = cpu_baseline(A, B, n) if ranks.world == 1 else None
+        cpu = cpu_baseline(A, B, n) if (ranks.world == 1 and not args.no_cpu_baseline) else None
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ranks.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config(w),
+            "data": "synthetic", "config": config(w, n),
             "tensor_path": "residues in [-128,127] as bf16 on tcgen05 kind::f16 (sm_103a has no kind::i8); "
                            "fp32 TMEM sums exact per 256-term chunk",
             "int8_equiv_tops_issued": algo_flops / gemm_s / 1e12,
@@ -357,6 +360,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ozk", choices=["ozk", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS),
+                    help="GEMM shape to time (the headline line uses the default)")
+    ap.add_argument("--moduli", type=int, default=N_MODULI)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     ranks = Ranks(world)

@@ -5,7 +5,8 @@
 // double load, exponent scaling, round, mod, balanced int8 conversion).
 //
 // All arithmetic on the operands is integer work on IEEE-754 bit patterns:
-// GB300's FP64 pipe is slow, and truncation of m * 2^sh is a shift.
+// GB300's FP64 pipe is slow, and rounding m * 2^sh to an integer is a shift
+// plus a rounding increment.
 #include "ozk_internal.h"
 
 namespace ozk {
@@ -121,15 +122,16 @@ __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_
 
 // ---------------------------------------------------------------------------
 // Quantisation.  x = (-1)^neg m 2^e exactly (m < 2^53); with sh = e + s the
-// truncated integer is |a'| = floor(m 2^sh) < 2^beta <= 2^72, held as five
-// 16-bit limbs.  Its residue mod p is sum_j L_j (2^16j mod p) reduced once.
+// integer is |a'| = m 2^sh rounded to nearest, ties to even (a shift and a
+// rounding increment), |a'| <= 2^beta <= 2^72, held as five 16-bit limbs.
+// Its residue mod p is sum_j L_j (2^16j mod p) reduced once.
 // ---------------------------------------------------------------------------
 struct Scaled {
   uint32_t l0, l1, l2, l3, l4;  // |a'| = l0 + l1 2^16 + l2 2^32 + l3 2^48 + l4 2^64
   uint32_t neg;
 };
 
-__device__ __forceinline__ Scaled scale_truncate(double x, int32_t sc) {
+__device__ __forceinline__ Scaled scale_round(double x, int32_t sc) {
   const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(x));
   const uint32_t ex = static_cast<uint32_t>(bits >> 52) & 0x7FFu;
   uint64_t m = bits & 0xFFFFFFFFFFFFFull;
@@ -143,10 +145,17 @@ __device__ __forceinline__ Scaled scale_truncate(double x, int32_t sc) {
   } else if (sh > 0) {
     lo = m << sh;
     hi = static_cast<uint32_t>(m >> (64 - sh));
-  } else if (sh > -64) {
-    lo = m >> (-sh);
+  } else if (sh == 0) {
+    lo = m;
     hi = 0;
-  } else {
+  } else if (sh > -64) {
+    const int r = -sh;  // 1..63 dropped bits
+    const uint64_t q = m >> r;
+    const uint64_t rem = m & ((1ull << r) - 1);
+    const uint64_t half = 1ull << (r - 1);
+    lo = q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);
+    hi = 0;
+  } else {  // m 2^sh < 2^-11: rounds to 0
     lo = 0;
     hi = 0;
   }
@@ -161,6 +170,7 @@ __device__ __forceinline__ Scaled scale_truncate(double x, int32_t sc) {
 }
 
 // Balanced residue of (-1)^neg |a'| modulo the k-th modulus, in [-128, 127].
+// x below stays under 2^16 + 3 * 2^16 * 255 + 2^9 * 255 < 2^26.
 template <int k>
 __device__ __forceinline__ int balanced_residue(const Scaled& a) {
   constexpr uint32_t p = modulus_at(k);
@@ -171,7 +181,7 @@ __device__ __forceinline__ int balanced_residue(const Scaled& a) {
   } else {
     constexpr uint32_t c1 = pow2_mod(16, p), c2 = pow2_mod(32, p), c3 = pow2_mod(48, p),
                        c4 = pow2_mod(64, p), mg = magic_of(p);
-    const uint32_t x = a.l0 + a.l1 * c1 + a.l2 * c2 + a.l3 * c3 + a.l4 * c4;  // < 2^26
+    const uint32_t x = a.l0 + a.l1 * c1 + a.l2 * c2 + a.l3 * c3 + a.l4 * c4;
     const uint32_t q = __umulhi(x, mg);
     int r = static_cast<int>(x - q * p);
     r += r < 0 ? static_cast<int>(p) : 0;                        // |a'| mod p
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(256) quantize_a_kernel(const double* __restric
   }
   Scaled x[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) x[e] = scale_truncate(v[e], sc);
+  for (int e = 0; e < 8; ++e) x[e] = scale_round(v[e], sc);
   uint4* dst = reinterpret_cast<uint4*>(out + row * kpad + k0);
   const int64_t plane = (M * kpad) >> 3;  // uint4 per modulus slice
   static_for<0, kMaxModuli>([&](auto kc) {
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(256) quantize_b_kernel(const double* __restric
   for (int r = 0; r < 8; ++r) {
     const int64_t k = k0 + kr + 8 * r;
     const double v = (live && k < K) ? __ldcs(B + k * ldb + j) : 0.0;
-    x[r] = scale_truncate(v, sc);
+    x[r] = scale_round(v, sc);
   }
   static_for<0, kMaxModuli>([&](auto kc) {
     constexpr int k = decltype(kc)::value;

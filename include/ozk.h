@@ -141,7 +141,8 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
 
 /* Residue quantisation of A ("double load, exponent scaling, round, mod,
  * balanced int8 conversion").  For each modulus p and element:
- * a'_ik = trunc(a_ik 2^s_i) and r = sym(a' mod p) in [-floor(p/2), ceil(p/2)-1],
+ * a'_ik = a_ik 2^s_i rounded to the nearest integer (ties to even) and
+ * r = sym(a' mod p) in [-floor(p/2), ceil(p/2)-1],
  * stored as bfloat16 (exact for these integers) at
  * a_slices[(p * M + i) * kpad + k]; columns K..kpad-1 are zero.
  * kpad = ozk_kpad(K).  Rows with s_i = OZK_SCALE_NONFINITE are zero. */

@@ -29,7 +29,7 @@ def lib():
             "ozk_ref_moduli": [i32, vp],
             "ozk_ref_beta": [i64, i32],
             "ozk_ref_scale": [i64, i64, i64, vp, i64, vp, i64, i32, vp, vp],
-            "ozk_ref_truncate": [i64, i64, vp, i64, vp, i32, vp],
+            "ozk_ref_integers": [i64, i64, vp, i64, vp, i32, vp],
             "ozk_ref_residues": [i64, vp, i32, vp],
             "ozk_ref_gemm_mod": [i64, i64, i64, vp, vp, i32, vp, vp],
             "ozk_ref_crt": [i64, i32, vp, vp],
@@ -92,12 +92,14 @@ def scale(A, B, n):
     return s, t
 
 
-def truncate(X, sc, by_row):
+def integers(X, sc, by_row):
+    """X * 2^scale rounded to nearest integers (ties to even), as exact float64."""
     X = _f64(X)
     rows, cols = X.shape
     sc = np.ascontiguousarray(sc, dtype=np.int32)
     out = np.zeros((rows, cols), dtype=np.float64)
-    _check(lib().ozk_ref_truncate(rows, cols, _p(X), X.strides[0] // 8, _p(sc), 1 if by_row else 0, _p(out)), "truncate")
+    _check(lib().ozk_ref_integers(rows, cols, _p(X), X.strides[0] // 8, _p(sc), 1 if by_row else 0, _p(out)),
+           "integers")
     return out
 
 

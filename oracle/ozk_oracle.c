@@ -146,9 +146,10 @@ static int ceil_log2_i64(int64_t K) {
   return c;
 }
 
-/* Reading R2: |a'|, |b'| < 2^beta gives |sum_k a'b'| < K 2^(2 beta); choosing
- * 2 beta <= floor(log2 P) - 1 - ceil(log2 K) makes that at most P/2, so the
- * symmetric CRT lift recovers the product exactly. */
+/* Reading R2: |a'|, |b'| <= 2^beta gives |sum_k a'b'| <= K 2^(2 beta); choosing
+ * 2 beta <= floor(log2 P) - 1 - ceil(log2 K) makes that at most
+ * 2^floor(log2 P) / 2 < P/2 (P is never a power of two), so the symmetric
+ * CRT lift recovers the product exactly. */
 int ozk_ref_beta(int64_t K, int n) {
   if (n < 2 || n > OZK_REF_NMAX) return OZK_REF_EUNSUPPORTED;
   if (K < 1) K = 1;
@@ -186,21 +187,23 @@ int ozk_ref_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
 }
 
 /* ------------------------------------------------------------------------- */
-/* Step 2: truncation to integers (reading R3: toward zero, exact)           */
+/* Step 2: exponent scaling and rounding to integers ("exponent scaling,     */
+/* round"; reading: to nearest, ties to even)                                */
 /* ------------------------------------------------------------------------- */
-static double trunc_scaled(double x, int32_t sc) {
+static double round_scaled_int(double x, int32_t sc) {
   if (sc == OZK_REF_NONFINITE) return 0.0;
-  /* |x 2^sc| < 2^beta: the scaling is exact wherever the result is >= 1, and
-   * anything below 1 truncates to 0 whatever ldexp rounds it to. */
-  return trunc(ldexp(x, sc));
+  /* |x 2^sc| < 2^beta: the scaling is exact wherever the result is >= 1/2,
+   * and anything smaller rounds to 0 whatever ldexp rounds it to.  nearbyint
+   * rounds in the default mode: to nearest, ties to even. */
+  return nearbyint(ldexp(x, sc));
 }
 
-int ozk_ref_truncate(int64_t rows, int64_t cols, const double* X, int64_t ld,
+int ozk_ref_integers(int64_t rows, int64_t cols, const double* X, int64_t ld,
                      const int32_t* scale, int by_row, double* out) {
   if (rows < 0 || cols < 0) return OZK_REF_EINVAL;
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c)
-      out[r * cols + c] = trunc_scaled(X[r * ld + c], by_row ? scale[r] : scale[c]);
+      out[r * cols + c] = round_scaled_int(X[r * ld + c], by_row ? scale[r] : scale[c]);
   return OZK_REF_OK;
 }
 
@@ -376,9 +379,9 @@ int ozk_ref_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
     goto done;
   }
   ozk_ref_scale(M, N, K, A, lda, B, ldb, n, s, t);
-  ozk_ref_truncate(M, K, A, lda, s, 1, Ap);
+  ozk_ref_integers(M, K, A, lda, s, 1, Ap);
   for (int64_t j = 0; j < N; ++j)
-    for (int64_t q = 0; q < K; ++q) Bt[j * K + q] = trunc_scaled(B[q * ldb + j], t[j]);
+    for (int64_t q = 0; q < K; ++q) Bt[j * K + q] = round_scaled_int(B[q * ldb + j], t[j]);
   ozk_ref_residues(M * K, Ap, n, ra);
   ozk_ref_residues(N * K, Bt, n, rbt);
 
@@ -446,8 +449,8 @@ int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     bigi xd, prod, xc;
     big_set_u32(&xd, 0);
     for (int64_t k = 0; k < K; ++k) {
-      double ap = trunc_scaled(arow[k], si);
-      double bp = trunc_scaled(bcol[k * ldb], tj);
+      double ap = round_scaled_int(arow[k], si);
+      double bp = round_scaled_int(bcol[k * ldb], tj);
       for (int p = 0; p < n; ++p)
         acc[p] += (int64_t)sym_residue(ap, MODULI[p]) * (int64_t)sym_residue(bp, MODULI[p]);
       big_mul_i128(&prod, (__int128)ap, (__int128)bp);

@@ -42,7 +42,7 @@ enum {
 int ozk_ref_moduli(int n, int32_t* out);
 
 /* Bit budget beta per operand (reading R2): the largest even split of
- * floor(log2 P) - 1 - ceil(log2 K) bits, so that 2*K*2^(2*beta) <= P.
+ * floor(log2 P) - 1 - ceil(log2 K) bits, so that 2*K*2^(2*beta) < P.
  * Returns beta, or OZK_REF_EUNSUPPORTED when beta < 1. */
 int ozk_ref_beta(int64_t K, int n);
 
@@ -52,10 +52,11 @@ int ozk_ref_beta(int64_t K, int n);
 int ozk_ref_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                   const double* B, int64_t ldb, int n, int32_t* s, int32_t* t);
 
-/* Truncation toward zero of x * 2^scale (exact).  by_row != 0: scale[r] applies
- * to row r; otherwise scale[c] applies to column c.  out is rows x cols dense.
+/* x * 2^scale rounded to the nearest integer, ties to even (the page's
+ * "exponent scaling, round").  by_row != 0: scale[r] applies to row r;
+ * otherwise scale[c] applies to column c.  out is rows x cols dense.
  * Entries whose scale is OZK_REF_NONFINITE give 0. */
-int ozk_ref_truncate(int64_t rows, int64_t cols, const double* X, int64_t ld,
+int ozk_ref_integers(int64_t rows, int64_t cols, const double* X, int64_t ld,
                      const int32_t* scale, int by_row, double* out);
 
 /* Balanced residues: out[p*count + e] = sym(xp[e] mod p_p), in

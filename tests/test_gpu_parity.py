@@ -51,8 +51,8 @@ def check_stages(A, B, n, splits=1):
     assert np.array_equal(t.cpu().numpy(), to)
     # 2. residue slices
     a_sl, b_sl = run_quantize(dA, dB, s, t, n)
-    Ap = oracle.truncate(A, so, True)
-    Bp = oracle.truncate(B, to, False)
+    Ap = oracle.integers(A, so, True)
+    Bp = oracle.integers(B, to, False)
     ra = oracle.residues(Ap, n)  # n x M x K
     rb = oracle.residues(Bp, n)  # n x K x N
     ga = a_sl.cpu().numpy().view(np.uint16)
@@ -137,11 +137,11 @@ def test_dgemm_square1024_wide(n):
         assert eta <= 1e-14
     elif n == 11:
         assert eta <= 2.0**-30
-    else:  # 8 moduli: the a-priori truncation bound
+    else:  # 8 moduli: the a-priori rounding bound
         s, t = oracle.scale(A, B, n)
-        bound = (np.abs(A).sum(1)[:, None] * np.ldexp(1.0, -t)[None, :]
-                 + np.ldexp(1.0, -s)[:, None] * np.abs(B).sum(0)[None, :]
-                 + w.K * np.ldexp(1.0, -(s[:, None] + t[None, :])))
+        bound = (np.abs(A).sum(1)[:, None] * np.ldexp(1.0, -t - 1)[None, :]
+                 + np.ldexp(1.0, -s - 1)[:, None] * np.abs(B).sum(0)[None, :]
+                 + w.K * np.ldexp(1.0, -(s[:, None] + t[None, :] + 2)))
         assert np.all(np.abs(C - R) <= bound * (1 + 1e-12) + np.spacing(np.abs(C)))
 
 

@@ -4,7 +4,7 @@ Every check here ties the oracle to something other than itself: exact
 rational arithmetic (``fractions.Fraction``), Python big-integer brute force on
 tiny inputs, the defining properties of the Chinese Remainder Theorem, closed
 forms, exact invariants of the method, and the a-priori error bound that
-follows from truncating each operand by less than one unit.
+follows from rounding each scaled operand to the nearest integer.
 
 Method: Ozaki scheme II as described on the "Day 12" page
 (ithelp.ithome.com.tw), section "Profile 不能只看 Tensor Core" (stage list) and
@@ -42,13 +42,13 @@ def bf_scale(vec, beta):
     return beta - math.frexp(amax)[1]
 
 
-def bf_trunc(x, s):
+def bf_round(x, s):
     if s == oracle.NONFINITE:
         return 0
-    return int(Fraction(x) * Fraction(2) ** s)  # int() of a Fraction truncates toward 0
+    return round(Fraction(x) * Fraction(2) ** s)  # Fraction rounds half to even
 
 
-def bf_round(X, S):
+def bf_unscale(X, S):
     """Correctly rounded X * 2^-S (CPython int/int true division is correctly rounded)."""
     if X == 0:
         return 0.0
@@ -71,8 +71,8 @@ def bf_method(A, B, n):
     beta = oracle.beta(K, n)
     s = [bf_scale(list(A[i, :]), beta) for i in range(M)]
     t = [bf_scale(list(B[:, j]), beta) for j in range(N)]
-    Ap = [[bf_trunc(float(A[i, k]), s[i]) for k in range(K)] for i in range(M)]
-    Bp = [[bf_trunc(float(B[k, j]), t[j]) for j in range(N)] for k in range(K)]
+    Ap = [[bf_round(float(A[i, k]), s[i]) for k in range(K)] for i in range(M)]
+    Bp = [[bf_round(float(B[k, j]), t[j]) for j in range(N)] for k in range(K)]
     X = [[sum(Ap[i][k] * Bp[k][j] for k in range(K)) for j in range(N)] for i in range(M)]
     C = np.zeros((M, N))
     for i in range(M):
@@ -80,7 +80,7 @@ def bf_method(A, B, n):
             if s[i] == oracle.NONFINITE or t[j] == oracle.NONFINITE:
                 C[i, j] = math.nan
             else:
-                C[i, j] = bf_round(X[i][j], s[i] + t[j])
+                C[i, j] = bf_unscale(X[i][j], s[i] + t[j])
     return C, X, s, t, Ap, Bp
 
 
@@ -139,7 +139,7 @@ def test_beta_values_at_the_workloads():
 
 
 # --------------------------------------------------------------------------
-# Stage 1 + 2: exponent scan and truncation
+# Stage 1 + 2: exponent scan, scaling and rounding to integers
 # --------------------------------------------------------------------------
 def special_matrix(rng, rows, cols):
     X = rng.standard_normal((rows, cols))
@@ -160,12 +160,12 @@ def test_scale_matches_frexp_and_uses_the_top_bit(n):
     beta = oracle.beta(9, n)
     assert list(s) == [bf_scale(list(A[i]), beta) for i in range(7)]
     assert list(t) == [bf_scale(list(B[:, j]), beta) for j in range(5)]
-    Ap = oracle.truncate(A, s, True)
+    Ap = oracle.integers(A, s, True)
     for i in range(7):
         top = max(abs(int(v)) for v in Ap[i])
         if np.any(A[i] != 0):
-            # |a'| < 2^beta, and the largest entry keeps its leading bit
-            assert 2 ** (beta - 1) <= top < 2 ** beta
+            # |a'| <= 2^beta, and the largest entry keeps its leading bit
+            assert 2 ** (beta - 1) <= top <= 2 ** beta
         else:
             assert top == 0
 
@@ -181,26 +181,29 @@ def test_scale_flags_nonfinite_rows_and_columns():
     assert [int(v) == oracle.NONFINITE for v in t] == [False] * 4 + [True]
 
 
-def test_truncation_is_exact_toward_zero():
+def test_rounding_to_nearest_integer_ties_to_even():
     rng = np.random.default_rng(5)
     X = special_matrix(rng, 6, 8)
     X[4, :] = -X[4, :]
+    X[5, :] = [0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.25, -7.75]  # exact ties at scale 0
     # scales keep |x 2^s| below 2^73, as the exponent scan guarantees
-    sc = np.array([50, 1100, -950, 3, 60, 17], dtype=np.int32)
-    out = oracle.truncate(X, sc, True)
+    sc = np.array([50, 1100, -950, 3, 60, 0], dtype=np.int32)
+    out = oracle.integers(X, sc, True)
     for r in range(6):
         for c in range(8):
             exact = Fraction(float(X[r, c])) * Fraction(2) ** int(sc[r])
             v = int(out[r, c])
-            assert out[r, c] == v and v == bf_trunc(float(X[r, c]), int(sc[r]))
-            assert abs(Fraction(v)) <= abs(exact) < abs(Fraction(v)) + 1
-            assert v == 0 or (v > 0) == (exact > 0)
+            assert out[r, c] == v and v == bf_round(float(X[r, c]), int(sc[r]))
+            assert abs(exact - v) <= Fraction(1, 2)
+            if abs(exact - v) == Fraction(1, 2):
+                assert v % 2 == 0
+    assert list(out[5]) == [0, 2, 2, 0, -2, -2, 3, -8]
     Y = rng.standard_normal((6, 8))
     colsc = np.array([10, 20, 30, 40, 50, 1, 2, 3], dtype=np.int32)
-    outc = oracle.truncate(Y, colsc, False)
+    outc = oracle.integers(Y, colsc, False)
     for r in range(6):
         for c in range(8):
-            assert int(outc[r, c]) == bf_trunc(float(Y[r, c]), int(colsc[c]))
+            assert int(outc[r, c]) == bf_round(float(Y[r, c]), int(colsc[c]))
 
 
 # --------------------------------------------------------------------------
@@ -278,11 +281,11 @@ def test_crt_satisfies_the_defining_congruences(n):
 
 
 def test_crt_recovers_extreme_products():
-    # values right at the edge of what beta allows: +-(K (2^beta - 1)^2)
+    # values right at the edge of what beta allows: +-K 2^(2 beta)
     for n in (8, 14, 20):
         K = 512
         beta = oracle.beta(K, n)
-        vals = [K * (2**beta - 1) ** 2, -K * (2**beta - 1) ** 2, 1, -1, 0]
+        vals = [K * 4**beta, -K * 4**beta, K * 4**beta - 1, 1, -1, 0]
         cm = np.array([[v % p for v in vals] for p in MODULI_ALL[:n]], dtype=np.uint8)
         assert oracle.limbs_to_int(oracle.crt(cm, n)) == vals
 
@@ -315,7 +318,7 @@ def test_round_is_correctly_rounded():
     S = np.array([s for _, s in cases], dtype=np.int32)
     out = oracle.round_scaled(X, S)
     for (x, s), got in zip(cases, out):
-        want = bf_round(x, s)
+        want = bf_unscale(x, s)
         assert np.float64(got).view(np.uint64) == np.float64(want).view(np.uint64), (x, s, got, want)
 
 
@@ -361,8 +364,9 @@ def exact_product(A, B):
 
 
 @pytest.mark.parametrize("n", [6, 8, 11, 14, 20])
-def test_dgemm_within_the_truncation_error_bound(n):
-    # |C - AB| < 2^-t sum|a| + 2^-s sum|b| + K 2^-(s+t), plus half an ulp of C
+def test_dgemm_within_the_rounding_error_bound(n):
+    # a' = a 2^s - da, |da| <= 1/2: |C - AB| <= 2^-(t+1) sum|a| + 2^-(s+1) sum|b|
+    # + K 2^-(s+t+2), plus half an ulp of C
     rng = np.random.default_rng(7 * n)
     M, N, K = 6, 5, 40
     A, B = tiny_case(rng, M, N, K, "wide")
@@ -374,7 +378,8 @@ def test_dgemm_within_the_truncation_error_bound(n):
             sa = sum(Fraction(abs(float(A[i, k]))) for k in range(K))
             sb = sum(Fraction(abs(float(B[k, j]))) for k in range(K))
             two = Fraction(2)
-            bound = two ** -int(t[j]) * sa + two ** -int(s[i]) * sb + K * two ** -(int(s[i]) + int(t[j]))
+            bound = (two ** -(int(t[j]) + 1) * sa + two ** -(int(s[i]) + 1) * sb
+                     + K * two ** -(int(s[i]) + int(t[j]) + 2))
             half_ulp = Fraction(math.ulp(float(C[i, j]))) / 2
             assert abs(Fraction(float(C[i, j])) - ex[i][j]) <= bound + half_ulp
 
@@ -414,11 +419,11 @@ def test_k1_is_the_correctly_rounded_outer_product():
     rng = np.random.default_rng(8)
     a = rng.standard_normal((13, 1)) * 2.0 ** rng.integers(-30, 30, (13, 1))
     b = rng.standard_normal((1, 11)) * 2.0 ** rng.integers(-30, 30, (1, 11))
-    # beta(1, 14) = 54 >= 53: nothing is truncated, and a*b is one IEEE product
+    # beta(1, 14) = 54 >= 53: no bit is rounded away, and a*b is one IEEE product
     assert same_bits(oracle.dgemm(a, b, 14), a * b)
 
 
-def test_twenty_moduli_without_truncation_round_the_exact_product():
+def test_twenty_moduli_without_lost_bits_round_the_exact_product():
     # beta = 72 at K = 512: rows/columns spanning <= 2^19 lose no bit, so C is
     # the correctly rounded exact product
     rng = np.random.default_rng(31)
@@ -484,7 +489,7 @@ def test_tolerances_of_the_moduli_counts():
     # 8 moduli give beta = 26 at K = 512: check the a-priori bound instead
     C8 = oracle.dgemm(A, B, 8)
     s, t = oracle.scale(A, B, 8)
-    bound = (np.ldexp(np.abs(A).sum(1)[:, None], 0) * np.ldexp(1.0, -t)[None, :]
-             + np.ldexp(1.0, -s)[:, None] * np.abs(B).sum(0)[None, :]
-             + 512 * np.ldexp(1.0, -(s[:, None] + t[None, :])))
+    bound = (np.abs(A).sum(1)[:, None] * np.ldexp(1.0, -t - 1)[None, :]
+             + np.ldexp(1.0, -s - 1)[:, None] * np.abs(B).sum(0)[None, :]
+             + 512 * np.ldexp(1.0, -(s[:, None] + t[None, :] + 2)))
     assert np.all(np.abs(C8 - R) <= bound * (1 + 1e-12) + np.spacing(np.abs(C8)))
