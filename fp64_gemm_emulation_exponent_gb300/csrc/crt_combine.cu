@@ -5,14 +5,14 @@
 // that more registers per thread made it slower; on GB300 the FP64 pipe is
 // slow, so this kernel is integer-only:
 //
-//   X = sum_k y_k (P/p_k) - q P,  y_k = c_k w_k,  w_k = (P/p_k)^-1 mod p_k,
+//   X = sum_k c_k e_k - q P,  e_k = (P/p_k) ((P/p_k)^-1 mod p_k),
 //
-// with y_k left unreduced (< 2^16), the limb sums accumulated in 64 bits
-// without carries, and q = round(sum_k y_k / p_k) estimated in 32.32 fixed
-// point (error < 2^20 / 2^32); the rare outputs whose estimate lies within
-// 2^21 of a rounding boundary get an exact correction.  The lifted X in
-// [-P/2, P/2) is then scaled by 2^-(s_i + t_j) and rounded to nearest-even in
-// integer arithmetic (subnormals and overflow included).
+// with the column sums of c_k e_k accumulated in 64 bits without carries, and
+// q = round(sum_k c_k w_k / p_k) estimated in 32.32 fixed point (error below
+// 2^12 / 2^32); the rare outputs whose estimate lies within 2^14 / 2^32 of a
+// rounding boundary get an exact correction.  The lifted X in [-P/2, P/2) is
+// then scaled by 2^-(s_i + t_j) and rounded to nearest-even in integer
+// arithmetic (subnormals and overflow included).
 #include "ozk_internal.h"
 
 namespace ozk {
@@ -138,8 +138,16 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&X)[NL], i
   return bits | (static_cast<uint64_t>(neg) << 63);
 }
 
+__device__ __forceinline__ void store4_f64(double* dst, const uint64_t (&b)[4]) {
+  asm volatile("st.global.cs.v4.b64 [%0], {%1, %2, %3, %4};" ::"l"(dst), "l"(b[0]), "l"(b[1]), "l"(b[2]),
+               "l"(b[3])
+               : "memory");
+}
+
 // One thread per 4 consecutive columns of one row.
 //  IN_KIND 0: uint8 residues [n][M][ldi];  1: int32 partial sums [splits][n][M][ldi].
+// All residue words are loaded before any arithmetic so that the loads of a
+// thread are in flight together.
 template <int NL, int IN_KIND, bool LIMBS>
 __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, int64_t ldi,
                                                   int64_t M, int64_t N, int splits,
@@ -154,64 +162,81 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
   const int64_t j0 = (g - i * groups) * 4;
   const int n = K.n;
 
-  uint64_t acc[4][NL];
-  uint64_t qacc[4];
-#pragma unroll
-  for (int o = 0; o < 4; ++o) {
-    qacc[o] = 0;
-#pragma unroll
-    for (int l = 0; l < NL; ++l) acc[o][l] = 0;
-  }
-
-  static_for<0, kMaxModuli>([&](auto kc) {
-    constexpr int k = decltype(kc)::value;
-    if (k < n) {
-      uint32_t c[4];
-      if constexpr (IN_KIND == 0) {
-        const uint8_t* plane = static_cast<const uint8_t*>(in) + (static_cast<int64_t>(k) * M + i) * ldi + j0;
-        const uint32_t w4 = __ldcs(reinterpret_cast<const unsigned int*>(plane));
-#pragma unroll
-        for (int o = 0; o < 4; ++o) c[o] = (w4 >> (8 * o)) & 0xFFu;
-      } else {
+  // canonical residues of the 4 outputs, 4 bytes per modulus
+  uint32_t cw[kMaxModuli];
+  if constexpr (IN_KIND == 0) {
+    const uint8_t* base = static_cast<const uint8_t*>(in) + i * ldi + j0;
+    const int64_t plane = M * ldi;
+    static_for<0, kMaxModuli>([&](auto kc) {
+      constexpr int k = decltype(kc)::value;
+      if (k < n) cw[k] = __ldcs(reinterpret_cast<const unsigned int*>(base + k * plane));
+    });
+  } else {
+    static_for<0, kMaxModuli>([&](auto kc) {
+      constexpr int k = decltype(kc)::value;
+      if (k < n) {
         int32_t sum[4] = {0, 0, 0, 0};
         for (int sp = 0; sp < splits; ++sp) {
-          const int32_t* row = static_cast<const int32_t*>(in) +
-                               ((static_cast<int64_t>(sp) * n + k) * M + i) * ldi + j0;
-          const int4 v = __ldcs(reinterpret_cast<const int4*>(row));
+          const int4 v = __ldcs(reinterpret_cast<const int4*>(static_cast<const int32_t*>(in) +
+                                                              ((static_cast<int64_t>(sp) * n + k) * M + i) * ldi + j0));
           sum[0] += v.x;
           sum[1] += v.y;
           sum[2] += v.z;
           sum[3] += v.w;
         }
-#pragma unroll
-        for (int o = 0; o < 4; ++o) c[o] = mod_p(sum[o], K.p[k], K.magic[k], K.bias[k]);
+        cw[k] = mod_p(sum[0], K.p[k], K.magic[k], K.bias[k]) |
+                (mod_p(sum[1], K.p[k], K.magic[k], K.bias[k]) << 8) |
+                (mod_p(sum[2], K.p[k], K.magic[k], K.bias[k]) << 16) |
+                (mod_p(sum[3], K.p[k], K.magic[k], K.bias[k]) << 24);
       }
+    });
+  }
+  int32_t si = 0;
+  int32_t tj[4] = {0, 0, 0, 0};
+  if constexpr (!LIMBS) {
+    si = s[i];
+    if (j0 + 3 < N) {
+      const int4 t4 = *reinterpret_cast<const int4*>(t + j0);
+      tj[0] = t4.x;
+      tj[1] = t4.y;
+      tj[2] = t4.z;
+      tj[3] = t4.w;
+    } else {
 #pragma unroll
-      for (int o = 0; o < 4; ++o) {
-        const uint32_t y = c[o] * K.w[k];  // < 2^16
-        qacc[o] += static_cast<uint64_t>(y) * K.r32[k];
-#pragma unroll
-        for (int l = 0; l < NL; ++l) acc[o][l] += static_cast<uint64_t>(y) * K.Mk[k][l];
-      }
+      for (int o = 0; o < 4; ++o) tj[o] = (j0 + o < N) ? t[j0 + o] : 0;
     }
-  });
+  }
 
-  const int32_t si = s ? s[i] : 0;
+  uint64_t outbits[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int o = 0; o < 4; ++o) {
-    const int64_t j = j0 + o;
-    if (j >= N) break;
-    // S = sum_k y_k P/p_k as NL 32-bit limbs
+    // S = sum_k c_k e_k (64-bit column sums, carries later) and
+    // q ~ S / P = sum_k c_k w_k / p_k in 32.32 fixed point
+    uint64_t acc[NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) acc[l] = 0;
+    uint64_t qacc = 0;
+    static_for<0, kMaxModuli>([&](auto kc) {
+      constexpr int k = decltype(kc)::value;
+      if (k < n) {
+        const uint32_t c = __byte_perm(cw[k], 0u, 0x4440 + o);
+        qacc += static_cast<uint64_t>(c) * K.frac[k];
+#pragma unroll
+        for (int l = 0; l < NL; ++l) acc[l] += static_cast<uint64_t>(c) * K.e[k][l];
+      }
+    });
     uint32_t X[NL];
     uint64_t carry = 0;
 #pragma unroll
     for (int l = 0; l < NL; ++l) {
-      const uint64_t v = acc[o][l] + carry;
+      const uint64_t v = acc[l] + carry;
       X[l] = static_cast<uint32_t>(v);
       carry = v >> 32;
     }
-    // q = round(S / P) from the fixed-point estimate; X = S - q P
-    const uint64_t shifted = qacc[o] + 0x80000000ull;
+    // X = S - q P with q = round(S / P); the estimate is off by less than
+    // 2^12 / 2^32, so only outputs within 2^14 / 2^32 of a rounding boundary
+    // need the exact check
+    const uint64_t shifted = qacc + 0x80000000ull;
     const uint32_t q = static_cast<uint32_t>(shifted >> 32);
     const uint32_t frac = static_cast<uint32_t>(shifted);
     uint64_t borrow = 0;
@@ -222,21 +247,30 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
       borrow = (sub >> 32) + (X[l] < lo ? 1u : 0u);
       X[l] -= lo;
     }
-    if (frac < (1u << 21) || frac > ~(1u << 21)) exact_lift<NL>(X, K);
+    if (frac < (1u << 14) || frac > ~(1u << 14)) exact_lift<NL>(X, K);
 
     if constexpr (LIMBS) {
-      uint32_t* dst = Xout + (i * N + j) * OZK_LIMBS;
-      const uint32_t ext = is_negative<NL>(X) ? 0xFFFFFFFFu : 0u;
+      if (j0 + o < N) {
+        uint32_t* dst = Xout + (i * N + j0 + o) * OZK_LIMBS;
+        const uint32_t ext = is_negative<NL>(X) ? 0xFFFFFFFFu : 0u;
 #pragma unroll
-      for (int l = 0; l < OZK_LIMBS; ++l) dst[l] = l < NL ? X[l] : ext;
+        for (int l = 0; l < OZK_LIMBS; ++l) dst[l] = l < NL ? X[l] : ext;
+      }
     } else {
-      const int32_t tj = t[j];
-      uint64_t bits;
-      if (si == OZK_SCALE_NONFINITE || tj == OZK_SCALE_NONFINITE)
-        bits = kQuietNaN;
+      if (si == OZK_SCALE_NONFINITE || tj[o] == OZK_SCALE_NONFINITE)
+        outbits[o] = kQuietNaN;
       else
-        bits = round_scaled_bits<NL>(X, si + tj);
-      __stcs(reinterpret_cast<unsigned long long*>(C + i * ldc + j), bits);
+        outbits[o] = round_scaled_bits<NL>(X, si + tj[o]);
+    }
+  }
+  if constexpr (!LIMBS) {
+    double* dst = C + i * ldc + j0;
+    if (j0 + 3 < N && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+      store4_f64(dst, outbits);
+    } else {
+#pragma unroll
+      for (int o = 0; o < 4; ++o)
+        if (j0 + o < N) __stcs(reinterpret_cast<unsigned long long*>(dst + o), outbits[o]);
     }
   }
 }

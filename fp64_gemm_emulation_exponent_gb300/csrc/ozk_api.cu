@@ -61,23 +61,23 @@ CrtConst build_crt_const(int n) {
     K.p[k] = p;
     K.magic[k] = magic_of(p);
     K.bias[k] = bias_of(p);
-    K.r32[k] = static_cast<uint32_t>((0x100000000ull + p / 2) / p);
-    Limbs Mk;
-    limbs_set(Mk, 1);
+    Limbs ek;  // P/p_k, then times w_k
+    limbs_set(ek, 1);
     uint32_t mk_mod_p = 1;
     for (int j = 0; j < n; ++j) {
       if (j == k) continue;
-      limbs_mul_small(Mk, modulus_at(j));
+      limbs_mul_small(ek, modulus_at(j));
       mk_mod_p = (mk_mod_p * (modulus_at(j) % p)) % p;
     }
-    for (int l = 0; l < kMaxCrtLimbs; ++l) K.Mk[k][l] = Mk.w[l];
-    uint32_t inv = 0;
+    uint32_t w = 0;
     for (uint32_t x = 1; x < p; ++x)
       if ((mk_mod_p * x) % p == 1u) {
-        inv = x;
+        w = x;
         break;
       }
-    K.w[k] = inv;
+    limbs_mul_small(ek, w);  // e_k = (P/p_k) w_k < P
+    for (int l = 0; l < kMaxCrtLimbs; ++l) K.e[k][l] = ek.w[l];
+    K.frac[k] = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + p / 2) / p);
   }
   return K;
 }
@@ -217,8 +217,7 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if ((rc = record(ev, 0, stream))) return rc;
   OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
   if ((rc = record(ev, 1, stream))) return rc;
-  OZK_CUDA(launch_quantize_a(M, K, L.kpad, A, lda, s, n, as, stream));
-  OZK_CUDA(launch_quantize_b(K, N, L.kpad, B, ldb, t, n, bs, stream));
+  OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, bs, stream));
   if ((rc = record(ev, 2, stream))) return rc;
   OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, bs, n, L.splits == 1 ? 0 : 1, out, L.ldo, L.splits,
                                sms, stream));
@@ -432,12 +431,14 @@ int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda, const int
   if (M < 0 || K < 0) return OZK_ERR_INVALID_ARG;
   if (n_moduli < 2 || n_moduli > kMaxModuli || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
   if (M == 0 || K == 0) return OZK_OK;
-  if (!A || lda < K || !s || !a_slices || reinterpret_cast<uintptr_t>(a_slices) % 16)
+  if (!A || lda < K || !s || !a_slices || reinterpret_cast<uintptr_t>(a_slices) % 32)
     return OZK_ERR_INVALID_ARG;
+  const int beta = beta_for(K, n_moduli);
+  if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
-  OZK_CUDA(launch_quantize_a(M, K, ozk_kpad(K), A, lda, s, n_moduli, a_slices,
-                             reinterpret_cast<cudaStream_t>(stream)));
+  OZK_CUDA(launch_quantize(M, 0, K, ozk_kpad(K), A, lda, nullptr, 0, s, nullptr, n_moduli, beta,
+                           a_slices, nullptr, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
 
@@ -446,12 +447,14 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb, const int
   if (N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
   if (n_moduli < 2 || n_moduli > kMaxModuli || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
   if (N == 0 || K == 0) return OZK_OK;
-  if (!B || ldb < N || !t || !b_slices || reinterpret_cast<uintptr_t>(b_slices) % 16)
+  if (!B || ldb < N || !t || !b_slices || reinterpret_cast<uintptr_t>(b_slices) % 32)
     return OZK_ERR_INVALID_ARG;
+  const int beta = beta_for(K, n_moduli);
+  if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
-  OZK_CUDA(launch_quantize_b(K, N, ozk_kpad(K), B, ldb, t, n_moduli, b_slices,
-                             reinterpret_cast<cudaStream_t>(stream)));
+  OZK_CUDA(launch_quantize(0, N, K, ozk_kpad(K), nullptr, 0, B, ldb, nullptr, t, n_moduli, beta,
+                           nullptr, b_slices, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
 

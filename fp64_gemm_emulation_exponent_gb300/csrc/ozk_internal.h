@@ -48,21 +48,22 @@ __host__ __device__ __forceinline__ void static_for(F&& f) {
   }
 }
 
-// Limb count of the CRT accumulator for n moduli: S = sum_k y_k P/p_k with
-// y_k < 2^16 stays below 2^(8n + 14) (log2 P <= 8n, n <= 20).  At least 3.
+// Limb count of the CRT accumulator for n moduli: S = sum_k c_k e_k with
+// c_k < 256, e_k < P <= 2^(8n) stays below n 2^(8n + 8) < 2^(8n + 14).  At least 3.
 __host__ __device__ constexpr int crt_limbs(int n) {
   return (8 * n + 14 + 31) / 32 < 3 ? 3 : (8 * n + 14 + 31) / 32;
 }
 constexpr int kMaxCrtLimbs = 6;
 
 // Constants of the CRT combine for one moduli count (built on the host).
+// e_k = (P/p_k) w_k with w_k = (P/p_k)^-1 mod p_k is the CRT basis vector of
+// modulus k (e_k = 1 mod p_k, 0 mod the others, e_k < P); e_k / P = w_k / p_k.
 struct CrtConst {
   uint32_t p[kMaxModuli];
   uint32_t magic[kMaxModuli];
   uint32_t bias[kMaxModuli];
-  uint32_t w[kMaxModuli];    // (P/p_k)^-1 mod p_k
-  uint32_t r32[kMaxModuli];  // round(2^32 / p_k)
-  uint32_t Mk[kMaxModuli][kMaxCrtLimbs];  // P/p_k, little-endian 32-bit limbs
+  uint32_t frac[kMaxModuli];  // round(2^32 w_k / p_k): e_k / P in 0.32 fixed point
+  uint32_t e[kMaxModuli][kMaxCrtLimbs];  // e_k, little-endian 32-bit limbs
   uint32_t P[kMaxCrtLimbs];
   int n;
 };
@@ -75,12 +76,12 @@ const CrtConst& crt_const(int n);
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                          const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
                          uint64_t* amax, cudaStream_t stream);
-cudaError_t launch_quantize_a(int64_t M, int64_t K, int64_t kpad, const double* A,
-                              int64_t lda, const int32_t* s, int n, uint16_t* out,
-                              cudaStream_t stream);
-cudaError_t launch_quantize_b(int64_t K, int64_t N, int64_t kpad, const double* B,
-                              int64_t ldb, const int32_t* t, int n, uint16_t* out,
-                              cudaStream_t stream);
+// Quantises A (when A is not null) and B (when B is not null) in one launch;
+// slices must be 32-byte aligned.
+cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
+                            int64_t lda, const double* B, int64_t ldb, const int32_t* s,
+                            const int32_t* t, int n, int beta, uint16_t* a_out, uint16_t* b_out,
+                            cudaStream_t stream);
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
                                 const uint16_t* b_slices, int n, int out_kind, void* out,
                                 int64_t ldo, int splits, int num_sms, cudaStream_t stream);

@@ -6,7 +6,7 @@
 //
 // All arithmetic on the operands is integer work on IEEE-754 bit patterns:
 // GB300's FP64 pipe is slow, and rounding m * 2^sh to an integer is a shift
-// plus a rounding increment.
+// plus a rounding increment.  Both kernels cover A and B in one launch.
 #include "ozk_internal.h"
 
 namespace ozk {
@@ -14,10 +14,9 @@ namespace {
 
 constexpr uint64_t kAbsMask = 0x7FFFFFFFFFFFFFFFull;
 constexpr uint64_t kInfBits = 0x7FF0000000000000ull;
-
-__device__ __forceinline__ uint64_t abs_bits(double x) {
-  return static_cast<uint64_t>(__double_as_longlong(x)) & kAbsMask;
-}
+constexpr int kScanThreads = 256;
+constexpr int kQThreads = 128;
+constexpr int kQK = 16;  // K elements per quantisation thread: one 32-byte store per modulus
 
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
@@ -27,73 +26,92 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
-// The scan reads A and B first; the quantisation re-reads them for the last
-// time, so only its loads are marked evict-first.
-__device__ __forceinline__ double2 load_keep2(const double* p) {
-  return __ldg(reinterpret_cast<const double2*>(p));
+// 32 bytes (four doubles' bit patterns) from a 32-byte aligned address.
+__device__ __forceinline__ void load4_u64(const double* p, uint64_t (&v)[4]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u64 {%0, %1, %2, %3}, [%4];"
+               : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3])
+               : "l"(p));
 }
 
-__device__ __forceinline__ double2 load_stream2(const double* p) {
-  return __ldcs(reinterpret_cast<const double2*>(p));
+__device__ __forceinline__ uint64_t load1_u64(const double* p) {
+  return static_cast<uint64_t>(__double_as_longlong(__ldg(p)));
 }
 
 // ---------------------------------------------------------------------------
 // Exponent scan.  For non-negative doubles the bit pattern orders like the
 // value, so max |x| is a max over 63-bit integers; Inf/NaN sort above every
-// finite value.
+// finite value.  Blocks [0, a_blocks) scan rows of A (one warp per row
+// segment), the rest scan columns of B (one thread per 1 or 4 columns over a
+// row segment); partial maxima meet in amax through 64-bit atomicMax.
 // ---------------------------------------------------------------------------
+struct ScanParams {
+  const double* A;
+  const double* B;
+  int64_t lda, ldb, M, N, K;
+  int64_t a_seg, a_segs, a_blocks;  // rows: 8 per block, a_segs segments of a_seg
+  int64_t b_seg, b_segs, b_cols;    // columns per block = 256 * b_cols
+  int a_vec, b_vec;                 // 32-byte loads possible
+  uint64_t* amax;                   // [M + N]
+};
 
-// One warp per (row of A, K segment).  VEC: rows start 16-byte aligned.
-template <bool VEC>
-__global__ void __launch_bounds__(256) scan_rows_kernel(const double* __restrict__ A, int64_t lda,
-                                                        int64_t M, int64_t K, int64_t seg,
-                                                        uint64_t* __restrict__ amax) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (row >= M) return;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * seg;
-  const int64_t k1 = min(K, k0 + seg);
-  const double* a = A + row * lda;
-  uint64_t m = 0;
-  if (VEC) {  // seg is even, so k0 is even and a + k0 is 16-byte aligned
-    const int64_t q1 = k1 >> 1;
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp) {
+  const int64_t bid = blockIdx.x;
+  if (bid < sp.a_blocks) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (bid / sp.a_segs) * 8 + warp;
+    if (row >= sp.M) return;
+    const int64_t k0 = (bid % sp.a_segs) * sp.a_seg;
+    const int64_t k1 = min(sp.K, k0 + sp.a_seg);
+    const double* a = sp.A + row * sp.lda;
+    uint64_t m = 0;
+    if (sp.a_vec) {  // a_seg is a multiple of 4: every group of 4 starts 32-byte aligned
+      const int64_t g1 = k1 >> 2;
+#pragma unroll 2
+      for (int64_t g = (k0 >> 2) + lane; g < g1; g += 32) {
+        uint64_t v[4];
+        load4_u64(a + 4 * g, v);
+        m = umax64(m, umax64(umax64(v[0] & kAbsMask, v[1] & kAbsMask), umax64(v[2] & kAbsMask, v[3] & kAbsMask)));
+      }
+      for (int64_t k = (g1 << 2) + lane; k < k1; k += 32) m = umax64(m, load1_u64(a + k) & kAbsMask);
+    } else {
 #pragma unroll 4
-    for (int64_t q = (k0 >> 1) + lane; q < q1; q += 32) {
-      double2 v = load_keep2(a + 2 * q);
-      m = umax64(m, umax64(abs_bits(v.x), abs_bits(v.y)));
+      for (int64_t k = k0 + lane; k < k1; k += 32) m = umax64(m, load1_u64(a + k) & kAbsMask);
     }
-    if ((k1 & 1) && lane == 0) m = umax64(m, abs_bits(a[k1 - 1]));
+    m = warp_max_u64(m);
+    if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + row), m);
   } else {
+    const int64_t b = bid - sp.a_blocks;
+    const int64_t cgrp = b / sp.b_segs;
+    const int64_t k0 = (b % sp.b_segs) * sp.b_seg;
+    const int64_t k1 = min(sp.K, k0 + sp.b_seg);
+    const int64_t c = (cgrp * kScanThreads + threadIdx.x) * sp.b_cols;
+    if (c >= sp.N) return;
+    uint64_t* out = sp.amax + sp.M + c;
+    if (sp.b_vec && c + 3 < sp.N) {
+      uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
 #pragma unroll 4
-    for (int64_t k = k0 + lane; k < k1; k += 32) m = umax64(m, abs_bits(__ldg(a + k)));
-  }
-  m = warp_max_u64(m);
-  if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned long long*>(amax + row), m);
-}
-
-// One thread per column pair (VEC) or column, over a K segment of B.
-template <bool VEC>
-__global__ void __launch_bounds__(256) scan_cols_kernel(const double* __restrict__ B, int64_t ldb,
-                                                        int64_t K, int64_t N, int64_t seg,
-                                                        uint64_t* __restrict__ amax) {
-  const int64_t c = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * (VEC ? 2 : 1);
-  if (c >= N) return;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * seg;
-  const int64_t k1 = min(K, k0 + seg);
-  uint64_t m0 = 0, m1 = 0;
-  if (VEC && c + 1 < N) {
+      for (int64_t k = k0; k < k1; ++k) {
+        uint64_t v[4];
+        load4_u64(sp.B + k * sp.ldb + c, v);
+        m0 = umax64(m0, v[0] & kAbsMask);
+        m1 = umax64(m1, v[1] & kAbsMask);
+        m2 = umax64(m2, v[2] & kAbsMask);
+        m3 = umax64(m3, v[3] & kAbsMask);
+      }
+      if (m0) atomicMax(reinterpret_cast<unsigned long long*>(out), m0);
+      if (m1) atomicMax(reinterpret_cast<unsigned long long*>(out + 1), m1);
+      if (m2) atomicMax(reinterpret_cast<unsigned long long*>(out + 2), m2);
+      if (m3) atomicMax(reinterpret_cast<unsigned long long*>(out + 3), m3);
+    } else {
+      const int64_t cend = min(sp.N, c + sp.b_cols);
+      for (int64_t cc = c; cc < cend; ++cc) {
+        uint64_t m0 = 0;
 #pragma unroll 4
-    for (int64_t k = k0; k < k1; ++k) {
-      double2 v = load_keep2(B + k * ldb + c);
-      m0 = umax64(m0, abs_bits(v.x));
-      m1 = umax64(m1, abs_bits(v.y));
+        for (int64_t k = k0; k < k1; ++k) m0 = umax64(m0, load1_u64(sp.B + k * sp.ldb + cc) & kAbsMask);
+        if (m0) atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + sp.M + cc), m0);
+      }
     }
-  } else {
-#pragma unroll 4
-    for (int64_t k = k0; k < k1; ++k) m0 = umax64(m0, abs_bits(__ldg(B + k * ldb + c)));
   }
-  if (m0) atomicMax(reinterpret_cast<unsigned long long*>(amax + c), m0);
-  if (VEC && m1) atomicMax(reinterpret_cast<unsigned long long*>(amax + c + 1), m1);
 }
 
 // s = beta - E with max|x| = f 2^E, f in [0.5, 1) (frexp's exponent, read off
@@ -122,17 +140,23 @@ __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_
 
 // ---------------------------------------------------------------------------
 // Quantisation.  x = (-1)^neg m 2^e exactly (m < 2^53); with sh = e + s the
-// integer is |a'| = m 2^sh rounded to nearest, ties to even (a shift and a
-// rounding increment), |a'| <= 2^beta <= 2^72, held as five 16-bit limbs.
-// Its residue mod p is sum_j L_j (2^16j mod p) reduced once.
+// integer is a' = (-1)^neg round(m 2^sh), rounded to nearest with ties to
+// even (a shift and a rounding increment), |a'| <= 2^beta <= 2^72.  a' is
+// kept as NL limbs of 22 bits of its two's complement modulo 2^(22 NL):
+// a' = v - neg * 2^(22 NL) with v = sum_j l_j 2^(22 j), so
+//   a' mod p = (sum_j l_j (2^22j mod p) + neg (p - 2^(22 NL) mod p)) mod p.
+// Three limbs hold every beta <= 64; four the rest.
 // ---------------------------------------------------------------------------
-struct Scaled {
-  uint32_t l0, l1, l2, l3, l4;  // |a'| = l0 + l1 2^16 + l2 2^32 + l3 2^48 + l4 2^64
-  uint32_t neg;
+constexpr uint32_t kMask22 = (1u << 22) - 1;
+
+template <int NL>
+struct Limbs22 {
+  uint32_t l[NL];
+  uint32_t neg;  // 1 when a' < 0
 };
 
-__device__ __forceinline__ Scaled scale_round(double x, int32_t sc) {
-  const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(x));
+template <int NL>
+__device__ __forceinline__ Limbs22<NL> scale_round(uint64_t bits, int32_t sc) {
   const uint32_t ex = static_cast<uint32_t>(bits >> 52) & 0x7FFu;
   uint64_t m = bits & 0xFFFFFFFFFFFFFull;
   if (ex) m |= 1ull << 52;
@@ -155,139 +179,152 @@ __device__ __forceinline__ Scaled scale_round(double x, int32_t sc) {
     const uint64_t half = 1ull << (r - 1);
     lo = q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);
     hi = 0;
-  } else {  // m 2^sh < 2^-11: rounds to 0
+  } else {  // m 2^sh < 2^-11 rounds to 0
     lo = 0;
     hi = 0;
   }
-  Scaled r;
-  r.l0 = static_cast<uint32_t>(lo) & 0xFFFFu;
-  r.l1 = static_cast<uint32_t>(lo >> 16) & 0xFFFFu;
-  r.l2 = static_cast<uint32_t>(lo >> 32) & 0xFFFFu;
-  r.l3 = static_cast<uint32_t>(lo >> 48);
-  r.l4 = hi;
-  r.neg = static_cast<uint32_t>(bits >> 63);
-  return r;
+  Limbs22<NL> a;
+  a.neg = static_cast<uint32_t>(bits >> 63) & ((lo | hi) != 0 ? 1u : 0u);
+  if (a.neg) {  // two's complement of the (hi:lo) magnitude
+    hi = ~hi + (lo == 0 ? 1u : 0u);
+    lo = 0ull - lo;
+  }
+  a.l[0] = static_cast<uint32_t>(lo) & kMask22;
+  a.l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
+  a.l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
+  if constexpr (NL == 4) a.l[3] = (hi >> 2) & kMask22;
+  return a;
 }
 
-// Balanced residue of (-1)^neg |a'| modulo the k-th modulus, in [-128, 127].
-// x below stays under 2^16 + 3 * 2^16 * 255 + 2^9 * 255 < 2^26.
-template <int k>
-__device__ __forceinline__ int balanced_residue(const Scaled& a) {
+// fp32 value v (|v| <= 2^22) from the integer magic + v, exactly.
+constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
+constexpr float kMagic = 12582912.0f;
+
+// (1.5 * 2^23 + residue) bits for the k-th modulus: the balanced residue
+// r in [-floor(p/2), ceil(p/2) - 1] of a', offset by the magic.
+template <int k, int NL>
+__device__ __forceinline__ uint32_t magic_residue(const Limbs22<NL>& a) {
   constexpr uint32_t p = modulus_at(k);
   if constexpr (p == 256u) {
-    // two's-complement low byte of the signed integer, read as int8
-    const uint32_t lowbyte = a.neg ? (0u - a.l0) : a.l0;
-    return static_cast<int>(static_cast<int8_t>(lowbyte & 0xFFu));
+    // the low byte of the two's complement, read as int8
+    return kMagicBits + static_cast<uint32_t>(static_cast<int32_t>(a.l[0] << 24) >> 24);
   } else {
-    constexpr uint32_t c1 = pow2_mod(16, p), c2 = pow2_mod(32, p), c3 = pow2_mod(48, p),
-                       c4 = pow2_mod(64, p), mg = magic_of(p);
-    const uint32_t x = a.l0 + a.l1 * c1 + a.l2 * c2 + a.l3 * c3 + a.l4 * c4;
-    const uint32_t q = __umulhi(x, mg);
-    int r = static_cast<int>(x - q * p);
-    r += r < 0 ? static_cast<int>(p) : 0;                        // |a'| mod p
-    r -= r > static_cast<int>((p - 1) / 2) ? static_cast<int>(p) : 0;  // balanced (p odd)
-    return a.neg ? -r : r;
+    constexpr uint32_t h = (p - 1) / 2;  // balanced = canonical of (x + h), minus h
+    constexpr uint32_t c1 = pow2_mod(22, p), c2 = pow2_mod(44, p);
+    if constexpr (NL == 3) {
+      // x < 2^22 (1 + 2 * 254) + 254 + 127 < 2^31: the 2^39 magic divides exactly
+      constexpr uint32_t d = (p - pow2_mod(66, p)) % p;
+      constexpr uint32_t m39 = static_cast<uint32_t>(((1ull << 39) + p - 1) / p);
+      const uint32_t x = a.l[0] + h + a.l[1] * c1 + a.l[2] * c2 + a.neg * d;
+      const uint32_t q = __umulhi(x, m39) >> 7;
+      return (kMagicBits - h) + (x - q * p);
+    } else {
+      // x < 2^32; the 2^32 magic quotient is exact or one too large
+      constexpr uint32_t c3 = pow2_mod(66, p);
+      constexpr uint32_t d = (p - pow2_mod(88, p)) % p;
+      constexpr uint32_t mg = magic_of(p);
+      const uint32_t x = a.l[0] + h + a.l[1] * c1 + a.l[2] * c2 + a.l[3] * c3 + a.neg * d;
+      const uint32_t q = __umulhi(x, mg);
+      int32_t r = static_cast<int32_t>(x - q * p);
+      r += r < 0 ? static_cast<int32_t>(p) : 0;
+      return (kMagicBits - h) + static_cast<uint32_t>(r);
+    }
   }
 }
 
-// bfloat16 bits of a small integer (|r| <= 256 is exact in bf16).
-__device__ __forceinline__ uint32_t bf16_bits_of_small_int(int r) {
-  const float f = __int_as_float(0x4B400000 + r) - 12582912.0f;  // exact: |r| < 2^22
-  return __float_as_uint(f) >> 16;
+// Two magic-offset residues to a packed pair of bfloat16 (exact integers).
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t mlo, uint32_t mhi) {
+  const float lo = __uint_as_float(mlo) - kMagic;
+  const float hi = __uint_as_float(mhi) - kMagic;
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(int lo, int hi) {
-  return bf16_bits_of_small_int(lo) | (bf16_bits_of_small_int(hi) << 16);
+__device__ __forceinline__ void store8_u32(uint16_t* dst, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
-// One thread per 8 consecutive K elements of one row of A.
-template <bool VEC>
-__global__ void __launch_bounds__(256) quantize_a_kernel(const double* __restrict__ A, int64_t lda,
-                                                         int64_t M, int64_t K, int64_t kpad,
-                                                         const int32_t* __restrict__ s, int n,
-                                                         uint16_t* __restrict__ out) {
-  const int64_t groups = kpad >> 3;
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (g >= M * groups) return;
-  const int64_t row = g / groups;
-  const int64_t k0 = (g - row * groups) * 8;
-  const int32_t sc = s[row];
-  const double* a = A + row * lda + k0;
-  double v[8];
+struct QuantParams {
+  const double* A;
+  const double* B;
+  const int32_t* s;
+  const int32_t* t;
+  uint16_t* a_out;  // [n][M][kpad]
+  uint16_t* b_out;  // [n][N][kpad]
+  int64_t lda, ldb, M, N, K, kpad;
+  int64_t groups;     // kpad / 16
+  int64_t a_threads;  // M * groups; B threads follow
+  int64_t b_threads;  // N * groups
+  int n;
+  int a_vec;  // rows of A are 32-byte aligned
+};
+
+// One thread: 16 consecutive K entries of one row of A (thread order: k fastest,
+// so loads and stores of a warp are contiguous) or of one column of B (thread
+// order: columns fastest, so each of the 16 row loads of a warp is contiguous).
+// Each writes one 32-byte run of every modulus' slice.
+template <int NL>
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams qp) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
+  uint64_t v[kQK];
+  int64_t row, k0, rows;
+  int32_t sc;
+  uint16_t* out;
+  if (g < qp.a_threads) {
+    row = g / qp.groups;
+    k0 = (g - row * qp.groups) * kQK;
+    rows = qp.M;
+    out = qp.a_out;
+    sc = qp.s[row];
+    const double* a = qp.A + row * qp.lda + k0;
+    if (qp.a_vec && k0 + kQK <= qp.K) {
+#pragma unroll
+      for (int e = 0; e < kQK / 4; ++e) {
+        uint64_t w[4];
+        load4_u64(a + 4 * e, w);
+        v[4 * e] = w[0];
+        v[4 * e + 1] = w[1];
+        v[4 * e + 2] = w[2];
+        v[4 * e + 3] = w[3];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kQK; ++e) v[e] = (k0 + e < qp.K) ? load1_u64(a + e) : 0ull;
+    }
+  } else {
+    const int64_t gb = g - qp.a_threads;
+    if (gb >= qp.b_threads) return;
+    const int64_t kg = gb / qp.N;
+    row = gb - kg * qp.N;  // column j of B
+    k0 = kg * kQK;
+    rows = qp.N;
+    out = qp.b_out;
+    sc = qp.t[row];
+    const double* b = qp.B + k0 * qp.ldb + row;
+#pragma unroll
+    for (int e = 0; e < kQK; ++e) v[e] = (k0 + e < qp.K) ? load1_u64(b + e * qp.ldb) : 0ull;
+  }
   if (sc == OZK_SCALE_NONFINITE) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = 0.0;
-  } else if (VEC && k0 + 8 <= K) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      double2 d = load_stream2(a + 2 * e);
-      v[2 * e] = d.x;
-      v[2 * e + 1] = d.y;
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (k0 + e < K) ? __ldcs(a + e) : 0.0;
+    for (int e = 0; e < kQK; ++e) v[e] = 0;
   }
-  Scaled x[8];
+  Limbs22<NL> x[kQK];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) x[e] = scale_round(v[e], sc);
-  uint4* dst = reinterpret_cast<uint4*>(out + row * kpad + k0);
-  const int64_t plane = (M * kpad) >> 3;  // uint4 per modulus slice
+  for (int e = 0; e < kQK; ++e) x[e] = scale_round<NL>(v[e], sc);
+  uint16_t* dst = out + row * qp.kpad + k0;
+  const int64_t plane = rows * qp.kpad;
+  const int n = qp.n;
   static_for<0, kMaxModuli>([&](auto kc) {
     constexpr int k = decltype(kc)::value;
     if (k < n) {
-      uint4 w;
-      w.x = pack_bf16x2(balanced_residue<k>(x[0]), balanced_residue<k>(x[1]));
-      w.y = pack_bf16x2(balanced_residue<k>(x[2]), balanced_residue<k>(x[3]));
-      w.z = pack_bf16x2(balanced_residue<k>(x[4]), balanced_residue<k>(x[5]));
-      w.w = pack_bf16x2(balanced_residue<k>(x[6]), balanced_residue<k>(x[7]));
-      dst[k * plane] = w;
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        w[e] = pack_bf16x2(magic_residue<k, NL>(x[2 * e]), magic_residue<k, NL>(x[2 * e + 1]));
+      store8_u32(dst + k * plane, w);
     }
   });
-}
-
-// B (K x N, row-major) to K-major slices [n][N][kpad]: a 64 (k) x 32 (j) tile
-// is read with coalesced row segments, quantised, transposed through shared
-// memory and written as 128-byte rows.
-constexpr int kQbK = 64, kQbJ = 32, kQbRow = kQbK + 2;  // +2 bf16: conflict-free columns
-
-__global__ void __launch_bounds__(256) quantize_b_kernel(const double* __restrict__ B, int64_t ldb,
-                                                         int64_t K, int64_t N, int64_t kpad,
-                                                         const int32_t* __restrict__ t, int n,
-                                                         uint16_t* __restrict__ out) {
-  extern __shared__ uint16_t tile[];  // [n][kQbJ][kQbRow]
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kQbJ;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kQbK;
-  const int jl = threadIdx.x & 31, kr = threadIdx.x >> 5;
-  const int64_t j = j0 + jl;
-  const int32_t sc = j < N ? t[j] : 0;
-  const bool live = j < N && sc != OZK_SCALE_NONFINITE;
-  Scaled x[8];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int64_t k = k0 + kr + 8 * r;
-    const double v = (live && k < K) ? __ldcs(B + k * ldb + j) : 0.0;
-    x[r] = scale_round(v, sc);
-  }
-  static_for<0, kMaxModuli>([&](auto kc) {
-    constexpr int k = decltype(kc)::value;
-    if (k < n) {
-      uint16_t* row = tile + (k * kQbJ + jl) * kQbRow + kr;
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        row[8 * r] = static_cast<uint16_t>(bf16_bits_of_small_int(balanced_residue<k>(x[r])));
-    }
-  });
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows = n * kQbJ;
-  for (int q = warp; q < rows; q += 8) {
-    const int p = q / kQbJ, jj = q - p * kQbJ;
-    if (j0 + jj >= N) continue;
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + q * kQbRow + 2 * lane);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out + (p * N + j0 + jj) * kpad + k0);
-    dst[lane] = w;
-  }
 }
 
 }  // namespace
@@ -295,73 +332,86 @@ __global__ void __launch_bounds__(256) quantize_b_kernel(const double* __restric
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                          const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
                          uint64_t* amax, cudaStream_t stream) {
+  if (M + N == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint64_t) * static_cast<size_t>(M + N), stream);
   if (e != cudaSuccess) return e;
-  int sms = 0;
-  int dev = 0;
+  int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = kNumSmsFallback;
-  const int64_t target_warps = static_cast<int64_t>(sms) * 48;
-  if (M > 0 && K > 0) {
+  ScanParams sp;
+  sp.A = A;
+  sp.B = B;
+  sp.lda = lda;
+  sp.ldb = ldb;
+  sp.M = M;
+  sp.N = N;
+  sp.K = K;
+  sp.amax = amax;
+  sp.a_vec = (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
+  sp.b_vec = (reinterpret_cast<uintptr_t>(B) % 32 == 0) && (ldb % 4 == 0);
+  sp.a_seg = sp.a_segs = sp.a_blocks = 0;
+  sp.b_seg = sp.b_segs = 1;
+  sp.b_cols = sp.b_vec ? 4 : 1;
+  int64_t b_blocks = 0;
+  if (K > 0 && M > 0) {
+    const int64_t target_warps = static_cast<int64_t>(sms) * 64;
     int64_t segs = (target_warps + M - 1) / M;
     int64_t seg = (K + segs - 1) / segs;
-    seg = ((seg + 255) / 256) * 256;  // even, and long enough to amortise the atomics
-    segs = (K + seg - 1) / seg;
-    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 2 == 0);
-    dim3 grid(static_cast<unsigned>((M + 7) / 8), static_cast<unsigned>(segs));
-    if (vec)
-      scan_rows_kernel<true><<<grid, 256, 0, stream>>>(A, lda, M, K, seg, amax);
-    else
-      scan_rows_kernel<false><<<grid, 256, 0, stream>>>(A, lda, M, K, seg, amax);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    seg = ((seg + 255) / 256) * 256;
+    sp.a_seg = seg;
+    sp.a_segs = (K + seg - 1) / seg;
+    sp.a_blocks = ((M + 7) / 8) * sp.a_segs;
   }
-  if (N > 0 && K > 0) {
-    const bool vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (ldb % 2 == 0);
-    const int64_t cols_per_block = vec ? 512 : 256;
-    const int64_t bx = (N + cols_per_block - 1) / cols_per_block;
-    int64_t segs = (static_cast<int64_t>(sms) * 6 + bx - 1) / bx;
+  if (K > 0 && N > 0) {
+    const int64_t cgroups = (N + kScanThreads * sp.b_cols - 1) / (kScanThreads * sp.b_cols);
+    int64_t segs = (static_cast<int64_t>(sms) * 8 + cgroups - 1) / cgroups;
     int64_t seg = (K + segs - 1) / segs;
-    if (seg < 32) seg = 32;
-    segs = (K + seg - 1) / seg;
-    dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(segs));
-    if (vec)
-      scan_cols_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, K, N, seg, amax + M);
-    else
-      scan_cols_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, K, N, seg, amax + M);
+    if (seg < 16) seg = 16;
+    sp.b_seg = seg;
+    sp.b_segs = (K + seg - 1) / seg;
+    b_blocks = cgroups * sp.b_segs;
+  }
+  const int64_t blocks = sp.a_blocks + b_blocks;
+  if (blocks > 0) {
+    scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (M + N > 0) {
-    const int64_t blocks = (M + N + 255) / 256;
-    finalize_scales_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(amax, M, N, beta, s, t);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-cudaError_t launch_quantize_a(int64_t M, int64_t K, int64_t kpad, const double* A, int64_t lda,
-                              const int32_t* s, int n, uint16_t* out, cudaStream_t stream) {
-  if (M == 0 || kpad == 0) return cudaSuccess;
-  const int64_t threads = M * (kpad / 8);
-  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && (lda % 2 == 0);
-  if (vec)
-    quantize_a_kernel<true><<<blocks, 256, 0, stream>>>(A, lda, M, K, kpad, s, n, out);
-  else
-    quantize_a_kernel<false><<<blocks, 256, 0, stream>>>(A, lda, M, K, kpad, s, n, out);
+  finalize_scales_kernel<<<static_cast<unsigned>((M + N + 255) / 256), 256, 0, stream>>>(amax, M, N, beta, s, t);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_b(int64_t K, int64_t N, int64_t kpad, const double* B, int64_t ldb,
-                              const int32_t* t, int n, uint16_t* out, cudaStream_t stream) {
-  if (N == 0 || kpad == 0) return cudaSuccess;
-  const size_t smem = sizeof(uint16_t) * static_cast<size_t>(n) * kQbJ * kQbRow;
-  // the attribute belongs to the current device's copy of the kernel
-  cudaError_t e = cudaFuncSetAttribute(quantize_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(sizeof(uint16_t) * kMaxModuli * kQbJ * kQbRow));
-  if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((N + kQbJ - 1) / kQbJ), static_cast<unsigned>(kpad / kQbK));
-  quantize_b_kernel<<<grid, 256, smem, stream>>>(B, ldb, K, N, kpad, t, n, out);
+cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
+                            int64_t lda, const double* B, int64_t ldb, const int32_t* s,
+                            const int32_t* t, int n, int beta, uint16_t* a_out, uint16_t* b_out,
+                            cudaStream_t stream) {
+  if (kpad == 0 || (M == 0 && N == 0)) return cudaSuccess;
+  QuantParams qp;
+  qp.A = A;
+  qp.B = B;
+  qp.s = s;
+  qp.t = t;
+  qp.a_out = a_out;
+  qp.b_out = b_out;
+  qp.lda = lda;
+  qp.ldb = ldb;
+  qp.M = A ? M : 0;
+  qp.N = B ? N : 0;
+  qp.K = K;
+  qp.kpad = kpad;
+  qp.groups = kpad / kQK;
+  qp.a_threads = qp.M * qp.groups;
+  qp.b_threads = qp.N * qp.groups;
+  qp.n = n;
+  qp.a_vec = A && (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
+  const int64_t threads = qp.a_threads + qp.b_threads;
+  if (threads == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((threads + kQThreads - 1) / kQThreads);
+  // |a'| <= 2^beta: three 22-bit limbs of two's complement hold beta <= 64
+  if (beta <= 64)
+    quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
+  else
+    quantize_kernel<4><<<blocks, kQThreads, 0, stream>>>(qp);
   return cudaGetLastError();
 }
 

@@ -145,13 +145,16 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
  * r = sym(a' mod p) in [-floor(p/2), ceil(p/2)-1],
  * stored as bfloat16 (exact for these integers) at
  * a_slices[(p * M + i) * kpad + k]; columns K..kpad-1 are zero.
- * kpad = ozk_kpad(K).  Rows with s_i = OZK_SCALE_NONFINITE are zero. */
+ * kpad = ozk_kpad(K); a_slices must be 32-byte aligned.  Rows with
+ * s_i = OZK_SCALE_NONFINITE are zero.  Returns OZK_ERR_UNSUPPORTED when
+ * ozk_beta(K, n_moduli) < 1. */
 int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda,
                    const int32_t* s, int n_moduli, uint16_t* a_slices,
                    ozk_stream_t stream);
 
 /* Residue quantisation of B, transposed to K-major: the residue of b'_kj is
- * stored at b_slices[(p * N + j) * kpad + k]; rows K..kpad-1 are zero. */
+ * stored at b_slices[(p * N + j) * kpad + k]; rows K..kpad-1 are zero;
+ * b_slices must be 32-byte aligned. */
 int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb,
                    const int32_t* t, int n_moduli, uint16_t* b_slices,
                    ozk_stream_t stream);
