@@ -152,10 +152,18 @@ int validate(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, cons
 struct Layout {
   size_t amax, s, t, a, b, out, total;
   int64_t kpad, ldo;
+  int64_t a_plane, b_plane, out_plane;  // elements between consecutive moduli's planes
   int splits;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Plane stride in bytes: at least `bytes`, an odd multiple of 256.
+size_t skewed_plane(size_t bytes) {
+  size_t units = (bytes + 255) / 256;
+  if (units % 2 == 0) ++units;
+  return units * 256;
+}
 
 Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   Layout L;
@@ -169,13 +177,19 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(M), 256);
   L.t = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(N), 1024);
+  const size_t a_plane = skewed_plane(2u * static_cast<size_t>(M) * L.kpad);
+  const size_t b_plane = skewed_plane(2u * static_cast<size_t>(N) * L.kpad);
+  const size_t esize = L.splits == 1 ? 1 : 4;  // uint8 residues or int32 partial sums
+  const size_t o_plane = skewed_plane(esize * static_cast<size_t>(M) * L.ldo);
+  L.a_plane = static_cast<int64_t>(a_plane / 2);
+  L.b_plane = static_cast<int64_t>(b_plane / 2);
+  L.out_plane = static_cast<int64_t>(o_plane / esize);
   L.a = off;
-  off = align_up(off + 2u * static_cast<size_t>(n) * M * L.kpad, 1024);
+  off = align_up(off + a_plane * static_cast<size_t>(n), 1024);
   L.b = off;
-  off = align_up(off + 2u * static_cast<size_t>(n) * N * L.kpad, 1024);
+  off = align_up(off + b_plane * static_cast<size_t>(n), 1024);
   L.out = off;
-  const size_t per = L.splits == 1 ? 1 : 4 * static_cast<size_t>(L.splits);
-  off = align_up(off + per * static_cast<size_t>(n) * M * L.ldo, 256);
+  off = align_up(off + o_plane * static_cast<size_t>(n) * static_cast<size_t>(L.splits), 256);
   L.total = off;
   return L;
 }
@@ -217,13 +231,14 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if ((rc = record(ev, 0, stream))) return rc;
   OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
   if ((rc = record(ev, 1, stream))) return rc;
-  OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, bs, stream));
+  OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, L.a_plane, bs,
+                           L.b_plane, stream));
   if ((rc = record(ev, 2, stream))) return rc;
-  OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, bs, n, L.splits == 1 ? 0 : 1, out, L.ldo, L.splits,
-                               sms, stream));
+  OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n, L.splits == 1 ? 0 : 1,
+                               out, L.ldo, L.out_plane, L.splits, sms, stream));
   if ((rc = record(ev, 3, stream))) return rc;
-  OZK_CUDA(launch_crt(M, N, n, out, L.splits == 1 ? 0 : 1, L.ldo, L.splits, s, t, C, ldc, nullptr,
-                      stream));
+  OZK_CUDA(launch_crt(M, N, n, out, L.splits == 1 ? 0 : 1, L.ldo, L.out_plane, L.splits, s, t, C, ldc,
+                      nullptr, stream));
   if ((rc = record(ev, 4, stream))) return rc;
   return OZK_OK;
 }
@@ -438,7 +453,7 @@ int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda, const int
   int rc = check_device(nullptr);
   if (rc) return rc;
   OZK_CUDA(launch_quantize(M, 0, K, ozk_kpad(K), A, lda, nullptr, 0, s, nullptr, n_moduli, beta,
-                           a_slices, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+                           a_slices, M * ozk_kpad(K), nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
 
@@ -454,7 +469,7 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb, const int
   int rc = check_device(nullptr);
   if (rc) return rc;
   OZK_CUDA(launch_quantize(0, N, K, ozk_kpad(K), nullptr, 0, B, ldb, nullptr, t, n_moduli, beta,
-                           nullptr, b_slices, reinterpret_cast<cudaStream_t>(stream)));
+                           nullptr, 0, b_slices, N * ozk_kpad(K), reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
 
@@ -481,8 +496,8 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
   int sms = 0;
   int rc = check_device(&sms);
   if (rc) return rc;
-  OZK_CUDA(launch_residue_gemm(M, N, kpad, a_slices, b_slices, n_moduli, out_kind, out, ldo, splits,
-                               sms, reinterpret_cast<cudaStream_t>(stream)));
+  OZK_CUDA(launch_residue_gemm(M, N, kpad, a_slices, M * kpad, b_slices, N * kpad, n_moduli, out_kind,
+                               out, ldo, M * ldo, splits, sms, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
 
@@ -509,7 +524,7 @@ int ozk_crt_combine(int64_t M, int64_t N, int n_moduli, const void* in, int in_k
   if (rc || M == 0 || N == 0) return rc;
   if (!s || !t || !C || ldc < N) return OZK_ERR_INVALID_ARG;
   if ((rc = check_device(nullptr))) return rc;
-  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, splits, s, t, C, ldc, nullptr,
+  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, M * ldi, splits, s, t, C, ldc, nullptr,
                       reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
@@ -520,7 +535,7 @@ int ozk_crt_lift(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind
   if (rc || M == 0 || N == 0) return rc;
   if (!X) return OZK_ERR_INVALID_ARG;
   if ((rc = check_device(nullptr))) return rc;
-  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, splits, nullptr, nullptr, nullptr, 0, X,
+  OZK_CUDA(launch_crt(M, N, n_moduli, in, in_kind, ldi, M * ldi, splits, nullptr, nullptr, nullptr, 0, X,
                       reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }

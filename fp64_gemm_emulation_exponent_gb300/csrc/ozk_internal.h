@@ -76,18 +76,24 @@ const CrtConst& crt_const(int n);
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                          const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
                          uint64_t* amax, cudaStream_t stream);
+// Per-modulus planes (residue slices, residue or partial-sum planes) sit
+// `plane` elements apart; the workspace spaces them an odd number of 256-byte
+// units apart so that the n streams of a kernel do not fall on the same DRAM
+// channels at the same time.
+//
 // Quantises A (when A is not null) and B (when B is not null) in one launch;
-// slices must be 32-byte aligned.
+// slices and plane strides must be 32-byte aligned.
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
                             int64_t lda, const double* B, int64_t ldb, const int32_t* s,
-                            const int32_t* t, int n, int beta, uint16_t* a_out, uint16_t* b_out,
-                            cudaStream_t stream);
+                            const int32_t* t, int n, int beta, uint16_t* a_out, int64_t a_plane,
+                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
-                                const uint16_t* b_slices, int n, int out_kind, void* out,
-                                int64_t ldo, int splits, int num_sms, cudaStream_t stream);
+                                int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
+                                int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
+                                int num_sms, cudaStream_t stream);
 cudaError_t launch_crt(int64_t M, int64_t N, int n, const void* in, int in_kind, int64_t ldi,
-                       int splits, const int32_t* s, const int32_t* t, double* C, int64_t ldc,
-                       uint32_t* X, cudaStream_t stream);
+                       int64_t plane, int splits, const int32_t* s, const int32_t* t, double* C,
+                       int64_t ldc, uint32_t* X, cudaStream_t stream);
 
 // Device status word latched by kernels (residue_gemm.cu).
 int take_device_status(cudaStream_t stream, int* status);

@@ -33,9 +33,14 @@ __device__ int g_status;  // latched device-side faults, read by ozk_stream_stat
 
 namespace {
 
-constexpr int BM = kTileM, BN = kTileN, BK = kKBlock;
-constexpr int kStages = 4;
-constexpr int kChunkKB = 4;  // k-blocks per exact fp32 chunk: 256 products, |sum| <= 2^22
+constexpr int BM = kTileM, BN = kTileN;
+constexpr int BK = 64;       // K elements (bf16) per pipeline stage: one swizzle row
+constexpr int kStages = 4;   // smem ring depth
+static_assert(kKBlock % BK == 0, "slices are padded to whole stages");
+constexpr int kSwizzleBytes = BK * 2;                  // 128-byte or 64-byte swizzle
+constexpr uint64_t kLayoutType = kSwizzleBytes == 128 ? 2 : 4;  // descriptor swizzle code
+constexpr int kChunk = 256;                            // exact fp32 chunk: |sum| <= 2^22
+constexpr int kChunkKB = kChunk / BK;                  // k-blocks per chunk
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0: control, 1-2: epilogue
 // Register split between the warpgroups (setmaxnreg).  The kernel launches
@@ -83,7 +88,7 @@ __constant__ ModTable c_mod = make_mod_table();
 
 struct GemmParams {
   int M, N, n, kblocks, tiles_m, tiles_n, splits, kb_per_split, out_kind;
-  int64_t ldo;
+  int64_t ldo, out_plane;  // row stride and per-(split, modulus) plane stride, in elements
   void* out;
 };
 
@@ -191,13 +196,14 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
                : "memory");
 }
 
-// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle:
-// start address >> 4 (bits 0-13), leading byte offset 16 B (unused for this
-// layout), stride byte offset 1024 B between 8-row groups (bits 32-45),
-// descriptor version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+// Shared-memory matrix descriptor, K-major operand with a swizzle as wide as
+// one BK row: start address >> 4 (bits 0-13), leading byte offset 16 B
+// (unused for this layout), stride byte offset between 8-row groups
+// (bits 32-45), descriptor version 1 (bit 46), swizzle mode (bits 61-63:
+// 2 = 128B, 4 = 64B).
+__device__ __forceinline__ uint64_t smem_desc_swizzled(uint32_t addr) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+         (static_cast<uint64_t>((8 * kSwizzleBytes) >> 4) << 32) | (1ull << 46) | (kLayoutType << 61);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -240,8 +246,17 @@ __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Waits for this thread's tcgen05.ld to land.  The loaded registers are
+// operands, so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]),
+                 "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]),
+                 "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -265,6 +280,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   return r;
 }
 
+// acc[base .. base+31] += the 32 exact chunk sums held as fp32 in v.
+__device__ __forceinline__ void add_chunk(int32_t (&acc)[128], int base, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) acc[base + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+}
+
 // x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
 __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic, uint32_t bias) {
   const uint32_t u = static_cast<uint32_t>(x) + bias;
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // 1024-aligned tiles
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -380,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * kABytes));
-            const uint64_t db = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
+            const uint64_t da = smem_desc_swizzled(smem_u32(sA + stage * kABytes));
+            const uint64_t db = smem_desc_swizzled(smem_u32(sB + stage * kBBytes));
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
               mma_bf16(d, da + 2ull * kk, db + 2ull * kk, kIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
@@ -429,15 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(ab * BN + half * 128);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t v[32];
-          tmem_ld32(taddr + 32 * q, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            acc[32 * q + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
-        }
+        // 4 x 32 columns, double-buffered: the load of the next 32 columns is
+        // in flight while the previous 32 are added up
+        uint32_t va[32], vb[32];
+        tmem_ld32(taddr, va);
+        tmem_wait_ld(va);
+        tmem_ld32(taddr + 32, vb);
+        add_chunk(acc, 0, va);
+        tmem_wait_ld(vb);
+        tmem_ld32(taddr + 64, va);
+        add_chunk(acc, 32, vb);
+        tmem_wait_ld(va);
+        tmem_ld32(taddr + 96, vb);
+        add_chunk(acc, 64, va);
+        tmem_wait_ld(vb);
+        add_chunk(acc, 96, vb);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce0 + 8 * ab);
@@ -454,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gi < prm.M) {
         if (prm.out_kind == 0) {
           const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
-          uint8_t* dst = static_cast<uint8_t*>(prm.out) +
-                         (static_cast<int64_t>(w.p) * prm.M + gi) * prm.ldo + gj0;
+          uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(w.p) * prm.out_plane +
+                         gi * prm.ldo + gj0;
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             if (gj0 + 16 * v < prm.ldo) {
@@ -472,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           int32_t* dst = static_cast<int32_t*>(prm.out) +
-                         ((static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.M + gi) * prm.ldo + gj0;
+                         (static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.out_plane + gi * prm.ldo + gj0;
 #pragma unroll
           for (int v = 0; v < 32; ++v)
             if (gj0 + 4 * v < prm.ldo)
@@ -513,19 +540,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D view [n][rows][kpad] of bf16 slices, box 64 (k) x box_rows x 1.
-bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t kpad, int n,
-                    uint32_t box_rows) {
+// 3-D view of bf16 slices (row stride kpad, modulus stride plane elements),
+// box BK (k) x box_rows x 1.
+bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t kpad,
+                    int64_t plane, int n, uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kpad), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(n)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kpad) * 2,
-                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(kpad) * 2};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kpad) * 2, static_cast<cuuint64_t>(plane) * 2};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             kSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -533,7 +561,7 @@ bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_
 
 int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   const int64_t tiles = static_cast<int64_t>(n) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int64_t kblocks = kpad / BK;
+  const int64_t kblocks = kpad / kKBlock;  // split shares are whole 64-element blocks
   if (tiles >= num_sms || kblocks < 32) return 1;
   auto eff = [&](int64_t s) {
     const int64_t units = tiles * s;
@@ -553,23 +581,26 @@ int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
 }
 
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
-                                const uint16_t* b_slices, int n, int out_kind, void* out,
-                                int64_t ldo, int splits, int num_sms, cudaStream_t stream) {
+                                int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
+                                int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
+                                int num_sms, cudaStream_t stream) {
   if (M == 0 || N == 0) return cudaSuccess;
   CUtensorMap tmA, tmB;
-  if (!make_slice_map(&tmA, a_slices, M, kpad, n, BM) || !make_slice_map(&tmB, b_slices, N, kpad, n, BN))
+  if (!make_slice_map(&tmA, a_slices, M, kpad, a_plane, n, BM) ||
+      !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, BN))
     return cudaErrorInvalidValue;
   GemmParams prm;
   prm.M = static_cast<int>(M);
   prm.N = static_cast<int>(N);
   prm.n = n;
-  prm.kblocks = static_cast<int>(kpad / BK);
+  prm.kblocks = static_cast<int>(kpad / BK);  // kpad is a multiple of kKBlock
   prm.tiles_m = static_cast<int>((M + BM - 1) / BM);
   prm.tiles_n = static_cast<int>((N + BN - 1) / BN);
   prm.splits = splits;
-  prm.kb_per_split = (prm.kblocks + splits - 1) / splits;
+  prm.kb_per_split = static_cast<int>((kpad / kKBlock + splits - 1) / splits) * (kKBlock / BK);
   prm.out_kind = out_kind;
   prm.ldo = ldo;
+  prm.out_plane = out_plane;
   prm.out = out;
   const int64_t units = static_cast<int64_t>(n) * splits * prm.tiles_m * prm.tiles_n;
   const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);

@@ -250,8 +250,9 @@ struct QuantParams {
   const double* B;
   const int32_t* s;
   const int32_t* t;
-  uint16_t* a_out;  // [n][M][kpad]
-  uint16_t* b_out;  // [n][N][kpad]
+  uint16_t* a_out;  // modulus k, row i at a_out + k * a_plane + i * kpad
+  uint16_t* b_out;  // modulus k, column j at b_out + k * b_plane + j * kpad
+  int64_t a_plane, b_plane;
   int64_t lda, ldb, M, N, K, kpad;
   int64_t groups;     // kpad / 16
   int64_t a_threads;  // M * groups; B threads follow
@@ -268,13 +269,13 @@ template <int NL>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams qp) {
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
   uint64_t v[kQK];
-  int64_t row, k0, rows;
+  int64_t row, k0, plane;
   int32_t sc;
   uint16_t* out;
   if (g < qp.a_threads) {
     row = g / qp.groups;
     k0 = (g - row * qp.groups) * kQK;
-    rows = qp.M;
+    plane = qp.a_plane;
     out = qp.a_out;
     sc = qp.s[row];
     const double* a = qp.A + row * qp.lda + k0;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
     const int64_t kg = gb / qp.N;
     row = gb - kg * qp.N;  // column j of B
     k0 = kg * kQK;
-    rows = qp.N;
+    plane = qp.b_plane;
     out = qp.b_out;
     sc = qp.t[row];
     const double* b = qp.B + k0 * qp.ldb + row;
@@ -313,7 +314,6 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
 #pragma unroll
   for (int e = 0; e < kQK; ++e) x[e] = scale_round<NL>(v[e], sc);
   uint16_t* dst = out + row * qp.kpad + k0;
-  const int64_t plane = rows * qp.kpad;
   const int n = qp.n;
   static_for<0, kMaxModuli>([&](auto kc) {
     constexpr int k = decltype(kc)::value;
@@ -383,8 +383,8 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64
 
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
                             int64_t lda, const double* B, int64_t ldb, const int32_t* s,
-                            const int32_t* t, int n, int beta, uint16_t* a_out, uint16_t* b_out,
-                            cudaStream_t stream) {
+                            const int32_t* t, int n, int beta, uint16_t* a_out, int64_t a_plane,
+                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream) {
   if (kpad == 0 || (M == 0 && N == 0)) return cudaSuccess;
   QuantParams qp;
   qp.A = A;
@@ -393,6 +393,8 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   qp.t = t;
   qp.a_out = a_out;
   qp.b_out = b_out;
+  qp.a_plane = a_plane;
+  qp.b_plane = b_plane;
   qp.lda = lda;
   qp.ldb = ldb;
   qp.M = A ? M : 0;
