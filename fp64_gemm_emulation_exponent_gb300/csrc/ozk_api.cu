@@ -256,6 +256,8 @@ int beta_for(int64_t K, int n) {
   return beta >= 1 ? beta : -1;
 }
 
+int current_device_supported(int* sms) { return check_device(sms); }
+
 const CrtConst& crt_const(int n) {
   std::call_once(g_crt_once, [] {
     for (int k = 2; k <= kMaxModuli; ++k) g_crt[k] = build_crt_const(k);

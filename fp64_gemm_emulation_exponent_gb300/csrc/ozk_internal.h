@@ -70,6 +70,8 @@ struct CrtConst {
 
 // Host-side method constants (ozk_api.cu).
 int beta_for(int64_t K, int n);  // -1 when unsupported
+// OZK_OK when the current device is an sm_103 GPU (its SM count in *sms when not null).
+int current_device_supported(int* sms);
 const CrtConst& crt_const(int n);
 
 // Launchers; each returns the first CUDA error it meets.

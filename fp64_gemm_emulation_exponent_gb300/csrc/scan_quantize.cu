@@ -7,6 +7,9 @@
 // All arithmetic on the operands is integer work on IEEE-754 bit patterns:
 // GB300's FP64 pipe is slow, and rounding m * 2^sh to an integer is a shift
 // plus a rounding increment.  Both kernels cover A and B in one launch.
+#include <map>
+#include <mutex>
+
 #include "ozk_internal.h"
 
 namespace ozk {
@@ -418,3 +421,65 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
 }
 
 }  // namespace ozk
+
+// ---------------------------------------------------------------------------
+// The exponent scan without caller-provided scratch.
+//
+// ozk_scale needs (M + N) uint64 of device scratch for the running maxima.
+// Some callers cannot hand over device memory they did not plan for: a
+// library embedded in a host application whose allocator owns every device
+// byte, or a latency-critical loop that must not call cudaMalloc (which can
+// synchronise the device).  ozk_scale_noalloc keeps that scratch in a
+// fixed array compiled into the library instead.  Every GPU that loads the
+// library holds the array (2 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint64_t g_noalloc_amax[OZK_SCALE_NOALLOC_MAX];
+
+namespace ozk {
+namespace {
+
+std::mutex g_noalloc_mutex;
+std::map<int, uint64_t*> g_noalloc_ptr;  // device -> device address of g_noalloc_amax
+
+// The device address of the fixed scratch on the current device.  The name
+// g_noalloc_amax in host code is only a host-side stand-in; the address is
+// looked up once per device, with that device current.
+int noalloc_scratch(uint64_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  auto it = g_noalloc_ptr.find(dev);
+  if (it == g_noalloc_ptr.end()) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess || p == nullptr) return OZK_ERR_CUDA;
+    it = g_noalloc_ptr.emplace(dev, static_cast<uint64_t*>(p)).first;
+  }
+  *out = it->second;
+  return OZK_OK;
+}
+
+}  // namespace
+}  // namespace ozk
+
+extern "C" int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                                 const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
+                                 ozk_stream_t stream) {
+  using namespace ozk;
+  if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  const int beta = beta_for(K, n_moduli);
+  if (beta < 1 || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (M + N > OZK_SCALE_NOALLOC_MAX) return OZK_ERR_WORKSPACE;  // beyond the fixed scratch
+  if (M + N == 0) return OZK_OK;
+  if ((M && !s) || (N && !t)) return OZK_ERR_INVALID_ARG;
+  if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;
+  int rc = current_device_supported(nullptr);
+  if (rc) return rc;
+  uint64_t* amax = nullptr;
+  if ((rc = noalloc_scratch(&amax))) return rc;
+  // launch_scale zeroes the M + N maxima it uses before the scan, so the
+  // contents left by an earlier call do not matter
+  if (launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return OZK_ERR_CUDA;
+  return OZK_OK;
+}

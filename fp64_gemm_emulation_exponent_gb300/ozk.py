@@ -24,6 +24,7 @@ OZK_MAX_MODULI = 20
 OZK_MAX_K = 131071
 OZK_SCALE_NONFINITE = -(2**31)
 OZK_LIMBS = 8
+OZK_SCALE_NOALLOC_MAX = 262144
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
 
@@ -41,6 +42,7 @@ SIGNATURES = {
     "ozk_stream_status": (_i32, [_vp]),
     "ozk_release_cached": (_i32, []),
     "ozk_scale": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "ozk_scale_noalloc": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp]),
     "ozk_quantize_a": (_i32, [_i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp]),
     "ozk_quantize_b": (_i32, [_i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp]),
     "ozk_residue_gemm": (_i32, [_i64, _i64, _i64, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _vp]),
@@ -177,6 +179,11 @@ def dgemm(A, B, n_moduli: int = 14, out=None, stream=None):
 # ---------------------------------------------------------------- stages
 def ozk_scale(M, N, K, A, lda, B, ldb, n_moduli, s, t, scratch, stream=None):
     return _call("ozk_scale", M, N, K, _ptr(A), lda, _ptr(B), ldb, n_moduli, _ptr(s), _ptr(t), _ptr(scratch),
+                 _stream(stream))
+
+
+def ozk_scale_noalloc(M, N, K, A, lda, B, ldb, n_moduli, s, t, stream=None):
+    return _call("ozk_scale_noalloc", M, N, K, _ptr(A), lda, _ptr(B), ldb, n_moduli, _ptr(s), _ptr(t),
                  _stream(stream))
 
 

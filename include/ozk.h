@@ -139,6 +139,26 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
               const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
               uint64_t* scratch, ozk_stream_t stream);
 
+/* The exponent scan of ozk_scale for callers that cannot give the library
+ * device memory: a library embedded in an application whose allocator owns
+ * all device memory, or a latency-critical loop that must not call
+ * cudaMalloc (which may synchronise the device).  The paper has no
+ * counterpart; it is the same scan with its (M + N) uint64 of scratch held
+ * in a fixed 2 MiB array compiled into the library (each GPU that loads the
+ * library keeps it until the process exits), so it allocates nothing.
+ * Same arguments and results as ozk_scale without `scratch`.
+ *  - M + N above OZK_SCALE_NOALLOC_MAX returns OZK_ERR_WORKSPACE (nothing runs).
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up, no allocation); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array: calls whose kernels may
+ *    overlap on the GPU (different streams without ordering) race and give
+ *    wrong scales.  Each call clears the part of the array it uses. */
+#define OZK_SCALE_NOALLOC_MAX 262144
+int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                      const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
+                      ozk_stream_t stream);
+
 /* Residue quantisation of A ("double load, exponent scaling, round, mod,
  * balanced int8 conversion").  For each modulus p and element:
  * a'_ik = a_ik 2^s_i rounded to the nearest integer (ties to even) and
