@@ -36,7 +36,7 @@ METRIC = "emulated-DGEMM effective FP64 TFLOP/s at 4096^3 (53-bit) and % INT8 te
 WORKLOAD = "square4096_normal"
 N_MODULI = 14
 STAGES = ["scan", "quantize", "residue_gemm", "crt_combine"]
-KERNELS_PER_STEP = 7  # scan_rows, scan_cols, finalize, quantize_a, quantize_b, residue_gemm, crt
+KERNELS_PER_STEP = 5  # scan, finalize_scales, quantize, residue_gemm, crt
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "residue_gemm_traffic.json")
 
 
@@ -185,10 +185,14 @@ def oracle_block_rate(A, B, n, rows, cols):
 def cpu_baseline(A, B, n, target_s=12.0):
     import oracle
 
-    rows, cols = 2, 256
+    # calibrate the row count of the sample so that it takes about target_s
+    rows, cols = 4, 256
     _, dt = oracle_block_rate(A, B, n, rows, cols)
-    scale = max(1.0, min(64.0, target_s / max(dt, 1e-3)))
-    rows = int(min(A.shape[0], max(2, round(rows * scale))))
+    while dt < target_s / 4 and rows < A.shape[0]:
+        rows = int(min(A.shape[0], max(rows * 2, rows * target_s / max(dt, 1e-3) / 2)))
+        _, dt = oracle_block_rate(A, B, n, rows, cols)
+    if dt < target_s / 2 and rows < A.shape[0]:
+        rows = int(min(A.shape[0], rows * target_s / max(dt, 1e-3)))
     rate, dt = oracle_block_rate(A, B, n, rows, cols)
     return {"value": rate, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"C[0:{rows}, 0:{cols}] of the {A.shape[0]}x{B.shape[1]}x{A.shape[1]} workload "
