@@ -53,7 +53,11 @@ static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "regis
 constexpr uint32_t kABytes = BM * BK * 2;
 constexpr uint32_t kBBytes = BN * BK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kCols = BN / 2;  // accumulator columns per epilogue thread (two warps per TMEM lane quadrant)
+static_assert(kCols % 32 == 0, "the drain moves 32 columns per tcgen05.ld");
+// two BN-column fp32 accumulators, allocated as a power of two >= 32 columns
+constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;
+static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators fit the allocation");
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 50000000ull;
@@ -281,9 +285,23 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
 }
 
 // acc[base .. base+31] += the 32 exact chunk sums held as fp32 in v.
-__device__ __forceinline__ void add_chunk(int32_t (&acc)[128], int base, const uint32_t (&v)[32]) {
+__device__ __forceinline__ void add_chunk(int32_t (&acc)[kCols], int base, const uint32_t (&v)[32]) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) acc[base + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+}
+
+// Adds this thread's kCols chunk sums from TMEM into acc, 32 columns per
+// tcgen05.ld, double-buffered: load Q+1 is in flight while load Q (in cur,
+// already landed) is added up.
+template <int Q>
+__device__ __forceinline__ void drain_chunk(int32_t (&acc)[kCols], uint32_t taddr, uint32_t (&cur)[32],
+                                            uint32_t (&nxt)[32]) {
+  if constexpr (Q + 1 < kCols / 32) tmem_ld32(taddr + 32 * (Q + 1), nxt);
+  add_chunk(acc, 32 * Q, cur);
+  if constexpr (Q + 1 < kCols / 32) {
+    tmem_wait_ld(nxt);
+    drain_chunk<Q + 1>(acc, taddr, nxt, cur);
+  }
 }
 
 // x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
@@ -431,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_inc<kEpiRegs>();
     const int ew = warp - 4;
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
-    const int half = ew >> 2;   // which 128 of the 256 tile columns
+    const int half = ew >> 2;   // which kCols of the BN tile columns
     const int row_in_tile = quad * 32 + lane;
     int ab = 0;
     uint32_t aphase = 0;
@@ -439,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit w = decode_unit(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
-      int32_t acc[128];
+      int32_t acc[kCols];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) acc[e] = 0;
+      for (int e = 0; e < kCols; ++e) acc[e] = 0;
       for (int c = 0; c < nchunks; ++c) {
         if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
           ok = false;
@@ -449,22 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(ab * BN + half * 128);
-        // 4 x 32 columns, double-buffered: the load of the next 32 columns is
-        // in flight while the previous 32 are added up
+                               static_cast<uint32_t>(ab * BN + half * kCols);
         uint32_t va[32], vb[32];
         tmem_ld32(taddr, va);
         tmem_wait_ld(va);
-        tmem_ld32(taddr + 32, vb);
-        add_chunk(acc, 0, va);
-        tmem_wait_ld(vb);
-        tmem_ld32(taddr + 64, va);
-        add_chunk(acc, 32, vb);
-        tmem_wait_ld(va);
-        tmem_ld32(taddr + 96, vb);
-        add_chunk(acc, 64, va);
-        tmem_wait_ld(vb);
-        add_chunk(acc, 96, vb);
+        drain_chunk<0>(acc, taddr, va, vb);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce0 + 8 * ab);
@@ -474,17 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const uint32_t offset = static_cast<uint32_t>(nchunks) * kMagicBits;
 #pragma unroll
-      for (int e = 0; e < 128; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
+      for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
 
       const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
-      const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * 128;
+      const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
       if (gi < prm.M) {
         if (prm.out_kind == 0) {
           const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
           uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(w.p) * prm.out_plane +
                          gi * prm.ldo + gj0;
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
+          for (int v = 0; v < kCols / 16; ++v) {
             if (gj0 + 16 * v < prm.ldo) {
               uint32_t word[4];
 #pragma unroll
@@ -501,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           int32_t* dst = static_cast<int32_t*>(prm.out) +
                          (static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.out_plane + gi * prm.ldo + gj0;
 #pragma unroll
-          for (int v = 0; v < 32; ++v)
+          for (int v = 0; v < kCols / 4; ++v)
             if (gj0 + 4 * v < prm.ldo)
               *reinterpret_cast<int4*>(dst + 4 * v) =
                   make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
