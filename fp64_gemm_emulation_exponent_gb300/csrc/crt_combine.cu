@@ -5,21 +5,26 @@
 // that more registers per thread made it slower; on GB300 the FP64 pipe is
 // slow, so this kernel is integer-only:
 //
-//   X = sum_k c_k e_k - q P,  e_k = (P/p_k) ((P/p_k)^-1 mod p_k),
+//   X = sum_j r_j E_j - q P  (mod 2^(32 NL)),
 //
-// with the column sums of c_k e_k accumulated in 64 bits without carries, and
-// q = round(sum_k c_k w_k / p_k) estimated in 32.32 fixed point (error below
-// 2^12 / 2^32); the rare outputs whose estimate lies within 2^14 / 2^32 of a
-// rounding boundary get an exact correction.  The lifted X in [-P/2, P/2) is
-// then scaled by 2^-(s_i + t_j) and rounded to nearest-even in integer
-// arithmetic (subnormals and overflow included).
+// over the moduli taken in pairs: r_j = (c_2j u_j0 + c_2j+1 u_j1) mod m_j is
+// the residue of the pair modulus m_j = p_2j p_2j+1 (two byte residues into one
+// 16-bit one with three integer multiplies), E_j = e_2j + e_2j+1 mod P its CRT
+// basis vector; an odd last modulus enters on its own.  Pairing halves the
+// 64-bit multiply-accumulates, which bound this kernel on the FMA-heavy pipe.
+// The limb sums of r_j E_j are accumulated in 64 bits without carries and
+// -q P is folded in as q (2^(32 NL) - P).  q = round(sum_j r_j w_j / m_j) is
+// estimated in 32.32 fixed point (error below 2^18 / 2^32); the rare outputs
+// whose estimate lies within 2^20 / 2^32 of a rounding boundary get an exact
+// correction.  The lifted X in [-P/2, P/2) is then scaled by 2^-(s_i + t_j)
+// and rounded to nearest-even in integer arithmetic (a short path for normal
+// results, a general one for subnormals and overflow).
 #include "ozk_internal.h"
 
 namespace ozk {
 namespace {
 
 constexpr uint64_t kQuietNaN = 0x7FF8000000000000ull;
-constexpr int kCrtGroups = 2;  // groups of 4 columns per thread (8 columns: 8-byte residue loads)
 constexpr uint64_t kInfBits = 0x7FF0000000000000ull;
 
 __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic, uint32_t bias) {
@@ -150,6 +155,59 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&X)[NL], i
   return bits | (static_cast<uint64_t>(neg) << 63);
 }
 
+// Fast path of round_scaled_bits for |X| >= 2^(32(NL-2)) with a normal
+// result: a 64-bit window from the top two nonzero-headed limbs, 53 bits
+// kept, round to nearest even with the bits below as sticky.  Returns false
+// (and leaves *out alone) when the slow path must decide.
+template <int NL>
+__device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S, uint64_t* out) {
+  const uint32_t sgn = X[NL - 1] >> 31;
+  const uint32_t flip = 0u - sgn;
+  uint32_t m[NL];
+  uint32_t c = sgn;
+#pragma unroll
+  for (int l = 0; l < NL; ++l) {  // |X| = (X ^ flip) + sgn
+    const uint32_t x = X[l] ^ flip;
+    m[l] = x + c;
+    c = (c && m[l] == 0u) ? 1u : 0u;
+  }
+  const bool top = m[NL - 1] != 0u;
+  const uint32_t t2 = top ? m[NL - 1] : m[NL - 2];
+  const uint32_t t1 = top ? m[NL - 2] : m[NL - 3];
+  uint32_t t0, st;
+  if constexpr (NL >= 4) {
+    uint32_t below = 0;  // OR of the limbs under t0 when the top limb leads
+#pragma unroll
+    for (int l = 0; l + 3 < NL; ++l) below |= m[l];
+    uint32_t below2 = 0;  // same when limb NL-2 leads
+#pragma unroll
+    for (int l = 0; l + 4 < NL; ++l) below2 |= m[l];
+    t0 = top ? m[NL - 3] : m[NL - 4];
+    st = top ? below : below2;
+  } else {
+    t0 = top ? m[0] : 0u;
+    st = 0u;
+  }
+  if (t2 == 0u) return false;
+  const int lz = __clz(t2);
+  const uint32_t hi = __funnelshift_l(t1, t2, lz);
+  const uint32_t mid = __funnelshift_l(t0, t1, lz);
+  const uint32_t lo = t0 << lz;
+  const int e = (top ? 32 * (NL - 1) : 32 * (NL - 2)) + 31 - lz - S;  // |X| 2^-S in [2^e, 2^(e+1))
+  if (e < -1022 || e > 1023) return false;
+  const uint32_t sig_lo = __funnelshift_r(mid, hi, 11);
+  const uint32_t sig_hi = hi >> 11;
+  const uint32_t rb = (mid >> 10) & 1u;
+  const uint32_t sticky = ((mid & 0x3FFu) | lo | st) != 0u ? 1u : 0u;
+  const uint32_t inc = rb & (sticky | (sig_lo & 1u));
+  // the significand carries the leading one at bit 52: exponent field e + 1022
+  // plus one; a rounding carry into bit 53 bumps it once more (to Inf at the top)
+  const uint64_t bits = (static_cast<uint64_t>(e + 1022) << 52) +
+                        ((static_cast<uint64_t>(sig_hi) << 32) | sig_lo) + inc;
+  *out = bits | (static_cast<uint64_t>(sgn) << 63);
+  return true;
+}
+
 __device__ __forceinline__ void store4_f64(double* dst, const uint64_t (&b)[4]) {
   asm volatile("st.global.cs.v4.b64 [%0], {%1, %2, %3, %4};" ::"l"(dst), "l"(b[0]), "l"(b[1]), "l"(b[2]),
                "l"(b[3])
@@ -189,8 +247,16 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
   const int64_t groups = (N + W - 1) / W;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= M * groups) return;
-  const int64_t i = gid / groups;
-  const int64_t jt = (gid - i * groups) * W;
+  int64_t i, jt;
+  if (M * groups <= 0x7FFFFFFF) {
+    const uint32_t g32 = static_cast<uint32_t>(gid), gr = static_cast<uint32_t>(groups);
+    const uint32_t i32 = g32 / gr;
+    i = i32;
+    jt = static_cast<int64_t>(g32 - i32 * gr) * W;
+  } else {
+    i = gid / groups;
+    jt = (gid - i * groups) * W;
+  }
   const int n = K.n;
 
   uint32_t cw[kMaxModuli][G];
@@ -225,6 +291,16 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
     });
   }
   const int32_t si = LIMBS ? 0 : s[i];
+  uint32_t Pn[NL];  // 2^(32 NL) - P: X = sum c_k e_k + q Pn (mod 2^(32 NL))
+  {
+    uint32_t c = 1;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t v = static_cast<uint64_t>(~K.P[l]) + c;
+      Pn[l] = static_cast<uint32_t>(v);
+      c = static_cast<uint32_t>(v >> 32);
+    }
+  }
 
 #pragma unroll 1
   for (int gg = 0; gg < G; ++gg) {
@@ -251,21 +327,45 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
 #pragma unroll
       for (int l = 0; l < NL; ++l) acc[o][l] = 0;
     }
-    static_for<0, kMaxModuli>([&](auto kc) {
-      constexpr int k = decltype(kc)::value;
-      if (k < n) {
-        uint32_t word = cw[k][0];
+    // moduli in pairs: one 16-bit pair residue per (pair, output)
+    static_for<0, kMaxModuli / 2>([&](auto jc) {
+      constexpr int j = decltype(jc)::value;
+      if (2 * j + 1 < n) {
+        uint32_t wa = cw[2 * j][0], wb = cw[2 * j + 1][0];
 #pragma unroll
-        for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
+        for (int x = 1; x < G; ++x) {
+          wa = gg == x ? cw[2 * j][x] : wa;
+          wb = gg == x ? cw[2 * j + 1][x] : wb;
+        }
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
-          const uint32_t c = __byte_perm(word, 0u, 0x4440 + o);
-          qacc[o] += static_cast<uint64_t>(c) * K.frac[k];
+          const uint32_t ca = __byte_perm(wa, 0u, 0x4440 + o);
+          const uint32_t cb = __byte_perm(wb, 0u, 0x4440 + o);
+          const uint32_t t = ca * K.pu[j][0] + cb * K.pu[j][1];  // < 2^25
+          const uint32_t r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
+          qacc[o] += static_cast<uint64_t>(r) * K.pfrac[j];
 #pragma unroll
-          for (int l = 0; l < NL; ++l) acc[o][l] += static_cast<uint64_t>(c) * K.e[k][l];
+          for (int l = 0; l < NL; ++l) acc[o][l] += static_cast<uint64_t>(r) * K.pe[j][l];
         }
       }
     });
+    if (n & 1) {  // the last modulus on its own
+      static_for<0, kMaxModuli>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        if (k == n - 1) {
+          uint32_t word = cw[k][0];
+#pragma unroll
+          for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
+#pragma unroll
+          for (int o = 0; o < 4; ++o) {
+            const uint32_t c = __byte_perm(word, 0u, 0x4440 + o);
+            qacc[o] += static_cast<uint64_t>(c) * K.frac[k];
+#pragma unroll
+            for (int l = 0; l < NL; ++l) acc[o][l] += static_cast<uint64_t>(c) * K.e[k][l];
+          }
+        }
+      });
+    }
     uint64_t outbits[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int o = 0; o < 4; ++o) {
@@ -273,14 +373,14 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
       const uint32_t q = static_cast<uint32_t>(shifted >> 32);
       const uint32_t frac = static_cast<uint32_t>(shifted);
       uint32_t X[NL];
-      int64_t carry = 0;
+      uint64_t carry = 0;
 #pragma unroll
       for (int l = 0; l < NL; ++l) {
-        const int64_t v = static_cast<int64_t>(acc[o][l] - static_cast<uint64_t>(q) * K.P[l]) + carry;
+        const uint64_t v = acc[o][l] + static_cast<uint64_t>(q) * Pn[l] + carry;
         X[l] = static_cast<uint32_t>(v);
         carry = v >> 32;
       }
-      if (frac < (1u << 14) || frac > ~(1u << 14)) exact_lift<NL>(X, K);
+      if (frac < (1u << 20) || frac > ~(1u << 20)) exact_lift<NL>(X, K);
       if constexpr (LIMBS) {
         if (j0 + o < N) {
           uint32_t* dst = Xout + (i * N + j0 + o) * OZK_LIMBS;
@@ -291,7 +391,7 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
       } else {
         if (si == OZK_SCALE_NONFINITE || tj[o] == OZK_SCALE_NONFINITE)
           outbits[o] = kQuietNaN;
-        else
+        else if (!round_scaled_fast<NL>(X, si + tj[o], &outbits[o]))
           outbits[o] = round_scaled_bits<NL>(X, si + tj[o]);
       }
     }
@@ -308,11 +408,10 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
   }
 }
 
-template <int NL>
-cudaError_t launch_nl(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane, int splits,
-                      const int32_t* s, const int32_t* t, double* C, int64_t ldc, uint32_t* X,
-                      const CrtConst& K, cudaStream_t stream) {
-  constexpr int G = kCrtGroups;
+template <int NL, int G>
+cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
+                        int splits, const int32_t* s, const int32_t* t, double* C, int64_t ldc, uint32_t* X,
+                        const CrtConst& K, cudaStream_t stream) {
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   if (in_kind == 0) {
@@ -327,6 +426,18 @@ cudaError_t launch_nl(int64_t M, int64_t N, const void* in, int in_kind, int64_t
       crt_kernel<NL, 1, false, G><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K);
   }
   return cudaGetLastError();
+}
+
+// 8 columns per thread (8-byte residue loads) when that still gives every SM
+// several blocks; 4 otherwise.
+template <int NL>
+cudaError_t launch_nl(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane, int splits,
+                      const int32_t* s, const int32_t* t, double* C, int64_t ldc, uint32_t* X,
+                      const CrtConst& K, cudaStream_t stream) {
+  constexpr int64_t kWideThreads = 152 * 256 * 4;
+  if (M * ((N + 7) / 8) >= kWideThreads)
+    return launch_nl_g<NL, 2>(M, N, in, in_kind, ldi, plane, splits, s, t, C, ldc, X, K, stream);
+  return launch_nl_g<NL, 1>(M, N, in, in_kind, ldi, plane, splits, s, t, C, ldc, X, K, stream);
 }
 
 }  // namespace

@@ -79,6 +79,42 @@ CrtConst build_crt_const(int n) {
     for (int l = 0; l < kMaxCrtLimbs; ++l) K.e[k][l] = ek.w[l];
     K.frac[k] = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + p / 2) / p);
   }
+  for (int j = 0; 2 * j + 1 < n; ++j) {
+    const uint32_t pa = modulus_at(2 * j), pb = modulus_at(2 * j + 1);
+    const uint32_t m = pa * pb;
+    K.pm[j] = m;
+    uint32_t ia = 0, ib = 0;  // pb^-1 mod pa, pa^-1 mod pb
+    for (uint32_t x = 1; x < pa; ++x)
+      if ((pb % pa) * x % pa == 1u) {
+        ia = x;
+        break;
+      }
+    for (uint32_t x = 1; x < pb; ++x)
+      if ((pa % pb) * x % pb == 1u) {
+        ib = x;
+        break;
+      }
+    K.pu[j][0] = pb * ia;
+    K.pu[j][1] = pa * ib;
+    K.pmagic[j] = static_cast<uint32_t>(((uint64_t{1} << 42) + m - 1) / m);
+    Limbs E;  // P / m_j, then times w_j
+    limbs_set(E, 1);
+    uint32_t rest_mod_m = 1;
+    for (int i = 0; i < n; ++i) {
+      if (i == 2 * j || i == 2 * j + 1) continue;
+      limbs_mul_small(E, modulus_at(i));
+      rest_mod_m = static_cast<uint32_t>(static_cast<uint64_t>(rest_mod_m) * (modulus_at(i) % m) % m);
+    }
+    uint32_t w = 0;
+    for (uint32_t x = 1; x < m; ++x)
+      if (static_cast<uint64_t>(rest_mod_m) * x % m == 1u) {
+        w = x;
+        break;
+      }
+    limbs_mul_small(E, w);  // E_j = (P/m_j) w_j < P
+    for (int l = 0; l < kMaxCrtLimbs; ++l) K.pe[j][l] = E.w[l];
+    K.pfrac[j] = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + m / 2) / m);
+  }
   return K;
 }
 

@@ -65,6 +65,15 @@ struct CrtConst {
   uint32_t frac[kMaxModuli];  // round(2^32 w_k / p_k): e_k / P in 0.32 fixed point
   uint32_t e[kMaxModuli][kMaxCrtLimbs];  // e_k, little-endian 32-bit limbs
   uint32_t P[kMaxCrtLimbs];
+  // Moduli taken in pairs (2j, 2j+1) with m_j = p_2j p_2j+1: the pair's
+  // residue r_j = (c_2j u_j0 + c_2j+1 u_j1) mod m_j (u_j0 = 1 mod p_2j and 0 mod
+  // p_2j+1, u_j1 the other way round) has CRT basis vector E_j = e_2j + e_2j+1
+  // (mod P), and E_j / P = w_j / m_j.
+  uint32_t pm[kMaxModuli / 2];
+  uint32_t pu[kMaxModuli / 2][2];
+  uint32_t pmagic[kMaxModuli / 2];  // ceil(2^42 / m_j): floor(t / m_j) = umulhi(t, pmagic) >> 10 for t < 2^25
+  uint32_t pfrac[kMaxModuli / 2];   // round(2^32 w_j / m_j)
+  uint32_t pe[kMaxModuli / 2][kMaxCrtLimbs];
   int n;
 };
 
