@@ -11,7 +11,7 @@
 namespace ozk {
 
 constexpr int kMaxModuli = 20;
-constexpr int kKBlock = 64;  // K elements (bf16) per smem row: 128 bytes, one swizzle row
+constexpr int kKBlock = 64;  // K elements (fp16) per smem row: 128 bytes, one swizzle row
 constexpr int kNumSmsFallback = 148;
 
 // Moduli in the order they are consumed: pairwise coprime integers <= 256,

@@ -5,7 +5,7 @@
 // registers per thread and the Tensor pipe at 7.5%).
 //
 // GB300 (sm_103a) has no tcgen05 kind::i8, so the residues (integers in
-// [-128, 127]) are fed to the bf16 tensor cores, where they are exact: every
+// [-128, 127]) are fed to the fp16 tensor cores, where they are exact: every
 // product is an integer below 2^14 in magnitude and every fp32 partial sum of
 // one 256-term chunk stays below 2^22, so the fp32 accumulator in TMEM holds
 // the chunk's exact integer sum.  The epilogue warps read each chunk out of
@@ -34,7 +34,7 @@ __device__ int g_status;  // latched device-side faults, read by ozk_stream_stat
 namespace {
 
 constexpr int BM = kTileM, BN = kTileN;
-constexpr int BK = 64;       // K elements (bf16) per pipeline stage: one swizzle row
+constexpr int BK = 64;       // K elements (fp16) per pipeline stage: one swizzle row
 constexpr int kStages = 4;   // smem ring depth
 static_assert(kKBlock % BK == 0, "slices are padded to whole stages");
 constexpr int kSwizzleBytes = BK * 2;                  // 128-byte or 64-byte swizzle
@@ -58,7 +58,12 @@ static_assert(kCols % 32 == 0, "the drain moves 32 columns per tcgen05.ld");
 // two BN-column fp32 accumulators, allocated as a power of two >= 32 columns
 constexpr uint32_t kTmemCols = (2 * BN <= 256) ? 256u : 512u;
 static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators fit the allocation");
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+// mbarriers after the ring: full and empty per stage, two accumulator-full,
+// two accumulator-empty, one drain; then the TMEM address and the abort flag
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr size_t kBarBytes = 256;
+static_assert(8 * kNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 50000000ull;
 
@@ -68,9 +73,9 @@ constexpr float kMagic = 12582912.0f;
 constexpr uint32_t kMagicBits = 0x4B400000u;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0),
+// A and B fp16 (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+constexpr uint32_t kIdesc = (1u << 4) |
                             (static_cast<uint32_t>(BN >> 3) << 17) |
                             (static_cast<uint32_t>(BM >> 4) << 24);
 
@@ -210,7 +215,7 @@ __device__ __forceinline__ uint64_t smem_desc_swizzled(uint32_t addr) {
          (static_cast<uint64_t>((8 * kSwizzleBytes) >> 4) << 32) | (1ull << 46) | (kLayoutType << 61);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -422,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t da = smem_desc_swizzled(smem_u32(sA + stage * kABytes));
             const uint64_t db = smem_desc_swizzled(smem_u32(sB + stage * kBBytes));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 bf16 = 32 bytes per MMA
-              mma_bf16(d, da + 2ull * kk, db + 2ull * kk, kIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 fp16 = 32 bytes per MMA
+              mma_f16(d, da + 2ull * kk, db + 2ull * kk, kIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
             mma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs are done
           }
           __syncwarp();
@@ -547,7 +552,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D view of bf16 slices (row stride kpad, modulus stride plane elements),
+// 3-D view of fp16 slices (row stride kpad, modulus stride plane elements),
 // box BK (k) x box_rows x 1.
 bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t kpad,
                     int64_t plane, int n, uint32_t box_rows) {
@@ -558,7 +563,7 @@ bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kpad) * 2, static_cast<cuuint64_t>(plane) * 2};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              kSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -44,15 +44,16 @@ __device__ __forceinline__ uint64_t load1_u64(const double* p) {
 // Exponent scan.  For non-negative doubles the bit pattern orders like the
 // value, so max |x| is a max over 63-bit integers; Inf/NaN sort above every
 // finite value.  Blocks [0, a_blocks) scan rows of A (one warp per row
-// segment), the rest scan columns of B (one thread per 1 or 4 columns over a
-// row segment); partial maxima meet in amax through 64-bit atomicMax.
+// segment), the rest scan columns of B (32 threads of 1 or 4 columns each, 8
+// row groups over a row segment, reduced in shared memory); partial maxima
+// meet in amax through 64-bit atomicMax.
 // ---------------------------------------------------------------------------
 struct ScanParams {
   const double* A;
   const double* B;
   int64_t lda, ldb, M, N, K;
   int64_t a_seg, a_segs, a_blocks;  // rows: 8 per block, a_segs segments of a_seg
-  int64_t b_seg, b_segs, b_cols;    // columns per block = 256 * b_cols
+  int64_t b_seg, b_segs, b_cols;    // columns per block = 32 * b_cols, rows per block = b_seg
   int a_vec, b_vec;                 // 32-byte loads possible
   uint64_t* amax;                   // [M + N]
 };
@@ -83,35 +84,46 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
     m = warp_max_u64(m);
     if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + row), m);
   } else {
+    // A block of B: 32 column threads (b_cols columns each) x 8 row groups
+    // over a row segment; the row groups meet in shared memory, so each
+    // column takes one atomic per block.
+    __shared__ uint64_t red[kScanThreads / 32][32 * 4];
     const int64_t b = bid - sp.a_blocks;
     const int64_t cgrp = b / sp.b_segs;
     const int64_t k0 = (b % sp.b_segs) * sp.b_seg;
     const int64_t k1 = min(sp.K, k0 + sp.b_seg);
-    const int64_t c = (cgrp * kScanThreads + threadIdx.x) * sp.b_cols;
-    if (c >= sp.N) return;
-    uint64_t* out = sp.amax + sp.M + c;
-    if (sp.b_vec && c + 3 < sp.N) {
-      uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    const int lane = threadIdx.x & 31, rg = threadIdx.x >> 5;
+    constexpr int kRowGroups = kScanThreads / 32;
+    const int64_t c = (cgrp * 32 + lane) * sp.b_cols;
+    uint64_t m[4] = {0, 0, 0, 0};
+    if (c < sp.N) {
+      if (sp.b_vec && c + 3 < sp.N) {
 #pragma unroll 4
-      for (int64_t k = k0; k < k1; ++k) {
-        uint64_t v[4];
-        load4_u64(sp.B + k * sp.ldb + c, v);
-        m0 = umax64(m0, v[0] & kAbsMask);
-        m1 = umax64(m1, v[1] & kAbsMask);
-        m2 = umax64(m2, v[2] & kAbsMask);
-        m3 = umax64(m3, v[3] & kAbsMask);
+        for (int64_t k = k0 + rg; k < k1; k += kRowGroups) {
+          uint64_t v[4];
+          load4_u64(sp.B + k * sp.ldb + c, v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m[j] = umax64(m[j], v[j] & kAbsMask);
+        }
+      } else {
+        for (int j = 0; j < 4 && j < sp.b_cols && c + j < sp.N; ++j) {
+#pragma unroll 4
+          for (int64_t k = k0 + rg; k < k1; k += kRowGroups)
+            m[j] = umax64(m[j], load1_u64(sp.B + k * sp.ldb + c + j) & kAbsMask);
+        }
       }
-      if (m0) atomicMax(reinterpret_cast<unsigned long long*>(out), m0);
-      if (m1) atomicMax(reinterpret_cast<unsigned long long*>(out + 1), m1);
-      if (m2) atomicMax(reinterpret_cast<unsigned long long*>(out + 2), m2);
-      if (m3) atomicMax(reinterpret_cast<unsigned long long*>(out + 3), m3);
-    } else {
-      const int64_t cend = min(sp.N, c + sp.b_cols);
-      for (int64_t cc = c; cc < cend; ++cc) {
-        uint64_t m0 = 0;
-#pragma unroll 4
-        for (int64_t k = k0; k < k1; ++k) m0 = umax64(m0, load1_u64(sp.B + k * sp.ldb + cc) & kAbsMask);
-        if (m0) atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + sp.M + cc), m0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) red[rg][lane * 4 + j] = m[j];
+    __syncthreads();
+    if (rg == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint64_t v = red[0][lane * 4 + j];
+#pragma unroll
+        for (int g = 1; g < kRowGroups; ++g) v = umax64(v, red[g][lane * 4 + j]);
+        if (v && j < sp.b_cols && c + j < sp.N)
+          atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + sp.M + c + j), v);
       }
     }
   }
@@ -145,101 +157,98 @@ __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_
 // Quantisation.  x = (-1)^neg m 2^e exactly (m < 2^53); with sh = e + s the
 // integer is a' = (-1)^neg round(m 2^sh), rounded to nearest with ties to
 // even (a shift and a rounding increment), |a'| <= 2^beta <= 2^72.  a' is
-// kept as NL limbs of 22 bits of its two's complement modulo 2^(22 NL):
-// a' = v - neg * 2^(22 NL) with v = sum_j l_j 2^(22 j), so
-//   a' mod p = (sum_j l_j (2^22j mod p) + neg (p - 2^(22 NL) mod p)) mod p.
-// Three limbs hold every beta <= 64; four the rest.
+// kept offset to a non-negative integer, a'' = a' + 2^(22 NL - 1) < 2^(22 NL),
+// as NL limbs of 22 bits: the two's complement of a' modulo 2^(22 NL) with its
+// top bit flipped.  Then, for every modulus,
+//   a' + h = sum_j l_j (2^22j mod p) + (h - 2^(22 NL - 1))   (mod p),
+// one integer below 2^32 whose canonical residue minus h is the balanced
+// residue.  Three limbs hold every beta <= 64; four the rest.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kMask22 = (1u << 22) - 1;
 
 template <int NL>
-struct Limbs22 {
-  uint32_t l[NL];
-  uint32_t neg;  // 1 when a' < 0
-};
-
-template <int NL>
-__device__ __forceinline__ Limbs22<NL> scale_round(uint64_t bits, int32_t sc) {
+__device__ __forceinline__ void scale_round(uint64_t bits, int32_t sc, uint32_t (&l)[NL]) {
   const uint32_t ex = static_cast<uint32_t>(bits >> 52) & 0x7FFu;
   uint64_t m = bits & 0xFFFFFFFFFFFFFull;
   if (ex) m |= 1ull << 52;
   const int sh = static_cast<int>(ex ? ex : 1u) - 1075 + sc;
   uint64_t lo;
-  uint32_t hi;
-  if (sh >= 64) {
-    lo = 0;
-    hi = static_cast<uint32_t>(m << (sh - 64));
-  } else if (sh > 0) {
-    lo = m << sh;
-    hi = static_cast<uint32_t>(m >> (64 - sh));
+  uint32_t hi = 0;
+  if (sh < 0) {
+    if (sh > -64) {
+      // round(m / 2^r), ties to even: add half - 1 and the kept lowest bit, shift
+      const int r = -sh;
+      const uint64_t lsb = (m >> r) & 1u;
+      lo = (m + ((1ull << (r - 1)) - 1u) + lsb) >> r;
+    } else {  // m 2^sh < 2^-11 rounds to 0
+      lo = 0;
+    }
   } else if (sh == 0) {
     lo = m;
-    hi = 0;
-  } else if (sh > -64) {
-    const int r = -sh;  // 1..63 dropped bits
-    const uint64_t q = m >> r;
-    const uint64_t rem = m & ((1ull << r) - 1);
-    const uint64_t half = 1ull << (r - 1);
-    lo = q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);
-    hi = 0;
-  } else {  // m 2^sh < 2^-11 rounds to 0
+  } else if (sh < 64) {
+    lo = m << sh;
+    hi = static_cast<uint32_t>(m >> (64 - sh));
+  } else {
     lo = 0;
-    hi = 0;
+    hi = static_cast<uint32_t>(m << (sh - 64));
   }
-  Limbs22<NL> a;
-  a.neg = static_cast<uint32_t>(bits >> 63) & ((lo | hi) != 0 ? 1u : 0u);
-  if (a.neg) {  // two's complement of the (hi:lo) magnitude
+  if (bits >> 63) {  // two's complement of the (hi:lo) magnitude
     hi = ~hi + (lo == 0 ? 1u : 0u);
     lo = 0ull - lo;
   }
-  a.l[0] = static_cast<uint32_t>(lo) & kMask22;
-  a.l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
-  a.l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
-  if constexpr (NL == 4) a.l[3] = (hi >> 2) & kMask22;
-  return a;
+  l[0] = static_cast<uint32_t>(lo) & kMask22;
+  l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
+  l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
+  if constexpr (NL == 4) l[3] = (hi >> 2) & kMask22;
+  l[NL - 1] ^= 1u << 21;  // + 2^(22 NL - 1)
 }
 
-// fp32 value v (|v| <= 2^22) from the integer magic + v, exactly.
-constexpr uint32_t kMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
-constexpr float kMagic = 12582912.0f;
-
-// (1.5 * 2^23 + residue) bits for the k-th modulus: the balanced residue
-// r in [-floor(p/2), ceil(p/2) - 1] of a', offset by the magic.
+// Canonical residue of a' + h for the k-th modulus (h = floor(p/2); the
+// balanced residue is this minus h).
 template <int k, int NL>
-__device__ __forceinline__ uint32_t magic_residue(const Limbs22<NL>& a) {
+__device__ __forceinline__ uint32_t shifted_residue(const uint32_t (&l)[NL]) {
   constexpr uint32_t p = modulus_at(k);
   if constexpr (p == 256u) {
-    // the low byte of the two's complement, read as int8
-    return kMagicBits + static_cast<uint32_t>(static_cast<int32_t>(a.l[0] << 24) >> 24);
+    return (l[0] ^ 0x80u) & 0xFFu;  // (a' + 128) mod 256 from the low byte
   } else {
-    constexpr uint32_t h = (p - 1) / 2;  // balanced = canonical of (x + h), minus h
+    constexpr uint32_t h = (p - 1) / 2;
     constexpr uint32_t c1 = pow2_mod(22, p), c2 = pow2_mod(44, p);
+    constexpr uint32_t off = (p - pow2_mod(22 * NL - 1, p)) % p + h;
     if constexpr (NL == 3) {
       // x < 2^22 (1 + 2 * 254) + 254 + 127 < 2^31: the 2^39 magic divides exactly
-      constexpr uint32_t d = (p - pow2_mod(66, p)) % p;
       constexpr uint32_t m39 = static_cast<uint32_t>(((1ull << 39) + p - 1) / p);
-      const uint32_t x = a.l[0] + h + a.l[1] * c1 + a.l[2] * c2 + a.neg * d;
+      const uint32_t x = l[0] + off + l[1] * c1 + l[2] * c2;
       const uint32_t q = __umulhi(x, m39) >> 7;
-      return (kMagicBits - h) + (x - q * p);
+      return x - q * p;
     } else {
       // x < 2^32; the 2^32 magic quotient is exact or one too large
       constexpr uint32_t c3 = pow2_mod(66, p);
-      constexpr uint32_t d = (p - pow2_mod(88, p)) % p;
       constexpr uint32_t mg = magic_of(p);
-      const uint32_t x = a.l[0] + h + a.l[1] * c1 + a.l[2] * c2 + a.l[3] * c3 + a.neg * d;
+      const uint32_t x = l[0] + off + l[1] * c1 + l[2] * c2 + l[3] * c3;
       const uint32_t q = __umulhi(x, mg);
       int32_t r = static_cast<int32_t>(x - q * p);
       r += r < 0 ? static_cast<int32_t>(p) : 0;
-      return (kMagicBits - h) + static_cast<uint32_t>(r);
+      return static_cast<uint32_t>(r);
     }
   }
 }
 
-// Two magic-offset residues to a packed pair of bfloat16 (exact integers).
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t mlo, uint32_t mhi) {
-  const float lo = __uint_as_float(mlo) - kMagic;
-  const float hi = __uint_as_float(mhi) - kMagic;
-  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+// fp16 bits 0x6600 + v are the value 1536 + v for |v| < 512 (fp16 steps by 1
+// in [1024, 2048)); subtracting 1536 leaves v exactly.
+constexpr uint32_t kHalfMagicBits = 0x6600u;
+constexpr uint32_t kNegHalfMagic2 = 0xE600E600u;  // (-1536, -1536) as f16x2
+
+// Two canonical residues of the k-th modulus to a packed pair of fp16
+// balanced residues (exact integers in [-128, 127]).
+template <int k>
+__device__ __forceinline__ uint32_t pack_f16x2(uint32_t rlo, uint32_t rhi) {
+  constexpr uint32_t p = modulus_at(k);
+  constexpr uint32_t h = p == 256u ? 128u : (p - 1) / 2;
+  constexpr uint32_t bias = (kHalfMagicBits - h) * 0x10001u;
+  const uint32_t w = rhi * 0x10000u + rlo + bias;
+  uint32_t out;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(w), "r"(kNegHalfMagic2));
+  return out;
 }
 
 __device__ __forceinline__ void store8_u32(uint16_t* dst, const uint32_t (&w)[8]) {
@@ -313,9 +322,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
 #pragma unroll
     for (int e = 0; e < kQK; ++e) v[e] = 0;
   }
-  Limbs22<NL> x[kQK];
+  uint32_t x[kQK][NL];
 #pragma unroll
-  for (int e = 0; e < kQK; ++e) x[e] = scale_round<NL>(v[e], sc);
+  for (int e = 0; e < kQK; ++e) scale_round<NL>(v[e], sc, x[e]);
   uint16_t* dst = out + row * qp.kpad + k0;
   const int n = qp.n;
   static_for<0, kMaxModuli>([&](auto kc) {
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
       uint32_t w[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        w[e] = pack_bf16x2(magic_residue<k, NL>(x[2 * e]), magic_residue<k, NL>(x[2 * e + 1]));
+        w[e] = pack_f16x2<k>(shifted_residue<k, NL>(x[2 * e]), shifted_residue<k, NL>(x[2 * e + 1]));
       store8_u32(dst + k * plane, w);
     }
   });
@@ -367,10 +376,10 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64
     sp.a_blocks = ((M + 7) / 8) * sp.a_segs;
   }
   if (K > 0 && N > 0) {
-    const int64_t cgroups = (N + kScanThreads * sp.b_cols - 1) / (kScanThreads * sp.b_cols);
-    int64_t segs = (static_cast<int64_t>(sms) * 8 + cgroups - 1) / cgroups;
+    const int64_t cgroups = (N + 32 * sp.b_cols - 1) / (32 * sp.b_cols);
+    int64_t segs = (static_cast<int64_t>(sms) * 4 + cgroups - 1) / cgroups;
     int64_t seg = (K + segs - 1) / segs;
-    if (seg < 16) seg = 16;
+    seg = seg < 64 ? 64 : ((seg + 7) / 8) * 8;
     sp.b_seg = seg;
     sp.b_segs = (K + seg - 1) / seg;
     b_blocks = cgroups * sp.b_segs;

@@ -163,7 +163,7 @@ int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* A, int64_t 
  * balanced int8 conversion").  For each modulus p and element:
  * a'_ik = a_ik 2^s_i rounded to the nearest integer (ties to even) and
  * r = sym(a' mod p) in [-floor(p/2), ceil(p/2)-1],
- * stored as bfloat16 (exact for these integers) at
+ * stored as IEEE binary16 (fp16; exact for these integers) at
  * a_slices[(p * M + i) * kpad + k]; columns K..kpad-1 are zero.
  * kpad = ozk_kpad(K); a_slices must be 32-byte aligned.  Rows with
  * s_i = OZK_SCALE_NONFINITE are zero.  Returns OZK_ERR_UNSUPPORTED when
@@ -179,7 +179,7 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb,
                    const int32_t* t, int n_moduli, uint16_t* b_slices,
                    ozk_stream_t stream);
 
-/* One integer GEMM per modulus ("INT8 GEMM", run on bf16 tensor cores: every
+/* One integer GEMM per modulus ("INT8 GEMM", run on fp16 tensor cores: every
  * product and every partial sum of 256 terms is an exact fp32 integer) with
  * the mod reduction fused into its epilogue.
  *  out_kind 0: out is uint8 [n][M][ldo], c = (sum_k ra rb) mod p in [0, p);

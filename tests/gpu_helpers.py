@@ -27,10 +27,9 @@ def ld_of(t: torch.Tensor) -> int:
     return max(t.stride(0), t.size(1), 1)
 
 
-def bf16_to_int(bits: np.ndarray) -> np.ndarray:
-    """Integers held in bfloat16 bit patterns (exact for |v| <= 256)."""
-    u = bits.astype(np.uint16).astype(np.uint32) << 16
-    f = u.view(np.float32)
+def f16_to_int(bits: np.ndarray) -> np.ndarray:
+    """Integers held in IEEE binary16 bit patterns (exact for |v| <= 2048)."""
+    f = np.ascontiguousarray(bits).astype(np.uint16).view(np.float16).astype(np.float64)
     assert np.all(f == np.round(f))
     return f.astype(np.int64)
 

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from fp64_gemm_emulation_exponent_gb300 import ozk, workloads
-from gpu_helpers import (bf16_to_int, dev, dgemm, ld_of, run_combine, run_gemm, run_lift,
+from gpu_helpers import (f16_to_int, dev, dgemm, ld_of, run_combine, run_gemm, run_lift,
                          run_quantize, run_scale, same_bits, strided)
 
 pytestmark = pytest.mark.gpu
@@ -57,8 +57,8 @@ def check_stages(A, B, n, splits=1):
     rb = oracle.residues(Bp, n)  # n x K x N
     ga = a_sl.cpu().numpy().view(np.uint16)
     gb = b_sl.cpu().numpy().view(np.uint16)
-    assert np.array_equal(bf16_to_int(ga[:, :, :K]), ra.astype(np.int64))
-    assert np.array_equal(bf16_to_int(gb[:, :, :K]), rb.transpose(0, 2, 1).astype(np.int64))
+    assert np.array_equal(f16_to_int(ga[:, :, :K]), ra.astype(np.int64))
+    assert np.array_equal(f16_to_int(gb[:, :, :K]), rb.transpose(0, 2, 1).astype(np.int64))
     assert np.all(ga[:, :, K:] == 0) and np.all(gb[:, :, K:] == 0)
     # 3. per-modulus exact int32 sums, and their reduction mod p
     raw, cmod = oracle.gemm_mod(ra, rb, n)
