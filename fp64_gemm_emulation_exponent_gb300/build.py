@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libozk.so")
-SOURCES = ["ozk_api.cu", "scan_quantize.cu", "residue_gemm.cu", "crt_combine.cu"]
+SOURCES = ["ozk_api.cu", "scan_quantize.cu", "residue_gemm.cu", "crt_combine.cu", "crt_fixed.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

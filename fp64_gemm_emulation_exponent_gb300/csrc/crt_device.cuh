@@ -1,0 +1,432 @@
+// Device code of the CRT combine: CRT reconstruction, symmetric lift, undo
+// scaling and FP64 write (the last three stages of the Ozaki-II pipeline on
+// the "Day 12" page, section
+// "Profile 不能只看 Tensor Core").  That page's section "Combine kernel
+// 的瓶頸又不一樣" measures its own combine at ~85% of the FP64 pipe and warns
+// that more registers per thread made it slower; on GB300 the FP64 pipe is
+// slow, so this kernel is integer-only:
+//
+//   X = sum_j r_j E_j - q P  (mod 2^(32 NL)),
+//
+// over the moduli taken in pairs: r_j = (c_2j u_j0 + c_2j+1 u_j1) mod m_j is
+// the residue of the pair modulus m_j = p_2j p_2j+1 (two byte residues into one
+// 16-bit one with three integer multiplies), E_j = e_2j + e_2j+1 mod P its CRT
+// basis vector; an odd last modulus enters on its own.  Pairing halves the
+// 64-bit multiply-accumulates, which bound this kernel on the FMA-heavy pipe.
+// The limb sums of r_j E_j are accumulated in 64 bits without carries and
+// -q P is folded in as q (2^(32 NL) - P).  q = round(sum_j r_j w_j / m_j) is
+// estimated in 32.32 fixed point (error below 2^18 / 2^32); the rare outputs
+// whose estimate lies within 2^20 / 2^32 of a rounding boundary get an exact
+// correction.  The lifted X in [-P/2, P/2) is then scaled by 2^-(s_i + t_j)
+// and rounded to nearest-even in integer arithmetic (a short path for normal
+// results, a general one for subnormals and overflow).
+#pragma once
+
+#include "ozk_internal.h"
+
+namespace ozk {
+namespace {
+
+constexpr uint64_t kQuietNaN = 0x7FF8000000000000ull;
+constexpr uint64_t kInfBits = 0x7FF0000000000000ull;
+
+__device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic, uint32_t bias) {
+  const uint32_t u = static_cast<uint32_t>(x) + bias;
+  const uint32_t q = __umulhi(u, magic);
+  int32_t r = static_cast<int32_t>(u - q * p);
+  r += r < 0 ? static_cast<int32_t>(p) : 0;
+  return static_cast<uint32_t>(r);
+}
+
+// a += P, or a -= P when subtract (two's complement, NL limbs).
+template <int NL>
+__device__ __forceinline__ void add_signed_P(uint32_t (&a)[NL], const CrtConst& K, bool subtract) {
+  uint64_t carry = subtract ? 1u : 0u;
+#pragma unroll
+  for (int l = 0; l < NL; ++l) {
+    const uint32_t pl = subtract ? ~K.P[l] : K.P[l];
+    const uint64_t v = static_cast<uint64_t>(a[l]) + pl + carry;
+    a[l] = static_cast<uint32_t>(v);
+    carry = v >> 32;
+  }
+}
+
+template <int NL>
+__device__ __forceinline__ bool is_negative(const uint32_t (&a)[NL]) {
+  return (a[NL - 1] >> 31) != 0;
+}
+
+// Exact symmetric lift for outputs whose quotient estimate was ambiguous:
+// move X into [-P/2, P/2) by one P if needed.
+template <int NL>
+__device__ __forceinline__ void exact_lift(uint32_t (&X)[NL], const CrtConst& K) {
+  uint32_t t[NL];  // 2X
+#pragma unroll
+  for (int l = 0; l < NL; ++l) {
+    const uint32_t hi = l ? (X[l - 1] >> 31) : 0u;
+    t[l] = (X[l] << 1) | hi;
+  }
+  // 2X - P >= 0  <=>  X >= P/2
+  uint32_t t2[NL];
+#pragma unroll
+  for (int l = 0; l < NL; ++l) t2[l] = t[l];
+  add_signed_P<NL>(t2, K, true);
+  if (!is_negative<NL>(t2)) {
+    add_signed_P<NL>(X, K, true);
+    return;
+  }
+  // t = 2X + P: X < -P/2  <=>  t < 0
+  add_signed_P<NL>(t, K, false);
+  if (is_negative<NL>(t)) add_signed_P<NL>(X, K, false);
+}
+
+// RN-even double of X * 2^-S for a two's-complement NL-limb integer X,
+// handled as up to three 64-bit words.
+template <int NL>
+__device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&X)[NL], int S) {
+  constexpr int NW = (NL + 1) / 2;
+  uint64_t w[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const uint32_t lo = X[2 * i];
+    const uint32_t hi = (2 * i + 1 < NL) ? X[2 * i + 1] : ((X[NL - 1] >> 31) ? 0xFFFFFFFFu : 0u);
+    w[i] = (static_cast<uint64_t>(hi) << 32) | lo;
+  }
+  const bool neg = (w[NW - 1] >> 63) != 0;
+  if (neg) {  // magnitude
+    uint64_t c = 1;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const uint64_t v = ~w[i] + c;
+      c = (c && v == 0) ? 1u : 0u;
+      w[i] = v;
+    }
+  }
+  uint64_t hi, mid, lo;
+  int base;
+  if (NW == 3 && w[NW - 1] != 0) {
+    hi = w[NW - 1];
+    mid = w[NW > 1 ? NW - 2 : 0];
+    lo = w[0];
+    base = 128;
+  } else if (NW >= 2 && w[NW >= 2 ? 1 : 0] != 0) {
+    hi = w[NW >= 2 ? 1 : 0];
+    mid = w[0];
+    lo = 0;
+    base = 64;
+  } else {
+    hi = w[0];
+    mid = 0;
+    lo = 0;
+    base = 0;
+  }
+  if (hi == 0) return 0ull;  // exact zero: +0
+  const int lz = __clzll(static_cast<long long>(hi));
+  const uint64_t win = lz ? (hi << lz) | (mid >> (64 - lz)) : hi;
+  const bool sticky = ((lz ? (mid << lz) : mid) | lo) != 0;  // bits below the window
+  const int h = base + 63 - lz;                              // leading bit of |X|
+  const int e = h - S;                                       // |X| 2^-S in [2^e, 2^(e+1))
+  uint64_t bits;
+  if (e > 1023) {
+    bits = kInfBits;
+  } else {
+    // drop sh >= 11 bits of the window: 53 significant bits, fewer below 2^-1022
+    const int sh = e >= -1022 ? 11 : 11 + (-1022 - e);
+    uint64_t q;
+    uint32_t rb, st;
+    if (sh >= 65) {
+      q = 0;
+      rb = 0;
+      st = 1;
+    } else if (sh == 64) {
+      q = 0;
+      rb = static_cast<uint32_t>(win >> 63);
+      st = ((win << 1) != 0) | sticky;
+    } else {
+      q = win >> sh;
+      rb = static_cast<uint32_t>(win >> (sh - 1)) & 1u;
+      st = ((win & ((1ull << (sh - 1)) - 1)) != 0) | sticky;
+    }
+    q += rb & (st | static_cast<uint32_t>(q & 1u));
+    // lowest kept bit has weight 2^(e + sh - 63); the biased exponent field
+    // base is e + sh + 1011 (0 in the subnormal range); a rounding carry
+    // into bit 53 bumps the exponent by itself
+    const uint64_t E0 = static_cast<uint64_t>(e + sh + 1011);
+    bits = (E0 << 52) + q;
+    if (bits >= kInfBits) bits = kInfBits;
+  }
+  return bits | (static_cast<uint64_t>(neg) << 63);
+}
+
+// Fast path of round_scaled_bits for |X| >= 2^(32(NL-2)) with a normal
+// result: a 64-bit window from the top two nonzero-headed limbs, 53 bits
+// kept, round to nearest even with the bits below as sticky.  Returns false
+// (and leaves *out alone) when the slow path must decide.
+template <int NL>
+__device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S, uint64_t* out) {
+  const uint32_t sgn = X[NL - 1] >> 31;
+  const uint32_t flip = 0u - sgn;
+  uint32_t m[NL];
+  if constexpr (NL == 4) {  // |X| = (X ^ flip) + sgn, one carry chain
+    asm("{\n\t"
+        "add.cc.u32 %0, %4, %8;\n\t"
+        "addc.cc.u32 %1, %5, 0;\n\t"
+        "addc.cc.u32 %2, %6, 0;\n\t"
+        "addc.u32 %3, %7, 0;\n\t}"
+        : "=r"(m[0]), "=r"(m[1]), "=r"(m[2]), "=r"(m[3])
+        : "r"(X[0] ^ flip), "r"(X[1] ^ flip), "r"(X[2] ^ flip), "r"(X[3] ^ flip), "r"(sgn));
+  } else {
+    uint32_t c = sgn;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const uint32_t x = X[l] ^ flip;
+      m[l] = x + c;
+      c = (c && m[l] == 0u) ? 1u : 0u;
+    }
+  }
+  const bool top = m[NL - 1] != 0u;
+  const uint32_t t2 = top ? m[NL - 1] : m[NL - 2];
+  const uint32_t t1 = top ? m[NL - 2] : m[NL - 3];
+  uint32_t t0, st;
+  if constexpr (NL >= 4) {
+    uint32_t below = 0;  // OR of the limbs under t0 when the top limb leads
+#pragma unroll
+    for (int l = 0; l + 3 < NL; ++l) below |= m[l];
+    uint32_t below2 = 0;  // same when limb NL-2 leads
+#pragma unroll
+    for (int l = 0; l + 4 < NL; ++l) below2 |= m[l];
+    t0 = top ? m[NL - 3] : m[NL - 4];
+    st = top ? below : below2;
+  } else {
+    t0 = top ? m[0] : 0u;
+    st = 0u;
+  }
+  if (t2 == 0u) return false;
+  const int lz = __clz(t2);
+  const uint32_t hi = __funnelshift_l(t1, t2, lz);
+  const uint32_t mid = __funnelshift_l(t0, t1, lz);
+  const uint32_t lo = t0 << lz;
+  const int e = (top ? 32 * (NL - 1) : 32 * (NL - 2)) + 31 - lz - S;  // |X| 2^-S in [2^e, 2^(e+1))
+  if (e < -1022 || e > 1023) return false;
+  const uint32_t sig_lo = __funnelshift_r(mid, hi, 11);
+  const uint32_t sig_hi = hi >> 11;
+  const uint32_t rb = (mid >> 10) & 1u;
+  const uint32_t sticky = ((mid & 0x3FFu) | lo | st) != 0u ? 1u : 0u;
+  const uint32_t inc = rb & (sticky | (sig_lo & 1u));
+  // the significand carries the leading one at bit 52: exponent field e + 1022
+  // plus one; a rounding carry into bit 53 bumps it once more (to Inf at the top)
+  const uint64_t bits = (static_cast<uint64_t>(e + 1022) << 52) +
+                        ((static_cast<uint64_t>(sig_hi) << 32) | sig_lo) + inc;
+  *out = bits | (static_cast<uint64_t>(sgn) << 63);
+  return true;
+}
+
+__device__ __forceinline__ void store4_f64(double* dst, const uint64_t (&b)[4]) {
+  asm volatile("st.global.cs.v4.b64 [%0], {%1, %2, %3, %4};" ::"l"(dst), "l"(b[0]), "l"(b[1]), "l"(b[2]),
+               "l"(b[3])
+               : "memory");
+}
+
+template <int G>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[G]) {
+  if constexpr (G == 1) {
+    w[0] = __ldcs(reinterpret_cast<const unsigned int*>(p));
+  } else if constexpr (G == 2) {
+    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  }
+}
+
+// One thread per 4G consecutive columns of one row, in G groups of 4.
+// NFIX > 0 fixes the moduli count at compile time (it must equal K.n).
+//  IN_KIND 0: uint8 residues, modulus k at in + k * plane, row i at + i * ldi;
+//  IN_KIND 1: int32 partial sums, split sp and modulus k at (sp * n + k) * plane.
+// All residue words are loaded before any arithmetic so that the loads of a
+// thread are in flight together.
+template <int NL, int IN_KIND, bool LIMBS, int G, int NFIX>
+__global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, int64_t ldi,
+                                                  int64_t plane, int64_t M, int64_t N, int splits,
+                                                  const int32_t* __restrict__ s,
+                                                  const int32_t* __restrict__ t,
+                                                  double* __restrict__ C, int64_t ldc,
+                                                  uint32_t* __restrict__ Xout, const CrtConst K) {
+  constexpr int W = 4 * G;  // columns per thread
+  const int64_t groups = (N + W - 1) / W;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= M * groups) return;
+  int64_t i, jt;
+  if (M * groups <= 0x7FFFFFFF) {
+    const uint32_t g32 = static_cast<uint32_t>(gid), gr = static_cast<uint32_t>(groups);
+    const uint32_t i32 = g32 / gr;
+    i = i32;
+    jt = static_cast<int64_t>(g32 - i32 * gr) * W;
+  } else {
+    i = gid / groups;
+    jt = (gid - i * groups) * W;
+  }
+  const int n = NFIX ? NFIX : K.n;  // a compile-time moduli count lets every loop unroll exactly
+
+  uint32_t cw[kMaxModuli][G];
+  if constexpr (IN_KIND == 0) {
+    const uint8_t* base = static_cast<const uint8_t*>(in) + i * ldi + jt;
+    static_for<0, kMaxModuli>([&](auto kc) {
+      constexpr int k = decltype(kc)::value;
+      if (k < n) load_words<G>(base + k * plane, cw[k]);
+    });
+  } else {
+    static_for<0, kMaxModuli>([&](auto kc) {
+      constexpr int k = decltype(kc)::value;
+      if (k < n) {
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          int32_t sum[4] = {0, 0, 0, 0};
+          for (int sp = 0; sp < splits; ++sp) {
+            const int4 v = __ldcs(reinterpret_cast<const int4*>(static_cast<const int32_t*>(in) +
+                                                                (static_cast<int64_t>(sp) * n + k) * plane +
+                                                                i * ldi + jt + 4 * gg));
+            sum[0] += v.x;
+            sum[1] += v.y;
+            sum[2] += v.z;
+            sum[3] += v.w;
+          }
+          cw[k][gg] = mod_p(sum[0], K.p[k], K.magic[k], K.bias[k]) |
+                      (mod_p(sum[1], K.p[k], K.magic[k], K.bias[k]) << 8) |
+                      (mod_p(sum[2], K.p[k], K.magic[k], K.bias[k]) << 16) |
+                      (mod_p(sum[3], K.p[k], K.magic[k], K.bias[k]) << 24);
+        }
+      }
+    });
+  }
+  const int32_t si = LIMBS ? 0 : s[i];
+  uint32_t Pn[NL];  // 2^(32 NL) - P: X = sum c_k e_k + q Pn (mod 2^(32 NL))
+  {
+    uint32_t c = 1;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t v = static_cast<uint64_t>(~K.P[l]) + c;
+      Pn[l] = static_cast<uint32_t>(v);
+      c = static_cast<uint32_t>(v >> 32);
+    }
+  }
+
+#pragma unroll 1
+  for (int gg = 0; gg < G; ++gg) {
+    const int64_t j0 = jt + 4 * gg;
+    if (j0 >= N) break;
+    int32_t tj[4] = {0, 0, 0, 0};
+    if constexpr (!LIMBS) {
+      if (j0 + 3 < N) {
+        const int4 t4 = *reinterpret_cast<const int4*>(t + j0);
+        tj[0] = t4.x;
+        tj[1] = t4.y;
+        tj[2] = t4.z;
+        tj[3] = t4.w;
+      } else {
+#pragma unroll
+        for (int o = 0; o < 4; ++o) tj[o] = (j0 + o < N) ? t[j0 + o] : 0;
+      }
+    }
+    // limb sums without carries; the top limb only matters modulo 2^32
+    uint64_t acc[4][NL - 1];
+    uint32_t acctop[4];
+    uint64_t qacc[4];
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      qacc[o] = 0;
+      acctop[o] = 0;
+#pragma unroll
+      for (int l = 0; l < NL - 1; ++l) acc[o][l] = 0;
+    }
+    // moduli in pairs: one 16-bit pair residue per (pair, output)
+    static_for<0, kMaxModuli / 2>([&](auto jc) {
+      constexpr int j = decltype(jc)::value;
+      if (2 * j + 1 < n) {
+        uint32_t wa = cw[2 * j][0], wb = cw[2 * j + 1][0];
+#pragma unroll
+        for (int x = 1; x < G; ++x) {
+          wa = gg == x ? cw[2 * j][x] : wa;
+          wb = gg == x ? cw[2 * j + 1][x] : wb;
+        }
+#pragma unroll
+        for (int o = 0; o < 4; ++o) {
+          const uint32_t ca = __byte_perm(wa, 0u, 0x4440 + o);
+          const uint32_t cb = __byte_perm(wb, 0u, 0x4440 + o);
+          const uint32_t t = ca * K.pu[j][0] + cb * K.pu[j][1];  // < 2^25
+          const uint32_t r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
+          qacc[o] += static_cast<uint64_t>(r) * K.pfrac[j];
+#pragma unroll
+          for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(r) * K.pe[j][l];
+          acctop[o] += r * K.pe[j][NL - 1];
+        }
+      }
+    });
+    if (n & 1) {  // the last modulus on its own
+      static_for<0, kMaxModuli>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        if (k == n - 1) {
+          uint32_t word = cw[k][0];
+#pragma unroll
+          for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
+#pragma unroll
+          for (int o = 0; o < 4; ++o) {
+            const uint32_t c = __byte_perm(word, 0u, 0x4440 + o);
+            qacc[o] += static_cast<uint64_t>(c) * K.frac[k];
+#pragma unroll
+            for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(c) * K.e[k][l];
+            acctop[o] += c * K.e[k][NL - 1];
+          }
+        }
+      });
+    }
+    uint64_t outbits[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      const uint64_t shifted = qacc[o] + 0x80000000ull;
+      const uint32_t q = static_cast<uint32_t>(shifted >> 32);
+      const uint32_t frac = static_cast<uint32_t>(shifted);
+      uint32_t X[NL];
+      uint64_t carry = 0;
+#pragma unroll
+      for (int l = 0; l < NL - 1; ++l) {
+        const uint64_t v = acc[o][l] + static_cast<uint64_t>(q) * Pn[l] + carry;
+        X[l] = static_cast<uint32_t>(v);
+        carry = v >> 32;
+      }
+      X[NL - 1] = acctop[o] + q * Pn[NL - 1] + static_cast<uint32_t>(carry);
+      if (frac < (1u << 20) || frac > ~(1u << 20)) exact_lift<NL>(X, K);
+      if constexpr (LIMBS) {
+        if (j0 + o < N) {
+          uint32_t* dst = Xout + (i * N + j0 + o) * OZK_LIMBS;
+          const uint32_t ext = is_negative<NL>(X) ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+          for (int l = 0; l < OZK_LIMBS; ++l) dst[l] = l < NL ? X[l] : ext;
+        }
+      } else {
+        if (si == OZK_SCALE_NONFINITE || tj[o] == OZK_SCALE_NONFINITE)
+          outbits[o] = kQuietNaN;
+        else if (!round_scaled_fast<NL>(X, si + tj[o], &outbits[o]))
+          outbits[o] = round_scaled_bits<NL>(X, si + tj[o]);
+      }
+    }
+    if constexpr (!LIMBS) {
+      double* dst = C + i * ldc + j0;
+      if (j0 + 3 < N && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+        store4_f64(dst, outbits);
+      } else {
+#pragma unroll
+        for (int o = 0; o < 4; ++o)
+          if (j0 + o < N) __stcs(reinterpret_cast<unsigned long long*>(dst + o), outbits[o]);
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace ozk

@@ -108,6 +108,34 @@ def test_split_k_partials_sum_to_the_exact_product(splits):
     check_stages(A, B, 14, splits=splits)
 
 
+@pytest.mark.parametrize("n", list(range(2, 21)))
+def test_crt_wide_outputs_every_moduli_count(n):
+    """Outputs wide enough for the kernels compiled per moduli count: random
+    residues (any residue vector is a valid CRT input), scales that give
+    normal, subnormal, underflowing, overflowing and NaN results; sampled
+    outputs against the oracle's CRT and rounding."""
+    M, N = 2048, 640
+    rng = np.random.default_rng(100 + n)
+    res = np.stack([rng.integers(0, p, size=(M, N), dtype=np.uint8) for p in oracle.moduli(n)])
+    s = rng.integers(-200, 200, M).astype(np.int32)
+    t = rng.integers(-200, 200, N).astype(np.int32)
+    s[10:20] = 1050 - 8 * n   # |X| 2^-(s+t) near the subnormal range
+    s[20:30] = -1000 + 8 * n  # near overflow
+    s[3] = oracle.NONFINITE
+    t[5] = oracle.NONFINITE
+    C = run_combine(dev(res), 0, N, 1, dev(s), dev(t), M, N, n).cpu().numpy()
+    ii = np.concatenate([rng.integers(0, M, 3000), np.arange(10, 30).repeat(20), np.full(50, 3)])
+    jj = np.concatenate([rng.integers(0, N, 3000), rng.integers(0, N, 400), rng.integers(0, N, 50)])
+    ii = np.concatenate([ii, rng.integers(0, M, 50)])
+    jj = np.concatenate([jj, np.full(50, 5)])
+    X = oracle.crt(res[:, ii, jj], n)
+    nonfinite = (s[ii] == oracle.NONFINITE) | (t[jj] == oracle.NONFINITE)
+    S = np.where(nonfinite, 0, s[ii].astype(np.int64) + t[jj]).astype(np.int32)
+    want = np.where(nonfinite, np.nan, oracle.round_scaled(X, S))
+    assert same_bits(C[ii, jj], want)
+    assert np.isnan(C[3]).all() and np.isnan(C[:, 5]).all()
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 700, 3), (513, 1, 77), (256, 256, 256), (129, 257, 1025)])
 @pytest.mark.parametrize("n", [8, 11, 14, 17, 20])
 def test_dgemm_bit_exact(M, N, K, n):
