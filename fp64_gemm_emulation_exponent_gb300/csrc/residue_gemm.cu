@@ -6,17 +6,21 @@
 //
 // GB300 (sm_103a) has no tcgen05 kind::i8, so the residues (integers in
 // [-128, 127]) are fed to the fp16 tensor cores, where they are exact: every
-// product is an integer below 2^14 in magnitude and every fp32 partial sum of
-// one 256-term chunk stays below 2^22, so the fp32 accumulator in TMEM holds
-// the chunk's exact integer sum.  The epilogue warps read each chunk out of
-// TMEM and add it into int32 registers (exact for K < 2^17), then reduce mod p
-// once per tile.
+// product is an integer of magnitude at most 2^14, so every fp32 partial sum
+// of a 1024-term chunk is an integer of magnitude at most 2^24 and the fp32
+// accumulator in TMEM holds the chunk's exact integer sum.  The epilogue
+// warps read each chunk out of TMEM, convert it exactly (cvt.rni) and add it
+// into int32 registers (exact for K < 2^17), then reduce mod p once per tile.
+// Short K (below 1024) uses 256-term chunks instead, whose sums (at most
+// 2^22) convert with one fp32 add of 1.5 * 2^23: cheaper per chunk when the
+// drain cannot be spread over a long K.
 //
 // Structure: persistent CTAs (one per SM), warp-specialised.
 //   warp 0      TMA producer: A and B slice tiles into a 4-stage smem ring
-//               (128-byte swizzle), one mbarrier pair per stage.
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and issues tcgen05.mma (M=128, N=256, K=16) from one lane.
+//               (128-byte swizzle), one mbarrier pair per stage; one lane
+//               walks the schedule.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators);
+//               one lane waits and issues tcgen05.mma (M=128, N=256, K=16).
 //   warps 2, 3  idle (they complete warpgroup 0, which hands its registers
 //               to the epilogue through setmaxnreg).
 //   warps 4..11 epilogue: TMEM -> registers -> int32 sums -> mod p -> HBM.
@@ -39,8 +43,12 @@ constexpr int kStages = 4;   // smem ring depth
 static_assert(kKBlock % BK == 0, "slices are padded to whole stages");
 constexpr int kSwizzleBytes = BK * 2;                  // 128-byte or 64-byte swizzle
 constexpr uint64_t kLayoutType = kSwizzleBytes == 128 ? 2 : 4;  // descriptor swizzle code
-constexpr int kChunk = 256;                            // exact fp32 chunk: |sum| <= 2^22
-constexpr int kChunkKB = kChunk / BK;                  // k-blocks per chunk
+// k-blocks per exact chunk: 1024 terms (|sum| <= 2^24, converted with
+// cvt.rni) or 256 terms (|sum| <= 2^22, converted with the 1.5 * 2^23 add)
+template <bool LONG>
+constexpr int chunk_kb() {
+  return (LONG ? 1024 : 256) / BK;
+}
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0: control, 1-2: epilogue
 // Register split between the warpgroups (setmaxnreg).  The kernel launches
@@ -290,22 +298,38 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
 }
 
 // acc[base .. base+31] += the 32 exact chunk sums held as fp32 in v.
+template <bool LONG>
 __device__ __forceinline__ void add_chunk(int32_t (&acc)[kCols], int base, const uint32_t (&v)[32]) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) acc[base + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+  for (int e = 0; e < 32; ++e) {
+    if constexpr (LONG)
+      acc[base + e] += __float2int_rn(__uint_as_float(v[e]));
+    else
+      acc[base + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+  }
 }
 
 // Adds this thread's kCols chunk sums from TMEM into acc, 32 columns per
-// tcgen05.ld, double-buffered: load Q+1 is in flight while load Q (in cur,
-// already landed) is added up.
-template <int Q>
+// tcgen05.ld.  Short chunks double-buffer the loads (load Q+1 in flight while
+// load Q is added up); long chunks, drained a quarter as often, load one
+// block at a time and keep the registers for the conversions.
+template <bool LONG, int Q>
 __device__ __forceinline__ void drain_chunk(int32_t (&acc)[kCols], uint32_t taddr, uint32_t (&cur)[32],
                                             uint32_t (&nxt)[32]) {
-  if constexpr (Q + 1 < kCols / 32) tmem_ld32(taddr + 32 * (Q + 1), nxt);
-  add_chunk(acc, 32 * Q, cur);
-  if constexpr (Q + 1 < kCols / 32) {
-    tmem_wait_ld(nxt);
-    drain_chunk<Q + 1>(acc, taddr, nxt, cur);
+  if constexpr (LONG) {
+    add_chunk<LONG>(acc, 32 * Q, cur);
+    if constexpr (Q + 1 < kCols / 32) {
+      tmem_ld32(taddr + 32 * (Q + 1), cur);
+      tmem_wait_ld(cur);
+      drain_chunk<LONG, Q + 1>(acc, taddr, cur, nxt);
+    }
+  } else {
+    if constexpr (Q + 1 < kCols / 32) tmem_ld32(taddr + 32 * (Q + 1), nxt);
+    add_chunk<LONG>(acc, 32 * Q, cur);
+    if constexpr (Q + 1 < kCols / 32) {
+      tmem_wait_ld(nxt);
+      drain_chunk<LONG, Q + 1>(acc, taddr, nxt, cur);
+    }
   }
 }
 
@@ -318,6 +342,7 @@ __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic,
   return static_cast<uint32_t>(r);
 }
 
+template <bool LONG>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
@@ -336,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accf0 = empty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
+  constexpr int kChunkKB = chunk_kb<LONG>();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -365,86 +391,78 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) regs_dec<kCtrlRegs>();
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    // The whole warp walks the schedule and waits; lane 0 issues the copies.
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued_parity[kStages];
-    for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(u, prm);
-      for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (!warp_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // One thread walks the schedule, waits and issues the copies.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[kStages];
+      for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(u, prm);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
           mbar_expect_tx(full0 + 8 * stage, kStageBytes);
-          tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p,
-                      full0 + 8 * stage);
-          tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, kb * BK, w.nt * BN, w.p,
-                      full0 + 8 * stage);
-        }
-        __syncwarp();
-        issued_parity[stage] = static_cast<int>(phase);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+          tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p, full0 + 8 * stage);
+          tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, kb * BK, w.nt * BN, w.p, full0 + 8 * stage);
+          issued_parity[stage] = static_cast<int>(phase);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    if (!ok && lane == 0) {  // let copies still in flight land before the CTA exits
-      for (int s = 0; s < kStages; ++s)
-        if (issued_parity[s] >= 0)
-          mbar_wait_drain(full0 + 8 * s, static_cast<uint32_t>(issued_parity[s]));
+      if (!ok) {  // let copies still in flight land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (issued_parity[s] >= 0) mbar_wait_drain(full0 + 8 * s, static_cast<uint32_t>(issued_parity[s]));
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // The whole warp walks the schedule and waits; lane 0 issues the MMAs.
-    int stage = 0;
-    uint32_t phase = 0;
-    int ab = 0;
-    uint32_t aphase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(u, prm);
-      for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
-        const int c1 = min(w.kb1, c0 + kChunkKB);
-        if (!warp_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
-        for (int kb = c0; kb < c1; ++kb) {
-          if (!warp_wait(full0 + 8 * stage, phase, abort_flag)) {
+    // One thread walks the schedule, waits and issues the MMAs.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(u, prm);
+        for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
+          const int c1 = min(w.kb1, c0 + kChunkKB);
+          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
+          const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
+          for (int kb = c0; kb < c1; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
             const uint64_t da = smem_desc_swizzled(smem_u32(sA + stage * kABytes));
             const uint64_t db = smem_desc_swizzled(smem_u32(sB + stage * kBBytes));
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 fp16 = 32 bytes per MMA
               mma_f16(d, da + 2ull * kk, db + 2ull * kk, kIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
             mma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs are done
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          __syncwarp();
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          mma_commit(accf0 + 8 * ab);  // chunk sum ready in TMEM buffer ab
+          ab ^= 1;
+          if (ab == 0) aphase ^= 1u;
         }
-        if (!ok) break;
-        if (lane == 0) mma_commit(accf0 + 8 * ab);  // chunk sum ready in TMEM buffer ab
-        __syncwarp();
-        ab ^= 1;
-        if (ab == 0) aphase ^= 1u;
       }
-    }
-    if (lane == 0) {
       mma_commit(drain);  // every issued MMA has finished before TMEM is freed
       mbar_wait_drain(drain, 0);
     }
@@ -476,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t va[32], vb[32];
         tmem_ld32(taddr, va);
         tmem_wait_ld(va);
-        drain_chunk<0>(acc, taddr, va, vb);
+        drain_chunk<LONG, 0>(acc, taddr, va, vb);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce0 + 8 * ab);
@@ -484,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ab == 0) aphase ^= 1u;
       }
       if (!ok) break;
-      const uint32_t offset = static_cast<uint32_t>(nchunks) * kMagicBits;
+      const uint32_t offset = LONG ? 0u : static_cast<uint32_t>(nchunks) * kMagicBits;  // the 1.5 * 2^23 adds
 #pragma unroll
       for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
 
@@ -616,15 +634,18 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
   prm.out = out;
   const int64_t units = static_cast<int64_t>(n) * splits * prm.tiles_m * prm.tiles_n;
   const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
-  cudaError_t e = cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // long chunks once a split holds a full 1024-term chunk
+  const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK >= 1024;
+  auto kernel = long_chunks ? residue_gemm_kernel<true> : residue_gemm_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the pool has the registers: refuse to launch
   // unless the compiled launch register count covers the split exactly.
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, residue_gemm_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-  residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, prm);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, prm);
   return cudaGetLastError();
 }
 
