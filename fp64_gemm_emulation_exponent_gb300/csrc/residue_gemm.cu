@@ -11,22 +11,30 @@
 // accumulator in TMEM holds the chunk's exact integer sum.  The epilogue
 // warps read each chunk out of TMEM, convert it exactly (cvt.rni) and add it
 // into int32 registers (exact for K < 2^17), then reduce mod p once per tile.
-// Short K (below 1024) uses 256-term chunks instead, whose sums (at most
-// 2^22) convert with one fp32 add of 1.5 * 2^23: cheaper per chunk when the
-// drain cannot be spread over a long K.
 //
-// Structure: persistent CTAs (one per SM), warp-specialised.
-//   warp 0      TMA producer: A and B slice tiles into a 4-stage smem ring
-//               (128-byte swizzle), one mbarrier pair per stage; one lane
-//               walks the schedule.
+// Two kernels, chosen by the K of a split:
+//  * K >= 2048: CTA pairs (clusters of two).  The even CTA issues
+//    tcgen05.mma.cta_group::2 (M=256, N=256, K=16): each CTA stages its 128
+//    rows of A and half of the B tile, so a stage is 32 KB per SM, the ring is
+//    6 deep and the shared-memory traffic per MMA is a third lower than with
+//    one CTA per tile.  Both CTAs drain their own 128 accumulator rows.
+//  * K < 2048: one CTA per 128 x 256 tile, 4-stage ring; 1024-term chunks
+//    from K = 1024, below that 256-term chunks (sums at most 2^22) converted
+//    with one fp32 add of 1.5 * 2^23, cheaper per chunk when the drain cannot
+//    be spread over a long K.
+//
+// Structure of both: persistent CTAs (one per SM), warp-specialised.
+//   warp 0      TMA producer: A and B slice tiles into the smem ring (128-byte
+//               swizzle), one mbarrier pair per stage; one lane walks the
+//               schedule.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators);
-//               one lane waits and issues tcgen05.mma (M=128, N=256, K=16).
+//               one lane waits and issues the MMAs (the even CTA of a pair).
 //   warps 2, 3  idle (they complete warpgroup 0, which hands its registers
 //               to the epilogue through setmaxnreg).
 //   warps 4..11 epilogue: TMEM -> registers -> int32 sums -> mod p -> HBM.
 // Every mbarrier wait is bounded (2 s); a wait that runs out latches
-// OZK_ERR_TIMEOUT on the device, makes all roles stop, drains in-flight copies
-// and MMAs, frees TMEM and returns.
+// OZK_ERR_TIMEOUT on the device, makes all roles of the CTA stop, drains
+// in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
 #include "ozk_internal.h"
@@ -72,6 +80,17 @@ constexpr int kNumBars = 2 * kStages + 5;
 constexpr size_t kBarBytes = 256;
 static_assert(8 * kNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+// CTA-pair kernel: each CTA holds 128 rows of A and half of the B tile per
+// stage (32 KB), so the ring is 6 deep in the same shared memory.
+constexpr int kPairMinK = 2048;  // K per split from which CTA pairs run (two long chunks)
+constexpr int kPairM = 2 * BM;  // a CTA pair computes a kPairM x BN tile
+constexpr int kBHalf = BN / 2;  // B rows (tile columns) each CTA of the pair loads
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairBBytes = kBHalf * BK * 2;
+constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;
+constexpr int kPairNumBars = 2 * kPairStages + 5;
+static_assert(8 * kPairNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 50000000ull;
 
@@ -86,6 +105,9 @@ constexpr uint32_t kMagicBits = 0x4B400000u;
 constexpr uint32_t kIdesc = (1u << 4) |
                             (static_cast<uint32_t>(BN >> 3) << 17) |
                             (static_cast<uint32_t>(BM >> 4) << 24);
+constexpr uint32_t kPairIdesc = (1u << 4) |  // M of the whole pair
+                                (static_cast<uint32_t>(BN >> 3) << 17) |
+                                (static_cast<uint32_t>(kPairM >> 4) << 24);
 
 struct ModTable {
   uint32_t p[kMaxModuli], magic[kMaxModuli], bias[kMaxModuli];
@@ -275,6 +297,86 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
                :
                : "memory");
 }
+
+
+// ---- CTA-pair (cta_group::2) forms ----
+// Arrival on an mbarrier of any CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// The shared::cluster address of `local` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Tile into this CTA's shared memory; completion is signalled on `bar`, an
+// mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// TMEM of the CTA pair: one warp of each CTA executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+
+// One pair MMA (M=256 across the two CTAs), issued by the even CTA.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the mbarrier at offset `bar` of both CTAs of the pair when
+// every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// As above, on this CTA's mbarrier only.
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -549,6 +651,224 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+constexpr int kPairChunkKB = chunk_kb<true>();
+
+// The CTA-pair kernel: tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
+// even CTA of a cluster of two; long (1024-term) chunks only.
+__global__ void __launch_bounds__(kThreads, 1)
+    residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPairNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: leader of the pair (issues the MMAs), 1: peer
+  const bool leader = rank == 0;
+  const uint32_t full0 = smem_u32(bars);           // leader: both CTAs' tiles of a stage landed
+  const uint32_t empty0 = full0 + 8 * kPairStages;     // both: the MMAs released a stage
+  const uint32_t accf0 = empty0 + 8 * kPairStages;     // both: a chunk sum is in TMEM
+  const uint32_t acce0 = accf0 + 16;               // leader: both epilogues drained a buffer
+  const uint32_t drain = acce0 + 16;               // leader: all MMAs finished
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {  // one warp of each CTA allocates the pair's TMEM together
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const int units = prm.n * prm.splits * prm.tiles_m * prm.tiles_n;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+
+  if (warp < 4) regs_dec<kCtrlRegs>();
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    // Each CTA loads its 128 rows of A and its half of B into its own ring;
+    // both signal the leader's full barrier, which the leader arms with the
+    // bytes of the two CTAs.  One thread walks the schedule.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_parity[kPairStages];
+      for (int s = 0; s < kPairStages; ++s) issued_parity[s] = -1;
+      bool ok = true;
+      for (int u = pair; u < units && ok; u += npairs) {
+        const Unit w = decode_unit(u, prm);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = cluster_addr(full0 + 8 * stage, 0);
+          if (leader) mbar_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
+          tma_load_3d_pair(smem_u32(sA + stage * kABytes), &tmA, kb * BK,
+                      w.mt * kPairM + static_cast<int>(rank) * BM, w.p, full_leader);
+          tma_load_3d_pair(smem_u32(sB + stage * kPairBBytes), &tmB, kb * BK,
+                      w.nt * BN + static_cast<int>(rank) * kBHalf, w.p, full_leader);
+          issued_parity[stage] = static_cast<int>(phase);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {  // let copies still in flight land before the pair exits
+        for (int s = 0; s < kPairStages; ++s)
+          if (issued_parity[s] >= 0) mbar_wait_drain(full0 + 8 * s, static_cast<uint32_t>(issued_parity[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 && leader) {
+    // ------------------------------ MMA issuer (leader) ------------------------------
+    // One thread issues M=256 MMAs that read A and B from both CTAs' rings and
+    // accumulate into both TMEMs.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int u = pair; u < units && ok; u += npairs) {
+        const Unit w = decode_unit(u, prm);
+        for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
+          const int c1 = min(w.kb1, c0 + kPairChunkKB);
+          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
+          for (int kb = c0; kb < c1; ++kb) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t da = smem_desc_swizzled(smem_u32(sA + stage * kABytes));
+            const uint64_t db = smem_desc_swizzled(smem_u32(sB + stage * kPairBBytes));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16_pair(d, da + 2ull * kk, db + 2ull * kk, kPairIdesc, (kb > c0 || kk > 0) ? 1u : 0u);
+            mma_commit_both(empty0 + 8 * stage);  // frees the stage in both CTAs
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_both(accf0 + 8 * ab);  // chunk sum ready in both TMEMs
+          ab ^= 1;
+          if (ab == 0) aphase ^= 1u;
+        }
+      }
+      mma_commit_local(drain);  // every issued MMA has finished before TMEM is freed
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------ epilogue ------------------------------
+    regs_inc<kEpiRegs>();
+    const int ew = warp - 4;
+    const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
+    const int half = ew >> 2;   // which kCols of the BN tile columns
+    const int row_in_tile = quad * 32 + lane;
+    int ab = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int u = pair; u < units && ok; u += npairs) {
+      const Unit w = decode_unit(u, prm);
+      const int nchunks = (w.kb1 - w.kb0 + kPairChunkKB - 1) / kPairChunkKB;
+      int32_t acc[kCols];
+#pragma unroll
+      for (int e = 0; e < kCols; ++e) acc[e] = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(ab * BN + half * kCols);
+        uint32_t va[32], vb[32];
+        tmem_ld32(taddr, va);
+        tmem_wait_ld(va);
+        drain_chunk<true, 0>(acc, taddr, va, vb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(acce0 + 8 * ab, 0));
+        ab ^= 1;
+        if (ab == 0) aphase ^= 1u;
+      }
+      if (!ok) break;
+
+      const int64_t gi = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + row_in_tile;
+      const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
+      if (gi < prm.M) {
+        if (prm.out_kind == 0) {
+          const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
+          uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(w.p) * prm.out_plane +
+                         gi * prm.ldo + gj0;
+#pragma unroll
+          for (int v = 0; v < kCols / 16; ++v) {
+            if (gj0 + 16 * v < prm.ldo) {
+              uint32_t word[4];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                word[b] = mod_p(acc[16 * v + 4 * b], p, mg, bs) |
+                          (mod_p(acc[16 * v + 4 * b + 1], p, mg, bs) << 8) |
+                          (mod_p(acc[16 * v + 4 * b + 2], p, mg, bs) << 16) |
+                          (mod_p(acc[16 * v + 4 * b + 3], p, mg, bs) << 24);
+              }
+              *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+            }
+          }
+        } else {
+          int32_t* dst = static_cast<int32_t*>(prm.out) +
+                         (static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.out_plane + gi * prm.ldo + gj0;
+#pragma unroll
+          for (int v = 0; v < kCols / 4; ++v)
+            if (gj0 + 4 * v < prm.ldo)
+              *reinterpret_cast<int4*>(dst + 4 * v) =
+                  make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's MMAs are done with the peer's ring and TMEM
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -590,7 +910,13 @@ bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_
 }  // namespace
 
 int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
-  const int64_t tiles = static_cast<int64_t>(n) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  // K of at least kPairMinK runs on CTA pairs (kPairM x BN tiles, one per SM
+  // pair); every split keeps at least that much K, so the choice holds
+  const bool pairs = kpad >= kPairMinK;
+  const int64_t min_blocks = pairs ? kPairMinK / kKBlock : 16;
+  const int64_t tm = pairs ? kPairM : BM;
+  const int64_t tiles = static_cast<int64_t>(n) * ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
+  if (pairs) num_sms /= 2;
   const int64_t kblocks = kpad / kKBlock;  // split shares are whole 64-element blocks
   if (tiles >= num_sms || kblocks < 32) return 1;
   auto eff = [&](int64_t s) {
@@ -600,7 +926,7 @@ int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   };
   int best = 1;
   double best_eff = eff(1);
-  for (int64_t s = 2; s <= 64 && kblocks / s >= 16; ++s) {
+  for (int64_t s = 2; s <= 64 && kblocks / s >= min_blocks; ++s) {
     const double e = eff(s);
     if (e > best_eff + 0.02) {
       best = static_cast<int>(s);
@@ -615,16 +941,11 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
                                 int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
                                 int num_sms, cudaStream_t stream) {
   if (M == 0 || N == 0) return cudaSuccess;
-  CUtensorMap tmA, tmB;
-  if (!make_slice_map(&tmA, a_slices, M, kpad, a_plane, n, BM) ||
-      !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, BN))
-    return cudaErrorInvalidValue;
   GemmParams prm;
   prm.M = static_cast<int>(M);
   prm.N = static_cast<int>(N);
   prm.n = n;
   prm.kblocks = static_cast<int>(kpad / BK);  // kpad is a multiple of kKBlock
-  prm.tiles_m = static_cast<int>((M + BM - 1) / BM);
   prm.tiles_n = static_cast<int>((N + BN - 1) / BN);
   prm.splits = splits;
   prm.kb_per_split = static_cast<int>((kpad / kKBlock + splits - 1) / splits) * (kKBlock / BK);
@@ -632,20 +953,53 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
   prm.ldo = ldo;
   prm.out_plane = out_plane;
   prm.out = out;
+  // CTA pairs with long chunks once every split holds kPairMinK terms;
+  // single CTAs with short chunks otherwise
+  const bool pairs = static_cast<int64_t>(prm.kb_per_split) * BK >= kPairMinK;
+  prm.tiles_m = static_cast<int>(pairs ? (M + kPairM - 1) / kPairM : (M + BM - 1) / BM);
+  CUtensorMap tmA, tmB;
+  if (!make_slice_map(&tmA, a_slices, M, kpad, a_plane, n, BM) ||
+      !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, pairs ? kBHalf : BN))
+    return cudaErrorInvalidValue;
   const int64_t units = static_cast<int64_t>(n) * splits * prm.tiles_m * prm.tiles_n;
-  const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
-  // long chunks once a split holds a full 1024-term chunk
   const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK >= 1024;
-  auto kernel = long_chunks ? residue_gemm_kernel<true> : residue_gemm_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  auto kernel = pairs ? residue_gemm_pair_kernel
+                      : (long_chunks ? residue_gemm_kernel<true> : residue_gemm_kernel<false>);
+  const size_t smem = pairs ? kPairSmemBytes : kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the pool has the registers: refuse to launch
   // unless the compiled launch register count covers the split exactly.
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
   if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, prm);
+  if (!pairs) {
+    const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
+    kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, prm);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: one CTA pair per co-resident cluster slot, at most one per SM pair
+  int64_t npairs = num_sms / 2;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);
+  int resident = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg)) != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  if (resident < npairs) npairs = resident;
+  if (units < npairs) npairs = units;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);  // clusters of two CTAs
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

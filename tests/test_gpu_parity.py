@@ -143,6 +143,14 @@ def test_dgemm_bit_exact(M, N, K, n):
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
 
+@pytest.mark.parametrize("M,N,K", [(129, 257, 2100), (1, 700, 4096), (300, 1, 2049), (257, 520, 6000)])
+def test_dgemm_bit_exact_cta_pairs(M, N, K):
+    """K of 2048 or more runs the residue GEMM on CTA pairs (256-row tiles,
+    1024-term chunks): ragged rows, columns and K against the oracle."""
+    A, B = inputs(M, N, K, seed=M + N + K)
+    assert same_bits(dgemm(A, B, 14), oracle.dgemm(A, B, 14))
+
+
 def test_dgemm_square256_normal_n14():
     w = workloads.WORKLOADS["square256_normal"]
     A, B = workloads.workload_operands(w)
