@@ -228,16 +228,20 @@ int ozk_ref_residues(int64_t count, const double* xp, int n, int8_t* out) {
 /* ------------------------------------------------------------------------- */
 /* Steps 4-5: one integer GEMM per modulus, then mod reduction               */
 /* ------------------------------------------------------------------------- */
+/* The residue c = acc mod p comes from the exact int64 sum for every K (the
+ * sums of K >= 2^17 terms are split into int32-exact chunks on the GPU, and
+ * a sum of chunk residues mod p is the same residue).  Only the raw int32 sum,
+ * when a caller asks for it, must fit int32; otherwise it is reported as 0
+ * with OZK_REF_ES32. */
 static int reduce_checked(int64_t acc, int32_t p, int32_t* raw, uint8_t* cmod) {
-  if (acc >= ((int64_t)1 << 31) || acc < -((int64_t)1 << 31)) {
-    if (raw) *raw = 0;
-    *cmod = 0;
-    return OZK_REF_ES32;
-  }
-  if (raw) *raw = (int32_t)acc;
   int64_t c = acc % p;
   if (c < 0) c += p;
   *cmod = (uint8_t)c;
+  if (acc >= ((int64_t)1 << 31) || acc < -((int64_t)1 << 31)) {
+    if (raw) *raw = 0;
+    return raw ? OZK_REF_ES32 : OZK_REF_OK;
+  }
+  if (raw) *raw = (int32_t)acc;
   return OZK_REF_OK;
 }
 
@@ -394,12 +398,8 @@ int ozk_ref_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
         const int8_t* b = rbt + (int64_t)k * N * K + j * K;
         int64_t acc = 0;
         for (int64_t q = 0; q < K; ++q) acc += (int64_t)a[q] * (int64_t)b[q];
-        int32_t raw;
         uint8_t cm;
-        if (reduce_checked(acc, MODULI[k], &raw, &cm)) {
-#pragma omp atomic write
-          err = OZK_REF_ES32;
-        }
+        reduce_checked(acc, MODULI[k], NULL, &cm);
         c[k] = cm;
       }
       bigi xc, xd, prod;
@@ -460,7 +460,7 @@ int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     for (int p = 0; p < n; ++p) {
       int32_t r;
       uint8_t cm;
-      if (reduce_checked(acc[p], MODULI[p], &r, &cm)) {
+      if (reduce_checked(acc[p], MODULI[p], raw ? &r : NULL, &cm)) {
 #pragma omp atomic write
         err = OZK_REF_ES32;
       }

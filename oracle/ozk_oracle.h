@@ -34,7 +34,7 @@ enum {
   OZK_REF_OK = 0,
   OZK_REF_EINVAL = -1,      /* bad argument */
   OZK_REF_EUNSUPPORTED = -2, /* bit budget too small for K, or n outside 2..20 */
-  OZK_REF_ES32 = -3,        /* a per-modulus dot product left the int32 range */
+  OZK_REF_ES32 = -3,        /* a requested raw int32 per-modulus sum left the int32 range */
   OZK_REF_ECRT = -4         /* CRT-lifted integer differs from the direct product */
 };
 

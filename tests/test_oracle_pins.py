@@ -261,6 +261,29 @@ def test_gemm_mod_worst_case_magnitude_at_k_limit():
     assert int(cmod[0, 0, 0]) == (2**14 * K) % 256
 
 
+def test_dgemm_k_beyond_the_int32_range_is_the_exact_integer_product():
+    # K >= 2^17: per-modulus sums may leave int32; the residues come from the
+    # exact sums (the GPU splits K into int32-exact chunks), and for small
+    # integer matrices the emulated product is the exact integer product
+    rng = np.random.default_rng(17)
+    K = 2**17 + 3
+    A = rng.integers(-7, 8, (3, K)).astype(np.float64)
+    B = rng.integers(-7, 8, (K, 2)).astype(np.float64)
+    A[0] = -7.0
+    B[:, 0] = -7.0  # C[0, 0] = 49 K, and every residue sum of that entry is large
+    ref = A.astype(np.int64) @ B.astype(np.int64)
+    C = oracle.dgemm(A, B, 14)
+    assert np.array_equal(C, ref.astype(np.float64))
+
+
+def test_gemm_mod_raw_sums_beyond_int32_are_refused():
+    K = 2**17 + 1
+    ra = np.full((1, 1, K), -128, dtype=np.int8)
+    rb = np.full((1, K, 1), -128, dtype=np.int8)
+    with pytest.raises(oracle.OracleError):
+        oracle.gemm_mod(ra, rb, 1)
+
+
 # --------------------------------------------------------------------------
 # Stage 6: CRT and symmetric lift
 # --------------------------------------------------------------------------
