@@ -286,15 +286,17 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
       if (k < n) {
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
+          // each partial is an exact int32 sum; their residues are added up
+          // (at most 64 * 255) so that K beyond one int32-exact sum stays exact
           int32_t sum[4] = {0, 0, 0, 0};
           for (int sp = 0; sp < splits; ++sp) {
             const int4 v = __ldcs(reinterpret_cast<const int4*>(static_cast<const int32_t*>(in) +
                                                                 (static_cast<int64_t>(sp) * n + k) * plane +
                                                                 i * ldi + jt + 4 * gg));
-            sum[0] += v.x;
-            sum[1] += v.y;
-            sum[2] += v.z;
-            sum[3] += v.w;
+            sum[0] += static_cast<int32_t>(mod_p(v.x, K.p[k], K.magic[k], K.bias[k]));
+            sum[1] += static_cast<int32_t>(mod_p(v.y, K.p[k], K.magic[k], K.bias[k]));
+            sum[2] += static_cast<int32_t>(mod_p(v.z, K.p[k], K.magic[k], K.bias[k]));
+            sum[3] += static_cast<int32_t>(mod_p(v.w, K.p[k], K.magic[k], K.bias[k]));
           }
           cw[k][gg] = mod_p(sum[0], K.p[k], K.magic[k], K.bias[k]) |
                       (mod_p(sum[1], K.p[k], K.magic[k], K.bias[k]) << 8) |

@@ -525,9 +525,12 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
     return OZK_ERR_INVALID_ARG;
   if (out_kind == 0) {
     if (splits != 1 || ldo < N || ldo % 16) return OZK_ERR_INVALID_ARG;
+    if (K >= (int64_t{1} << 17)) return OZK_ERR_INVALID_ARG;  // one int32-exact sum over all of K
   } else if (out_kind == 1) {
     if (splits < 1 || splits > 64 || splits > kpad / kKBlock || ldo < N || ldo % 4)
       return OZK_ERR_INVALID_ARG;
+    // each split's K (whole 64-blocks) must keep its int32 sums exact
+    if ((kpad / kKBlock + splits - 1) / splits * kKBlock > OZK_SPLIT_MAX_K) return OZK_ERR_INVALID_ARG;
   } else {
     return OZK_ERR_INVALID_ARG;
   }

@@ -918,15 +918,17 @@ int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   const int64_t tiles = static_cast<int64_t>(n) * ((M + tm - 1) / tm) * ((N + BN - 1) / BN);
   if (pairs) num_sms /= 2;
   const int64_t kblocks = kpad / kKBlock;  // split shares are whole 64-element blocks
-  if (tiles >= num_sms || kblocks < 32) return 1;
+  // K beyond one int32-exact sum (2^14 K < 2^31) needs at least this many splits
+  const int64_t min_s = (kblocks + OZK_SPLIT_MAX_K / kKBlock - 1) / (OZK_SPLIT_MAX_K / kKBlock);
+  if (min_s == 1 && (tiles >= num_sms || kblocks < 32)) return 1;
   auto eff = [&](int64_t s) {
     const int64_t units = tiles * s;
     const int64_t waves = (units + num_sms - 1) / num_sms;
     return static_cast<double>(units) / static_cast<double>(waves * num_sms);
   };
-  int best = 1;
-  double best_eff = eff(1);
-  for (int64_t s = 2; s <= 64 && kblocks / s >= min_blocks; ++s) {
+  int best = static_cast<int>(min_s);
+  double best_eff = eff(min_s);
+  for (int64_t s = min_s + 1; s <= 64 && kblocks / s >= min_blocks; ++s) {
     const double e = eff(s);
     if (e > best_eff + 0.02) {
       best = static_cast<int>(s);

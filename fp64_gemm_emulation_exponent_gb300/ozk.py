@@ -21,7 +21,8 @@ OZK_ERR_CUDA = 4
 OZK_ERR_TIMEOUT = 5
 OZK_ERR_DEVICE = 6
 OZK_MAX_MODULI = 20
-OZK_MAX_K = 131071
+OZK_MAX_K = 4194304
+OZK_SPLIT_MAX_K = 131008
 OZK_SCALE_NONFINITE = -(2**31)
 OZK_LIMBS = 8
 OZK_SCALE_NOALLOC_MAX = 262144

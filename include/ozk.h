@@ -42,7 +42,7 @@ typedef struct CUevent_st* ozk_event_t;   /* identical to cudaEvent_t */
 typedef enum {
   OZK_OK = 0,
   OZK_ERR_INVALID_ARG = 1, /* bad pointer, size, leading dimension or overlap */
-  OZK_ERR_UNSUPPORTED = 2, /* K >= 2^17, n_moduli outside 2..20, or too few moduli for K */
+  OZK_ERR_UNSUPPORTED = 2, /* K > OZK_MAX_K, n_moduli outside 2..20, or too few moduli for K */
   OZK_ERR_WORKSPACE = 3,   /* caller workspace too small, or allocation failed */
   OZK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   OZK_ERR_TIMEOUT = 5,     /* a kernel's bounded pipeline wait ran out (device-side) */
@@ -50,7 +50,8 @@ typedef enum {
 } ozk_status;
 
 #define OZK_MAX_MODULI 20
-#define OZK_MAX_K 131071           /* exact int32 sums need 2^14 * K < 2^31 */
+#define OZK_MAX_K 4194304          /* K = 2^22; the workspace holds 2 n (M + N) K bytes of slices */
+#define OZK_SPLIT_MAX_K 131008     /* K of one int32-exact partial sum: 2^14 * K < 2^31, whole 64-blocks */
 #define OZK_SCALE_NONFINITE INT32_MIN
 #define OZK_LIMBS 8                /* lifted integers: 8 x uint32, two's complement */
 
@@ -180,15 +181,18 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb,
                    ozk_stream_t stream);
 
 /* One integer GEMM per modulus ("INT8 GEMM", run on fp16 tensor cores: every
- * product and every partial sum of 256 terms is an exact fp32 integer) with
- * the mod reduction fused into its epilogue.
+ * product and every partial sum of up to 1024 terms is an exact fp32 integer)
+ * with the mod reduction fused into its epilogue.
  *  out_kind 0: out is uint8 [n][M][ldo], c = (sum_k ra rb) mod p in [0, p);
- *              ldo >= N, a multiple of 16; splits must be 1.
+ *              ldo >= N, a multiple of 16; splits must be 1 and K < 2^17
+ *              (one int32-exact sum).
  *  out_kind 1: out is int32 [splits][n][M][ldo], the exact partial sums over
- *              the split'th share of K (their sum is the exact dot product);
- *              ldo >= N, a multiple of 4.
+ *              the split'th share of K, ceil(kpad/64/splits) blocks of 64
+ *              (their sum is the exact dot product); ldo >= N, a multiple of 4;
+ *              each share must hold at most OZK_SPLIT_MAX_K terms, so K beyond
+ *              that needs at least ceil(kpad / OZK_SPLIT_MAX_K) splits.
  * K is the inner dimension the slices were quantised with (kpad = ozk_kpad(K)).
- * splits in 1..64 and at most kpad/64. */
+ * splits in 1..64 and at most kpad/64; violations return OZK_ERR_INVALID_ARG. */
 int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
                      const uint16_t* b_slices, int n_moduli, int out_kind,
                      void* out, int64_t ldo, int splits, ozk_stream_t stream);
@@ -196,7 +200,8 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
 /* CRT reconstruction with symmetric lift, undo scaling, FP64 write:
  * C_ij = RN-even(X_ij 2^-(s_i + t_j)) with X_ij the unique integer in
  * [-P/2, P/2) congruent to the residues; NaN where s_i or t_j is
- * OZK_SCALE_NONFINITE.  in / in_kind / ldi / splits as ozk_residue_gemm's out. */
+ * OZK_SCALE_NONFINITE.  in / in_kind / ldi / splits as ozk_residue_gemm's out;
+ * int32 partial sums are reduced mod p one by one before they are added. */
 int ozk_crt_combine(int64_t M, int64_t N, int n_moduli, const void* in,
                     int in_kind, int64_t ldi, int splits, const int32_t* s,
                     const int32_t* t, double* C, int64_t ldc, ozk_stream_t stream);

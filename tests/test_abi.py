@@ -51,7 +51,7 @@ def test_moduli_match_the_oracle():
 
 def test_beta_matches_the_oracle():
     for n in range(2, 21):
-        for K in [1, 2, 3, 63, 64, 65, 255, 256, 512, 1000, 1024, 4096, 8192, 65536, 131071]:
+        for K in [1, 2, 3, 63, 64, 65, 255, 256, 512, 1000, 1024, 4096, 8192, 65536, 131071, 131072, 10**6, 4194304]:
             try:
                 want = oracle.beta(K, n)
             except oracle.OracleError:
@@ -67,7 +67,12 @@ def test_workspace_size():
     assert ozk.ozk_workspace_size(0, 10, 10, 14) == 0
     assert ozk.ozk_workspace_size(10, 10, 0, 14) == 0
     assert ozk.ozk_workspace_size(10, 10, 10, 1) == 0
-    assert ozk.ozk_workspace_size(10, 10, 131072, 14) == 0
+    assert ozk.ozk_workspace_size(10, 10, ozk.OZK_MAX_K + 1, 14) == 0
+    # K beyond one int32-exact sum: int32 partial planes of at least ceil(kpad / OZK_SPLIT_MAX_K) splits
+    for K in (131072, 10**6, ozk.OZK_MAX_K):
+        kpad = ozk.ozk_kpad(K)
+        min_splits = -(-kpad // ozk.OZK_SPLIT_MAX_K)
+        assert ozk.ozk_workspace_size(10, 10, K, 14) >= 2 * 14 * 20 * kpad + 4 * min_splits * 14 * 10 * 12
     for (M, N, K, n) in [(1, 1, 1, 2), (256, 256, 256, 14), (4096, 4096, 4096, 14), (8192, 8192, 512, 20),
                          (512, 512, 65536, 20)]:
         ws = ozk.ozk_workspace_size(M, N, K, n)

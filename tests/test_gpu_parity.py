@@ -151,6 +151,14 @@ def test_dgemm_bit_exact_cta_pairs(M, N, K):
     assert same_bits(dgemm(A, B, 14), oracle.dgemm(A, B, 14))
 
 
+@pytest.mark.parametrize("M,N,K,n", [(5, 9, 2**17 + 3, 14), (3, 5, 2**20 + 7, 14), (17, 3, 300000, 20)])
+def test_dgemm_k_beyond_one_int32_sum(M, N, K, n):
+    """K >= 2^17: the residue GEMM splits K into int32-exact shares (at most
+    OZK_SPLIT_MAX_K terms) and the combine reduces each share mod p."""
+    A, B = inputs(M, N, K, seed=K % 1000)
+    assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
+
+
 def test_dgemm_square256_normal_n14():
     w = workloads.WORKLOADS["square256_normal"]
     A, B = workloads.workload_operands(w)
@@ -260,7 +268,8 @@ def test_rejected_arguments():
     a, b, c = A.data_ptr(), B.data_ptr(), C.data_ptr()
     assert call(4, 5, 8, a, 8, b, 5, c, 5, 1) == ozk.OZK_ERR_UNSUPPORTED
     assert call(4, 5, 8, a, 8, b, 5, c, 5, 21) == ozk.OZK_ERR_UNSUPPORTED
-    assert call(4, 5, 131072, a, 131072, b, 5, c, 5, 14) == ozk.OZK_ERR_UNSUPPORTED
+    big = ozk.OZK_MAX_K + 1
+    assert call(4, 5, big, a, big, b, 5, c, 5, 14) == ozk.OZK_ERR_UNSUPPORTED
     assert call(4, 5, 8, a, 7, b, 5, c, 5, 14) == ozk.OZK_ERR_INVALID_ARG      # lda < K
     assert call(4, 5, 8, a, 8, b, 5, c, 4, 14) == ozk.OZK_ERR_INVALID_ARG      # ldc < N
     assert call(4, 5, 8, a, 8, b, 5, a, 5, 14) == ozk.OZK_ERR_INVALID_ARG      # C overlaps A
@@ -270,6 +279,14 @@ def test_rejected_arguments():
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     rc = L.ozk_dgemm_ws(4, 5, 8, p(a), 8, p(b), 5, p(c), 5, 14, p(ws.data_ptr()), 16, s)
     assert rc == ozk.OZK_ERR_WORKSPACE
+    # residue GEMM stage: one int32-exact sum needs K < 2^17; splits of at most OZK_SPLIT_MAX_K
+    sl = torch.zeros(2 * 4 * 262144, dtype=torch.int16, device="cuda")
+    out = torch.zeros(2 * 4 * 16 * 4, dtype=torch.int32, device="cuda")
+    gemm = lambda K, kind, ldo, splits: L.ozk_residue_gemm(4, 4, K, p(sl.data_ptr()), p(sl.data_ptr()), 2, kind,
+                                                          p(out.data_ptr()), ldo, splits, s)
+    assert gemm(2**17, 0, 16, 1) == ozk.OZK_ERR_INVALID_ARG
+    assert gemm(2**17, 1, 4, 1) == ozk.OZK_ERR_INVALID_ARG
+    assert gemm(262144, 1, 4, 2) == ozk.OZK_ERR_INVALID_ARG   # 131072 terms per split
     assert ozk.ozk_stream_status() == 0
 
 
