@@ -1,45 +1,49 @@
 // Launchers of the CRT combine (the arithmetic is in crt_device.cuh): the
-// kernels with a runtime moduli count for split-K int32 partial sums, the
-// exact-integer (limb) output and narrow outputs, and the dispatch to the
-// compile-time-count kernels of crt_fixed.cu for the common case.
+// kernels with a runtime moduli count for byte residues, split-K int32
+// partial sums, the exact-integer (limb) output and narrow outputs, and the
+// dispatch to the compile-time-count kernels of crt_fixed.cu for the common
+// case (pair residues, FP64 output, wide).
 #include "crt_device.cuh"
 
 namespace ozk {
 namespace {
 
-template <int NL, int G>
+// Runtime moduli count, 4 columns per thread.
+template <int NL>
 cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
                         int splits, const int32_t* s, const int32_t* t, double* C, int64_t ldc, uint32_t* X,
                         const CrtConst& K, cudaStream_t stream) {
+  constexpr int G = 1;
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  if (in_kind == 0) {
-    if (X)
-      crt_kernel<NL, 0, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K);
-    else
-      crt_kernel<NL, 0, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K);
-  } else {
-    if (X)
-      crt_kernel<NL, 1, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K);
-    else
-      crt_kernel<NL, 1, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K);
-  }
+#define OZK_CRT_LAUNCH(KIND)                                                                                      \
+  do {                                                                                                            \
+    if (X)                                                                                                        \
+      crt_kernel<NL, KIND, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K); \
+    else                                                                                                          \
+      crt_kernel<NL, KIND, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K); \
+  } while (0)
+  if (in_kind == 0)
+    OZK_CRT_LAUNCH(0);
+  else if (in_kind == 1)
+    OZK_CRT_LAUNCH(1);
+  else
+    OZK_CRT_LAUNCH(2);
+#undef OZK_CRT_LAUNCH
   return cudaGetLastError();
 }
 
-// 8 columns per thread (8-byte residue loads) when that still gives every SM
-// several blocks; 4 otherwise.
+// The FP64 output from byte or pair residues (what the GEMM path writes) on
+// outputs wide enough to give every SM several blocks of 8-column threads runs
+// the kernel compiled for its moduli count; everything else the runtime-count one.
 template <int NL>
 cudaError_t launch_nl(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane, int splits,
                       const int32_t* s, const int32_t* t, double* C, int64_t ldc, uint32_t* X,
                       const CrtConst& K, cudaStream_t stream) {
   constexpr int64_t kWideThreads = 152 * 256 * 4;
-  if (M * ((N + 7) / 8) >= kWideThreads) {
-    // the FP64 output from byte residues, the common case, has one kernel per moduli count
-    if (in_kind == 0 && X == nullptr) return launch_crt_fixed(M, N, in, ldi, plane, s, t, C, ldc, K, stream);
-    return launch_nl_g<NL, 2>(M, N, in, in_kind, ldi, plane, splits, s, t, C, ldc, X, K, stream);
-  }
-  return launch_nl_g<NL, 1>(M, N, in, in_kind, ldi, plane, splits, s, t, C, ldc, X, K, stream);
+  if (M * ((N + 7) / 8) >= kWideThreads && in_kind != 1 && X == nullptr)
+    return launch_crt_fixed(M, N, in, in_kind, ldi, plane, s, t, C, ldc, K, stream);
+  return launch_nl_g<NL>(M, N, in, in_kind, ldi, plane, splits, s, t, C, ldc, X, K, stream);
 }
 
 }  // namespace

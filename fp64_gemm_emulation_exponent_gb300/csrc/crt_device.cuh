@@ -273,8 +273,22 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
   }
   const int n = NFIX ? NFIX : K.n;  // a compile-time moduli count lets every loop unroll exactly
 
+  // IN_KIND 0/1: cw[k][gg] holds the 4 byte residues of modulus k for
+  // columns 4 gg .. 4 gg + 3.  IN_KIND 2: plane j's 2G words (two uint16
+  // residues each) sit in cw[2j][0..G-1], cw[2j+1][0..G-1].
   uint32_t cw[kMaxModuli][G];
-  if constexpr (IN_KIND == 0) {
+  if constexpr (IN_KIND == 2) {
+    const uint16_t* base = static_cast<const uint16_t*>(in) + i * ldi + jt;
+    static_for<0, kMaxModuli / 2>([&](auto jc) {
+      constexpr int j = decltype(jc)::value;
+      if (2 * j < n) {
+        uint32_t w[2 * G];
+        load_words<2 * G>(reinterpret_cast<const uint8_t*>(base + j * plane), w);
+#pragma unroll
+        for (int x = 0; x < 2 * G; ++x) cw[2 * j + x / G][x % G] = w[x];
+      }
+    });
+  } else if constexpr (IN_KIND == 0) {
     const uint8_t* base = static_cast<const uint8_t*>(in) + i * ldi + jt;
     static_for<0, kMaxModuli>([&](auto kc) {
       constexpr int k = decltype(kc)::value;
@@ -350,18 +364,36 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
     static_for<0, kMaxModuli / 2>([&](auto jc) {
       constexpr int j = decltype(jc)::value;
       if (2 * j + 1 < n) {
-        uint32_t wa = cw[2 * j][0], wb = cw[2 * j + 1][0];
+        // IN_KIND 2: words 2 gg, 2 gg + 1 of plane j; else the byte words of moduli 2j, 2j+1
+        uint32_t wa, wb;
+        if constexpr (IN_KIND == 2) {
+          wa = cw[2 * j + (2 * 0) / G][0];
+          wb = cw[2 * j + 1 / G][1 % G];
 #pragma unroll
-        for (int x = 1; x < G; ++x) {
-          wa = gg == x ? cw[2 * j][x] : wa;
-          wb = gg == x ? cw[2 * j + 1][x] : wb;
+          for (int x = 1; x < G; ++x) {
+            wa = gg == x ? cw[2 * j + (2 * x) / G][(2 * x) % G] : wa;
+            wb = gg == x ? cw[2 * j + (2 * x + 1) / G][(2 * x + 1) % G] : wb;
+          }
+        } else {
+          wa = cw[2 * j][0];
+          wb = cw[2 * j + 1][0];
+#pragma unroll
+          for (int x = 1; x < G; ++x) {
+            wa = gg == x ? cw[2 * j][x] : wa;
+            wb = gg == x ? cw[2 * j + 1][x] : wb;
+          }
         }
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
-          const uint32_t ca = __byte_perm(wa, 0u, 0x4440 + o);
-          const uint32_t cb = __byte_perm(wb, 0u, 0x4440 + o);
-          const uint32_t t = ca * K.pu[j][0] + cb * K.pu[j][1];  // < 2^25
-          const uint32_t r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
+          uint32_t r;
+          if constexpr (IN_KIND == 2) {
+            r = ((o < 2 ? wa : wb) >> (16 * (o & 1))) & 0xFFFFu;
+          } else {
+            const uint32_t ca = __byte_perm(wa, 0u, 0x4440 + o);
+            const uint32_t cb = __byte_perm(wb, 0u, 0x4440 + o);
+            const uint32_t t = ca * K.pu[j][0] + cb * K.pu[j][1];  // < 2^25
+            r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
+          }
           qacc[o] += static_cast<uint64_t>(r) * K.pfrac[j];
 #pragma unroll
           for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(r) * K.pe[j][l];
@@ -373,12 +405,23 @@ __global__ void __launch_bounds__(256) crt_kernel(const void* __restrict__ in, i
       static_for<0, kMaxModuli>([&](auto kc) {
         constexpr int k = decltype(kc)::value;
         if (k == n - 1) {
-          uint32_t word = cw[k][0];
+          uint32_t word = cw[k][0], word2 = 0;
+          if constexpr (IN_KIND == 2) {  // plane (n-1)/2 holds the last residue as uint16
+            word = cw[k][0];
+            word2 = cw[k + 1 / G][1 % G];
 #pragma unroll
-          for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
+            for (int x = 1; x < G; ++x) {
+              word = gg == x ? cw[k + (2 * x) / G][(2 * x) % G] : word;
+              word2 = gg == x ? cw[k + (2 * x + 1) / G][(2 * x + 1) % G] : word2;
+            }
+          } else {
+#pragma unroll
+            for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
+          }
 #pragma unroll
           for (int o = 0; o < 4; ++o) {
-            const uint32_t c = __byte_perm(word, 0u, 0x4440 + o);
+            const uint32_t c = IN_KIND == 2 ? (((o < 2 ? word : word2) >> (16 * (o & 1))) & 0xFFFFu)
+                                            : __byte_perm(word, 0u, 0x4440 + o);
             qacc[o] += static_cast<uint64_t>(c) * K.frac[k];
 #pragma unroll
             for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(c) * K.e[k][l];

@@ -1,5 +1,6 @@
 // The CRT combine kernel with the moduli count fixed at compile time, one
-// instantiation per count, for the FP64 output from byte residues: with the
+// instantiation per count and input (byte residues or the 16-bit residues of
+// moduli pairs), for the FP64 output: with the
 // count known, the pair loop, the accumulator set-up and the limb count are
 // resolved by the compiler (about 40 fewer instructions per output than the
 // runtime-count kernel in crt_combine.cu, which serves the other cases).
@@ -9,33 +10,40 @@ namespace ozk {
 namespace {
 
 template <int NM>
-cudaError_t launch_fixed(int64_t M, int64_t N, const void* in, int64_t ldi, int64_t plane, const int32_t* s,
-                         const int32_t* t, double* C, int64_t ldc, const CrtConst& K, cudaStream_t stream) {
+cudaError_t launch_fixed(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
+                         const int32_t* s, const int32_t* t, double* C, int64_t ldc, const CrtConst& K,
+                         cudaStream_t stream) {
   constexpr int G = 2;
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  crt_kernel<crt_limbs(NM), 0, false, G, NM>
-      <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);
+  if (in_kind == 2)
+    crt_kernel<crt_limbs(NM), 2, false, G, NM>
+        <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);
+  else
+    crt_kernel<crt_limbs(NM), 0, false, G, NM>
+        <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);
   return cudaGetLastError();
 }
 
 template <int NM>
-cudaError_t dispatch(int n, int64_t M, int64_t N, const void* in, int64_t ldi, int64_t plane, const int32_t* s,
-                     const int32_t* t, double* C, int64_t ldc, const CrtConst& K, cudaStream_t stream) {
+cudaError_t dispatch(int n, int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
+                     const int32_t* s, const int32_t* t, double* C, int64_t ldc, const CrtConst& K,
+                     cudaStream_t stream) {
   if constexpr (NM > kMaxModuli) {
     return cudaErrorInvalidValue;
   } else {
-    if (n == NM) return launch_fixed<NM>(M, N, in, ldi, plane, s, t, C, ldc, K, stream);
-    return dispatch<NM + 1>(n, M, N, in, ldi, plane, s, t, C, ldc, K, stream);
+    if (n == NM) return launch_fixed<NM>(M, N, in, in_kind, ldi, plane, s, t, C, ldc, K, stream);
+    return dispatch<NM + 1>(n, M, N, in, in_kind, ldi, plane, s, t, C, ldc, K, stream);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_crt_fixed(int64_t M, int64_t N, const void* in, int64_t ldi, int64_t plane, const int32_t* s,
-                             const int32_t* t, double* C, int64_t ldc, const CrtConst& K, cudaStream_t stream) {
-  if (K.n < 2 || K.n > kMaxModuli) return cudaErrorInvalidValue;
-  return dispatch<2>(K.n, M, N, in, ldi, plane, s, t, C, ldc, K, stream);
+cudaError_t launch_crt_fixed(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
+                             const int32_t* s, const int32_t* t, double* C, int64_t ldc, const CrtConst& K,
+                             cudaStream_t stream) {
+  if (K.n < 2 || K.n > kMaxModuli || (in_kind != 0 && in_kind != 2)) return cudaErrorInvalidValue;
+  return dispatch<2>(K.n, M, N, in, in_kind, ldi, plane, s, t, C, ldc, K, stream);
 }
 
 }  // namespace ozk

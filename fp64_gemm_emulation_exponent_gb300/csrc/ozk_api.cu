@@ -15,6 +15,7 @@ namespace ozk {
 namespace {
 
 constexpr int kSplitSms = 152;  // SM count the split-K choice plans for (GB300)
+constexpr int64_t kPairOutMinK = 8192;  // K from which the GEMM writes pair residues
 constexpr int64_t kMaxDim = INT32_MAX / 2;  // rows/columns the kernels index with int
 
 // ---- small unsigned multi-limb integers for the host-side constants -------
@@ -189,7 +190,7 @@ struct Layout {
   size_t amax, s, t, a, b, out, total;
   int64_t kpad, ldo;
   int64_t a_plane, b_plane, out_plane;  // elements between consecutive moduli's planes
-  int splits;
+  int splits, planes, kind;
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -205,7 +206,12 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   Layout L;
   L.kpad = ozk_kpad(K);
   L.splits = choose_splits(M, N, L.kpad, n, kSplitSms);
-  L.ldo = L.splits == 1 ? round_up(N, 16) : round_up(N, 4);
+  // one split: byte residues (kind 0), or for long K the uint16 residues of
+  // moduli pairs (kind 2: the GEMM's epilogue does the first CRT step, which
+  // pays only once K amortises the heavier tile tail); split-K: int32 sums
+  L.kind = L.splits > 1 ? 1 : (K >= kPairOutMinK ? 2 : 0);
+  L.ldo = L.kind == 1 ? round_up(N, 4) : round_up(N, 16);
+  L.planes = L.kind == 1 ? n * L.splits : (L.kind == 2 ? (n + 1) / 2 : n);
   size_t off = 0;
   L.amax = off;
   off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(M + N), 256);
@@ -215,7 +221,7 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(N), 1024);
   const size_t a_plane = skewed_plane(2u * static_cast<size_t>(M) * L.kpad);
   const size_t b_plane = skewed_plane(2u * static_cast<size_t>(N) * L.kpad);
-  const size_t esize = L.splits == 1 ? 1 : 4;  // uint8 residues or int32 partial sums
+  const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
   const size_t o_plane = skewed_plane(esize * static_cast<size_t>(M) * L.ldo);
   L.a_plane = static_cast<int64_t>(a_plane / 2);
   L.b_plane = static_cast<int64_t>(b_plane / 2);
@@ -225,7 +231,7 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   L.b = off;
   off = align_up(off + b_plane * static_cast<size_t>(n), 1024);
   L.out = off;
-  off = align_up(off + o_plane * static_cast<size_t>(n) * static_cast<size_t>(L.splits), 256);
+  off = align_up(off + o_plane * static_cast<size_t>(L.planes), 256);
   L.total = off;
   return L;
 }
@@ -270,11 +276,10 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, L.a_plane, bs,
                            L.b_plane, stream));
   if ((rc = record(ev, 2, stream))) return rc;
-  OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n, L.splits == 1 ? 0 : 1,
-                               out, L.ldo, L.out_plane, L.splits, sms, stream));
+  OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n, L.kind, out, L.ldo, L.out_plane,
+                               L.splits, sms, stream));
   if ((rc = record(ev, 3, stream))) return rc;
-  OZK_CUDA(launch_crt(M, N, n, out, L.splits == 1 ? 0 : 1, L.ldo, L.out_plane, L.splits, s, t, C, ldc,
-                      nullptr, stream));
+  OZK_CUDA(launch_crt(M, N, n, out, L.kind, L.ldo, L.out_plane, L.splits, s, t, C, ldc, nullptr, stream));
   if ((rc = record(ev, 4, stream))) return rc;
   return OZK_OK;
 }
@@ -531,6 +536,9 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
       return OZK_ERR_INVALID_ARG;
     // each split's K (whole 64-blocks) must keep its int32 sums exact
     if ((kpad / kKBlock + splits - 1) / splits * kKBlock > OZK_SPLIT_MAX_K) return OZK_ERR_INVALID_ARG;
+  } else if (out_kind == 2) {
+    if (splits != 1 || ldo < N || ldo % 8) return OZK_ERR_INVALID_ARG;
+    if (K >= (int64_t{1} << 17)) return OZK_ERR_INVALID_ARG;
   } else {
     return OZK_ERR_INVALID_ARG;
   }
@@ -552,6 +560,8 @@ static int check_crt_args(int64_t M, int64_t N, int n_moduli, const void* in, in
     if (splits != 1 || ldi < N || ldi % 16) return OZK_ERR_INVALID_ARG;
   } else if (in_kind == 1) {
     if (splits < 1 || splits > 64 || ldi < N || ldi % 4) return OZK_ERR_INVALID_ARG;
+  } else if (in_kind == 2) {
+    if (splits != 1 || ldi < N || ldi % 8) return OZK_ERR_INVALID_ARG;
   } else {
     return OZK_ERR_INVALID_ARG;
   }

@@ -102,10 +102,11 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
                                 int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
                                 int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
                                 int num_sms, cudaStream_t stream);
-// The same for in_kind 0 and an FP64 output, through a kernel compiled for
-// this moduli count (crt_fixed.cu).
-cudaError_t launch_crt_fixed(int64_t M, int64_t N, const void* in, int64_t ldi, int64_t plane, const int32_t* s,
-                             const int32_t* t, double* C, int64_t ldc, const CrtConst& K, cudaStream_t stream);
+// The same for in_kind 0 or 2 and an FP64 output, through a kernel compiled
+// for this moduli count (crt_fixed.cu).
+cudaError_t launch_crt_fixed(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
+                             const int32_t* s, const int32_t* t, double* C, int64_t ldc, const CrtConst& K,
+                             cudaStream_t stream);
 cudaError_t launch_crt(int64_t M, int64_t N, int n, const void* in, int in_kind, int64_t ldi,
                        int64_t plane, int splits, const int32_t* s, const int32_t* t, double* C,
                        int64_t ldc, uint32_t* X, cudaStream_t stream);

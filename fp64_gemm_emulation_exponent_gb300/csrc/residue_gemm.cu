@@ -91,6 +91,12 @@ constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;
 constexpr int kPairNumBars = 2 * kPairStages + 5;
 static_assert(8 * kPairNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarBytes;
+// out_kind 2: each epilogue thread parks the residues of the first modulus of
+// a pair (kCols bytes) in shared memory until the second modulus is done
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr size_t kStashBytes = static_cast<size_t>(kEpiThreads) * kCols;
+static_assert(kSmemBytes + kStashBytes <= 232448 && kPairSmemBytes + kStashBytes <= 232448,
+              "ring, barriers and stash exceed the shared memory of a CTA");
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 50000000ull;
 
@@ -109,9 +115,20 @@ constexpr uint32_t kPairIdesc = (1u << 4) |  // M of the whole pair
                                 (static_cast<uint32_t>(BN >> 3) << 17) |
                                 (static_cast<uint32_t>(kPairM >> 4) << 24);
 
+// Per modulus: p, and the constants of mod_p.  Per pair of moduli (2j, 2j+1)
+// with m = p_2j p_2j+1: u0 = 1 mod p_2j and 0 mod p_2j+1, u1 the other way
+// round, so (c_2j u0 + c_2j+1 u1) mod m is the residue of the pair modulus;
+// t < 2^25 is divided exactly as umulhi(t, ceil(2^42 / m)) >> 10.
 struct ModTable {
   uint32_t p[kMaxModuli], magic[kMaxModuli], bias[kMaxModuli];
+  uint32_t pu0[kMaxModuli / 2], pu1[kMaxModuli / 2], pm[kMaxModuli / 2], pmagic[kMaxModuli / 2];
 };
+
+__host__ __device__ constexpr uint32_t inverse_mod(uint32_t a, uint32_t p) {
+  for (uint32_t x = 1; x < p; ++x)
+    if ((a % p) * x % p == 1u) return x;
+  return 0;
+}
 
 __host__ __device__ constexpr ModTable make_mod_table() {
   ModTable t{};
@@ -120,6 +137,13 @@ __host__ __device__ constexpr ModTable make_mod_table() {
     t.magic[k] = magic_of(t.p[k]);
     t.bias[k] = bias_of(t.p[k]);
   }
+  for (int j = 0; j < kMaxModuli / 2; ++j) {
+    const uint32_t pa = modulus_at(2 * j), pb = modulus_at(2 * j + 1);
+    t.pu0[j] = pb * inverse_mod(pb, pa);
+    t.pu1[j] = pa * inverse_mod(pa, pb);
+    t.pm[j] = pa * pb;
+    t.pmagic[j] = static_cast<uint32_t>(((uint64_t{1} << 42) + pa * pb - 1) / (pa * pb));
+  }
   return t;
 }
 
@@ -127,6 +151,7 @@ __constant__ ModTable c_mod = make_mod_table();
 
 struct GemmParams {
   int M, N, n, kblocks, tiles_m, tiles_n, splits, kb_per_split, out_kind;
+  int mod_units;           // n, or ceil(n/2) pairs of moduli for out_kind 2
   int64_t ldo, out_plane;  // row stride and per-(split, modulus) plane stride, in elements
   void* out;
 };
@@ -381,8 +406,10 @@ __device__ __forceinline__ void mma_commit_local(uint32_t bar) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// One work unit: a tile (mt, nt) of split sk for one modulus p, or for
+// out_kind 2 the two moduli p, p+1 of pair q one after the other (passes).
 struct Unit {
-  int p, sk, mt, nt, kb0, kb1;
+  int p, q, passes, sk, mt, nt, kb0, kb1;
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
@@ -392,7 +419,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   r.mt = u % prm.tiles_m;
   u /= prm.tiles_m;
   r.sk = u % prm.splits;
-  r.p = u / prm.splits;
+  r.q = u / prm.splits;
+  if (prm.out_kind == 2) {
+    r.p = 2 * r.q;
+    r.passes = min(2, prm.n - r.p);
+  } else {
+    r.p = r.q;
+    r.passes = 1;
+  }
   r.kb0 = r.sk * prm.kb_per_split;
   r.kb1 = min(prm.kblocks, r.kb0 + prm.kb_per_split);
   if (r.kb1 < r.kb0) r.kb1 = r.kb0;
@@ -444,6 +478,82 @@ __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic,
   return static_cast<uint32_t>(r);
 }
 
+// Writes pass ps of unit w for this thread's kCols columns gj0.. of row gi,
+// acc holding the exact int32 sums.  out_kind 0: (x mod p) as uint8 in plane p;
+// 1: x as int32 in plane (sk, p); 2: pass 0 of a pair parks (x mod p) in the
+// thread's stash slots (stash[v * kEpiThreads]), pass 1 combines it with its
+// own residue into the pair residue, written as uint16 in plane q (an odd
+// last modulus writes its own residue there).
+__device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Unit& w, int ps, int64_t gi,
+                                           int64_t gj0, const GemmParams& prm, uint4* stash) {
+  const int p = w.p + ps;
+  const uint32_t pp = c_mod.p[p], mg = c_mod.magic[p], bs = c_mod.bias[p];
+  if (prm.out_kind == 2 && ps == 0 && w.passes == 2) {
+#pragma unroll
+    for (int v = 0; v < kCols / 16; ++v) {
+      uint32_t word[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        word[b] = mod_p(acc[16 * v + 4 * b], pp, mg, bs) | (mod_p(acc[16 * v + 4 * b + 1], pp, mg, bs) << 8) |
+                  (mod_p(acc[16 * v + 4 * b + 2], pp, mg, bs) << 16) |
+                  (mod_p(acc[16 * v + 4 * b + 3], pp, mg, bs) << 24);
+      }
+      stash[v * kEpiThreads] = make_uint4(word[0], word[1], word[2], word[3]);
+    }
+    return;
+  }
+  if (gi >= prm.M) return;
+  if (prm.out_kind == 0) {
+    uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(p) * prm.out_plane + gi * prm.ldo + gj0;
+#pragma unroll
+    for (int v = 0; v < kCols / 16; ++v) {
+      if (gj0 + 16 * v < prm.ldo) {
+        uint32_t word[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          word[b] = mod_p(acc[16 * v + 4 * b], pp, mg, bs) | (mod_p(acc[16 * v + 4 * b + 1], pp, mg, bs) << 8) |
+                    (mod_p(acc[16 * v + 4 * b + 2], pp, mg, bs) << 16) |
+                    (mod_p(acc[16 * v + 4 * b + 3], pp, mg, bs) << 24);
+        }
+        *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+      }
+    }
+  } else if (prm.out_kind == 1) {
+    int32_t* dst = static_cast<int32_t*>(prm.out) + (static_cast<int64_t>(w.sk) * prm.n + p) * prm.out_plane +
+                   gi * prm.ldo + gj0;
+#pragma unroll
+    for (int v = 0; v < kCols / 4; ++v)
+      if (gj0 + 4 * v < prm.ldo)
+        *reinterpret_cast<int4*>(dst + 4 * v) = make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+  } else {
+    uint16_t* dst = static_cast<uint16_t*>(prm.out) + static_cast<int64_t>(w.q) * prm.out_plane + gi * prm.ldo + gj0;
+    const bool pair = w.passes == 2;
+    const uint32_t u0 = c_mod.pu0[w.q], u1 = c_mod.pu1[w.q], m = c_mod.pm[w.q], pmg = c_mod.pmagic[w.q];
+#pragma unroll
+    for (int v = 0; v < kCols / 16; ++v) {
+      const uint4 first = pair ? stash[v * kEpiThreads] : make_uint4(0, 0, 0, 0);
+      const uint32_t fw[4] = {first.x, first.y, first.z, first.w};
+      uint32_t r[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t c = mod_p(acc[16 * v + e], pp, mg, bs);
+        if (pair) {
+          const uint32_t t = ((fw[e >> 2] >> (8 * (e & 3))) & 0xFFu) * u0 + c * u1;  // < 2^25
+          r[e] = t - (__umulhi(t, pmg) >> 10) * m;
+        } else {
+          r[e] = c;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (gj0 + 16 * v + 8 * h < prm.ldo)
+          *reinterpret_cast<uint4*>(dst + 16 * v + 8 * h) =
+              make_uint4(r[8 * h] | (r[8 * h + 1] << 16), r[8 * h + 2] | (r[8 * h + 3] << 16),
+                         r[8 * h + 4] | (r[8 * h + 5] << 16), r[8 * h + 6] | (r[8 * h + 7] << 16));
+    }
+  }
+}
+
 template <bool LONG>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -488,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const int units = prm.n * prm.splits * prm.tiles_m * prm.tiles_n;
+  const int units = prm.mod_units * prm.splits * prm.tiles_m * prm.tiles_n;
 
   if (warp < 4) regs_dec<kCtrlRegs>();
   if (warp == 0) {
@@ -502,18 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = decode_unit(u, prm);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(full0 + 8 * stage, kStageBytes);
-          tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p, full0 + 8 * stage);
-          tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, kb * BK, w.nt * BN, w.p, full0 + 8 * stage);
-          issued_parity[stage] = static_cast<int>(phase);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+        for (int ps = 0; ps < w.passes && ok; ++ps) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full0 + 8 * stage, kStageBytes);
+            tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p + ps, full0 + 8 * stage);
+            tma_load_3d(smem_u32(sB + stage * kBBytes), &tmB, kb * BK, w.nt * BN, w.p + ps, full0 + 8 * stage);
+            issued_parity[stage] = static_cast<int>(phase);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
@@ -534,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = decode_unit(u, prm);
+        for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
           const int c1 = min(w.kb1, c0 + kChunkKB);
           if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
@@ -579,65 +692,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     bool ok = true;
+    uint4* stash = reinterpret_cast<uint4*>(smem + kStages * kStageBytes + kBarBytes) + (threadIdx.x - 128);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit w = decode_unit(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
-      int32_t acc[kCols];
-#pragma unroll
-      for (int e = 0; e < kCols; ++e) acc[e] = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(ab * BN + half * kCols);
-        uint32_t va[32], vb[32];
-        tmem_ld32(taddr, va);
-        tmem_wait_ld(va);
-        drain_chunk<LONG, 0>(acc, taddr, va, vb);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce0 + 8 * ab);
-        ab ^= 1;
-        if (ab == 0) aphase ^= 1u;
-      }
-      if (!ok) break;
-      const uint32_t offset = LONG ? 0u : static_cast<uint32_t>(nchunks) * kMagicBits;  // the 1.5 * 2^23 adds
-#pragma unroll
-      for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
-
       const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
-      if (gi < prm.M) {
-        if (prm.out_kind == 0) {
-          const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
-          uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(w.p) * prm.out_plane +
-                         gi * prm.ldo + gj0;
+      for (int ps = 0; ps < w.passes && ok; ++ps) {
+        int32_t acc[kCols];
 #pragma unroll
-          for (int v = 0; v < kCols / 16; ++v) {
-            if (gj0 + 16 * v < prm.ldo) {
-              uint32_t word[4];
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                word[b] = mod_p(acc[16 * v + 4 * b], p, mg, bs) |
-                          (mod_p(acc[16 * v + 4 * b + 1], p, mg, bs) << 8) |
-                          (mod_p(acc[16 * v + 4 * b + 2], p, mg, bs) << 16) |
-                          (mod_p(acc[16 * v + 4 * b + 3], p, mg, bs) << 24);
-              }
-              *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
-            }
+        for (int e = 0; e < kCols; ++e) acc[e] = 0;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+            ok = false;
+            break;
           }
-        } else {
-          int32_t* dst = static_cast<int32_t*>(prm.out) +
-                         (static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.out_plane + gi * prm.ldo + gj0;
-#pragma unroll
-          for (int v = 0; v < kCols / 4; ++v)
-            if (gj0 + 4 * v < prm.ldo)
-              *reinterpret_cast<int4*>(dst + 4 * v) =
-                  make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(ab * BN + half * kCols);
+          uint32_t va[32], vb[32];
+          tmem_ld32(taddr, va);
+          tmem_wait_ld(va);
+          drain_chunk<LONG, 0>(acc, taddr, va, vb);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce0 + 8 * ab);
+          ab ^= 1;
+          if (ab == 0) aphase ^= 1u;
         }
+        if (!ok) break;
+        const uint32_t offset = LONG ? 0u : static_cast<uint32_t>(nchunks) * kMagicBits;  // the 1.5 * 2^23 adds
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
+        store_tile(acc, w, ps, gi, gj0, prm, stash);
       }
     }
   }
@@ -700,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const int units = prm.n * prm.splits * prm.tiles_m * prm.tiles_n;
+  const int units = prm.mod_units * prm.splits * prm.tiles_m * prm.tiles_n;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int npairs = static_cast<int>(gridDim.x >> 1);
 
@@ -718,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
         const Unit w = decode_unit(u, prm);
+        for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
             ok = false;
@@ -726,9 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full_leader = cluster_addr(full0 + 8 * stage, 0);
           if (leader) mbar_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
           tma_load_3d_pair(smem_u32(sA + stage * kABytes), &tmA, kb * BK,
-                      w.mt * kPairM + static_cast<int>(rank) * BM, w.p, full_leader);
+                      w.mt * kPairM + static_cast<int>(rank) * BM, w.p + ps, full_leader);
           tma_load_3d_pair(smem_u32(sB + stage * kPairBBytes), &tmB, kb * BK,
-                      w.nt * BN + static_cast<int>(rank) * kBHalf, w.p, full_leader);
+                      w.nt * BN + static_cast<int>(rank) * kBHalf, w.p + ps, full_leader);
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == kPairStages) {
             stage = 0;
@@ -754,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
         const Unit w = decode_unit(u, prm);
+        for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
           const int c1 = min(w.kb1, c0 + kPairChunkKB);
           if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
@@ -799,62 +888,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aphase = 0;
     bool ok = true;
+    uint4* stash = reinterpret_cast<uint4*>(smem + kPairStages * kPairStageBytes + kBarBytes) + (threadIdx.x - 128);
     for (int u = pair; u < units && ok; u += npairs) {
       const Unit w = decode_unit(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kPairChunkKB - 1) / kPairChunkKB;
-      int32_t acc[kCols];
-#pragma unroll
-      for (int e = 0; e < kCols; ++e) acc[e] = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(ab * BN + half * kCols);
-        uint32_t va[32], vb[32];
-        tmem_ld32(taddr, va);
-        tmem_wait_ld(va);
-        drain_chunk<true, 0>(acc, taddr, va, vb);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(cluster_addr(acce0 + 8 * ab, 0));
-        ab ^= 1;
-        if (ab == 0) aphase ^= 1u;
-      }
-      if (!ok) break;
-
       const int64_t gi = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + row_in_tile;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
-      if (gi < prm.M) {
-        if (prm.out_kind == 0) {
-          const uint32_t p = c_mod.p[w.p], mg = c_mod.magic[w.p], bs = c_mod.bias[w.p];
-          uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(w.p) * prm.out_plane +
-                         gi * prm.ldo + gj0;
+      for (int ps = 0; ps < w.passes && ok; ++ps) {
+        int32_t acc[kCols];
 #pragma unroll
-          for (int v = 0; v < kCols / 16; ++v) {
-            if (gj0 + 16 * v < prm.ldo) {
-              uint32_t word[4];
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                word[b] = mod_p(acc[16 * v + 4 * b], p, mg, bs) |
-                          (mod_p(acc[16 * v + 4 * b + 1], p, mg, bs) << 8) |
-                          (mod_p(acc[16 * v + 4 * b + 2], p, mg, bs) << 16) |
-                          (mod_p(acc[16 * v + 4 * b + 3], p, mg, bs) << 24);
-              }
-              *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
-            }
+        for (int e = 0; e < kCols; ++e) acc[e] = 0;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+            ok = false;
+            break;
           }
-        } else {
-          int32_t* dst = static_cast<int32_t*>(prm.out) +
-                         (static_cast<int64_t>(w.sk) * prm.n + w.p) * prm.out_plane + gi * prm.ldo + gj0;
-#pragma unroll
-          for (int v = 0; v < kCols / 4; ++v)
-            if (gj0 + 4 * v < prm.ldo)
-              *reinterpret_cast<int4*>(dst + 4 * v) =
-                  make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(ab * BN + half * kCols);
+          uint32_t va[32], vb[32];
+          tmem_ld32(taddr, va);
+          tmem_wait_ld(va);
+          drain_chunk<true, 0>(acc, taddr, va, vb);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(cluster_addr(acce0 + 8 * ab, 0));
+          ab ^= 1;
+          if (ab == 0) aphase ^= 1u;
         }
+        if (!ok) break;
+        store_tile(acc, w, ps, gi, gj0, prm, stash);
       }
     }
   }
@@ -952,6 +1015,7 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
   prm.splits = splits;
   prm.kb_per_split = static_cast<int>((kpad / kKBlock + splits - 1) / splits) * (kKBlock / BK);
   prm.out_kind = out_kind;
+  prm.mod_units = out_kind == 2 ? (n + 1) / 2 : n;
   prm.ldo = ldo;
   prm.out_plane = out_plane;
   prm.out = out;
@@ -963,11 +1027,11 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
   if (!make_slice_map(&tmA, a_slices, M, kpad, a_plane, n, BM) ||
       !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, pairs ? kBHalf : BN))
     return cudaErrorInvalidValue;
-  const int64_t units = static_cast<int64_t>(n) * splits * prm.tiles_m * prm.tiles_n;
+  const int64_t units = static_cast<int64_t>(prm.mod_units) * splits * prm.tiles_m * prm.tiles_n;
   const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK >= 1024;
   auto kernel = pairs ? residue_gemm_pair_kernel
                       : (long_chunks ? residue_gemm_kernel<true> : residue_gemm_kernel<false>);
-  const size_t smem = pairs ? kPairSmemBytes : kSmemBytes;
+  const size_t smem = (pairs ? kPairSmemBytes : kSmemBytes) + kStashBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the pool has the registers: refuse to launch

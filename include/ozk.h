@@ -191,6 +191,11 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb,
  *              (their sum is the exact dot product); ldo >= N, a multiple of 4;
  *              each share must hold at most OZK_SPLIT_MAX_K terms, so K beyond
  *              that needs at least ceil(kpad / OZK_SPLIT_MAX_K) splits.
+ *  out_kind 2: out is uint16 [(n+1)/2][M][ldo]: plane j holds the residue of
+ *              the moduli pair (2j, 2j+1), the unique r < p_2j p_2j+1 with
+ *              r = c_2j mod p_2j and r = c_2j+1 mod p_2j+1 (the first CRT step,
+ *              done in the epilogue); for odd n the last plane holds c_n-1.
+ *              ldo >= N, a multiple of 8; splits must be 1 and K < 2^17.
  * K is the inner dimension the slices were quantised with (kpad = ozk_kpad(K)).
  * splits in 1..64 and at most kpad/64; violations return OZK_ERR_INVALID_ARG. */
 int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
@@ -200,8 +205,9 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
 /* CRT reconstruction with symmetric lift, undo scaling, FP64 write:
  * C_ij = RN-even(X_ij 2^-(s_i + t_j)) with X_ij the unique integer in
  * [-P/2, P/2) congruent to the residues; NaN where s_i or t_j is
- * OZK_SCALE_NONFINITE.  in / in_kind / ldi / splits as ozk_residue_gemm's out;
- * int32 partial sums are reduced mod p one by one before they are added. */
+ * OZK_SCALE_NONFINITE.  in / in_kind / ldi / splits as ozk_residue_gemm's out
+ * (in_kind 0, 1 or 2); int32 partial sums are reduced mod p one by one before
+ * they are added. */
 int ozk_crt_combine(int64_t M, int64_t N, int n_moduli, const void* in,
                     int in_kind, int64_t ldi, int splits, const int32_t* s,
                     const int32_t* t, double* C, int64_t ldc, ozk_stream_t stream);

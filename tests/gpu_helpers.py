@@ -59,6 +59,9 @@ def run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0, splits=1):
     if out_kind == 0:
         ldo = (N + 15) // 16 * 16
         out = torch.full((n, M, ldo), 0xEE, dtype=torch.uint8, device="cuda")
+    elif out_kind == 2:
+        ldo = (N + 7) // 8 * 8
+        out = torch.full(((n + 1) // 2, M, ldo), -1, dtype=torch.int16, device="cuda")
     else:
         ldo = (N + 3) // 4 * 4
         out = torch.full((splits, n, M, ldo), -7, dtype=torch.int32, device="cuda")

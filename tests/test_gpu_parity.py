@@ -67,18 +67,34 @@ def check_stages(A, B, n, splits=1):
     assert np.array_equal(g32, raw.astype(np.int64))
     out8, ld8 = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
     assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    # 3b. residues of the moduli pairs (2j, 2j+1) as uint16: the unique r < p_2j p_2j+1
+    #     with r = c_2j mod p_2j and r = c_2j+1 mod p_2j+1; an odd last plane holds c_n-1
+    out16, ld16 = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=2)
+    g16 = out16.cpu().numpy()[:, :, :N].view(np.uint16).astype(np.int64)
+    ps = oracle.moduli(n)
+    for j in range((n + 1) // 2):
+        if 2 * j + 1 < n:
+            assert np.all(g16[j] < ps[2 * j] * ps[2 * j + 1])
+            assert np.array_equal(g16[j] % ps[2 * j], cmod[2 * j].astype(np.int64))
+            assert np.array_equal(g16[j] % ps[2 * j + 1], cmod[2 * j + 1].astype(np.int64))
+        else:
+            assert np.array_equal(g16[j], cmod[2 * j].astype(np.int64))
     # 4. lifted integers, from either representation
     Xo = oracle.crt(cmod, n)
     X8 = run_lift(out8, 0, ld8, 1, M, N, n).cpu().numpy().view(np.uint32)
     assert np.array_equal(X8, Xo)
     X32 = run_lift(out32, 1, ld32, splits, M, N, n).cpu().numpy().view(np.uint32)
     assert np.array_equal(X32, Xo)
+    X16 = run_lift(out16, 2, ld16, 1, M, N, n).cpu().numpy().view(np.uint32)
+    assert np.array_equal(X16, Xo)
     # 5. undo scaling, write double
     Co = oracle.dgemm(A, B, n)
     C8 = run_combine(out8, 0, ld8, 1, s, t, M, N, n).cpu().numpy()
     assert same_bits(C8, Co)
     C32 = run_combine(out32, 1, ld32, splits, s, t, M, N, n).cpu().numpy()
     assert same_bits(C32, Co)
+    C16 = run_combine(out16, 2, ld16, 1, s, t, M, N, n).cpu().numpy()
+    assert same_bits(C16, Co)
     return Co
 
 
@@ -110,20 +126,27 @@ def test_split_k_partials_sum_to_the_exact_product(splits):
 
 @pytest.mark.parametrize("n", list(range(2, 21)))
 def test_crt_wide_outputs_every_moduli_count(n):
-    """Outputs wide enough for the kernels compiled per moduli count: random
-    residues (any residue vector is a valid CRT input), scales that give
+    """Outputs wide enough for the kernels compiled per moduli count (uint16
+    residues of moduli pairs): random residues (any residue vector is a valid
+    CRT input), scales that give
     normal, subnormal, underflowing, overflowing and NaN results; sampled
     outputs against the oracle's CRT and rounding."""
     M, N = 2048, 640
     rng = np.random.default_rng(100 + n)
-    res = np.stack([rng.integers(0, p, size=(M, N), dtype=np.uint8) for p in oracle.moduli(n)])
+    ps = [int(p) for p in oracle.moduli(n)]
+    # random residues of the moduli pairs; the byte residues follow from them
+    pair = np.stack([rng.integers(0, ps[2 * j] * ps[2 * j + 1] if 2 * j + 1 < n else ps[2 * j], size=(M, N))
+                     for j in range((n + 1) // 2)]).astype(np.int64)
+    res = np.stack([pair[k // 2] % p for k, p in enumerate(ps)]).astype(np.uint8)
     s = rng.integers(-200, 200, M).astype(np.int32)
     t = rng.integers(-200, 200, N).astype(np.int32)
     s[10:20] = 1050 - 8 * n   # |X| 2^-(s+t) near the subnormal range
     s[20:30] = -1000 + 8 * n  # near overflow
     s[3] = oracle.NONFINITE
     t[5] = oracle.NONFINITE
-    C = run_combine(dev(res), 0, N, 1, dev(s), dev(t), M, N, n).cpu().numpy()
+    C = run_combine(dev(pair.astype(np.uint16).view(np.int16)), 2, N, 1, dev(s), dev(t), M, N, n).cpu().numpy()
+    C8 = run_combine(dev(res), 0, N, 1, dev(s), dev(t), M, N, n).cpu().numpy()
+    assert same_bits(C8, C)  # byte residues through the runtime-count kernel
     ii = np.concatenate([rng.integers(0, M, 3000), np.arange(10, 30).repeat(20), np.full(50, 3)])
     jj = np.concatenate([rng.integers(0, N, 3000), rng.integers(0, N, 400), rng.integers(0, N, 50)])
     ii = np.concatenate([ii, rng.integers(0, M, 50)])
@@ -140,6 +163,14 @@ def test_crt_wide_outputs_every_moduli_count(n):
 @pytest.mark.parametrize("n", [8, 11, 14, 17, 20])
 def test_dgemm_bit_exact(M, N, K, n):
     A, B = inputs(M, N, K, seed=1 + n, kind="special")
+    assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
+
+
+@pytest.mark.parametrize("M,N,K,n", [(65, 300, 8200, 13), (130, 90, 8192, 14)])
+def test_dgemm_bit_exact_pair_residue_path(M, N, K, n):
+    """K of 8192 or more: the GEMM's epilogue writes uint16 residues of moduli
+    pairs (an odd last modulus alone) and the combine starts from them."""
+    A, B = inputs(M, N, K, seed=M + N + K + n)
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
 
