@@ -338,6 +338,20 @@ int ozk_beta(int64_t K, int n_moduli) {
 
 int64_t ozk_kpad(int64_t K) { return K <= 0 ? 0 : (K + kKBlock - 1) / kKBlock * kKBlock; }
 
+int ozk_moduli_for_bits(int64_t K, int target_bits) {
+  if (target_bits < 1) return -OZK_ERR_INVALID_ARG;
+  for (int n = 2; n <= kMaxModuli; ++n)
+    if (beta_for(K, n) >= target_bits) return n;
+  return -OZK_ERR_UNSUPPORTED;
+}
+
+int ozk_dgemm_bits(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                   int64_t ldb, double* C, int64_t ldc, int target_bits, ozk_stream_t stream) {
+  const int n = K == 0 ? 2 : ozk_moduli_for_bits(K, target_bits);
+  if (n < 0) return -n;
+  return ozk_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n, stream);
+}
+
 size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli) {
   if (M <= 0 || N <= 0 || K <= 0 || K > OZK_MAX_K) return 0;
   if (M > kMaxDim || N > kMaxDim || beta_for(K, n_moduli) < 1) return 0;

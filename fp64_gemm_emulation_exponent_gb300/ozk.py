@@ -35,6 +35,8 @@ SIGNATURES = {
     "ozk_moduli": (_i32, [_i32, _vp]),
     "ozk_beta": (_i32, [_i64, _i32]),
     "ozk_kpad": (_i64, [_i64]),
+    "ozk_moduli_for_bits": (_i32, [_i64, _i32]),
+    "ozk_dgemm_bits": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
     "ozk_dgemm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_dgemm_ws": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp]),
@@ -108,6 +110,10 @@ def ozk_kpad(K: int) -> int:
     return lib().ozk_kpad(K)
 
 
+def ozk_moduli_for_bits(K: int, target_bits: int) -> int:
+    return lib().ozk_moduli_for_bits(K, target_bits)
+
+
 def ozk_workspace_size(M: int, N: int, K: int, n_moduli: int) -> int:
     return lib().ozk_workspace_size(M, N, K, n_moduli)
 
@@ -163,8 +169,9 @@ def ozk_release_cached():
     return _call("ozk_release_cached")
 
 
-def dgemm(A, B, n_moduli: int = 14, out=None, stream=None):
-    """C = A @ B for float64 CUDA tensors through ozk_dgemm."""
+def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None):
+    """C = A @ B for float64 CUDA tensors through ozk_dgemm (or ozk_dgemm_bits
+    when target_bits is given: the moduli count then follows from K)."""
     import torch
 
     M, K = A.shape
@@ -173,7 +180,11 @@ def dgemm(A, B, n_moduli: int = 14, out=None, stream=None):
         raise ValueError("inner dimensions differ")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float64, device=A.device)
-    ozk_dgemm(M, N, K, A, _ld(A), B, _ld(B), out, _ld(out), n_moduli, stream)
+    if target_bits is None:
+        ozk_dgemm(M, N, K, A, _ld(A), B, _ld(B), out, _ld(out), n_moduli, stream)
+    else:
+        _call("ozk_dgemm_bits", M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(out), _ld(out), target_bits,
+              _stream(stream))
     return out
 
 

@@ -72,6 +72,15 @@ int ozk_moduli(int n_moduli, int32_t* out);
  * or -OZK_ERR_UNSUPPORTED when the moduli cannot cover K. */
 int ozk_beta(int64_t K, int n_moduli);
 
+/* The moduli count for a target precision: the smallest n_moduli in 2..20
+ * with ozk_beta(K, n_moduli) >= target_bits, i.e. every element of A and B
+ * keeps at least target_bits bits below the largest magnitude of its row of A
+ * or column of B (the fixed-mantissa contract of the "Day 12" page's
+ * precision-contract list, "先定義公平比較": target mantissa bits beside the
+ * modulus count).  Returns the count, -OZK_ERR_INVALID_ARG when
+ * target_bits < 1, or -OZK_ERR_UNSUPPORTED when 20 moduli do not reach it. */
+int ozk_moduli_for_bits(int64_t K, int target_bits);
+
 /* Row length of the residue slices: K rounded up to a multiple of 64. */
 int64_t ozk_kpad(int64_t K);
 
@@ -83,6 +92,13 @@ size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli);
 /* ------------------------------------------------------------------ */
 /* The GEMM.                                                           */
 /* ------------------------------------------------------------------ */
+
+/* ozk_dgemm with n_moduli = ozk_moduli_for_bits(K, target_bits); errors of
+ * that choice are returned as positive status codes.  K = 0 (nothing to
+ * reduce) uses 2 moduli. */
+int ozk_dgemm_bits(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                   const double* B, int64_t ldb, double* C, int64_t ldc,
+                   int target_bits, ozk_stream_t stream);
 
 /* C = A * B with n_moduli residue GEMMs.  A, B, C are device pointers.
  * C must not overlap A or B (OZK_ERR_INVALID_ARG).  Rows of A or columns of

@@ -59,6 +59,25 @@ def test_beta_matches_the_oracle():
             assert ozk.ozk_beta(K, n) == want, (K, n)
 
 
+def test_moduli_for_bits_is_the_smallest_count_reaching_the_target():
+    # against the oracle's own beta: the chosen count reaches the target and one fewer does not
+    for K in [1, 64, 1000, 4096, 8192, 65536, 131072, 10**6]:
+        betas = {}
+        for n in range(2, 21):
+            try:
+                betas[n] = oracle.beta(K, n)
+            except oracle.OracleError:
+                betas[n] = 0
+        for target in [1, 8, 20, 26, 30, 34, 40, 46, 48, 50, 53, 60, 72, 80]:
+            got = ozk.ozk_moduli_for_bits(K, target)
+            reach = [n for n in range(2, 21) if betas[n] >= target]
+            if not reach:
+                assert got == -ozk.OZK_ERR_UNSUPPORTED, (K, target)
+            else:
+                assert got == reach[0], (K, target)
+    assert ozk.ozk_moduli_for_bits(4096, 0) == -ozk.OZK_ERR_INVALID_ARG
+
+
 def test_kpad():
     assert [ozk.ozk_kpad(k) for k in [0, 1, 63, 64, 65, 128, 131071]] == [0, 64, 64, 64, 128, 128, 131072]
 

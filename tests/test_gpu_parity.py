@@ -190,6 +190,25 @@ def test_dgemm_k_beyond_one_int32_sum(M, N, K, n):
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
 
+@pytest.mark.parametrize("target", [30, 40, 48])
+def test_dgemm_bits_picks_the_count_and_keeps_its_bound(target):
+    """ozk_dgemm_bits = ozk_dgemm with the smallest count whose beta reaches the
+    target; the result keeps the a-priori bound of its beta."""
+    A, B = inputs(96, 80, 3000, seed=target)
+    n = ozk.ozk_moduli_for_bits(3000, target)
+    assert 2 <= n <= 20 and oracle.beta(3000, n) >= target
+    Cb = ozk.dgemm(dev(A), dev(B), target_bits=target).cpu().numpy()
+    assert same_bits(Cb, dgemm(A, B, n))
+    R = oracle.dot2(A, B)
+    beta = oracle.beta(3000, n)
+    so, to = oracle.scale(A, B, n)
+    bound = (np.ldexp(1.0, -so.astype(np.int64))[:, None] * np.abs(B).sum(0)[None, :]
+             + np.ldexp(1.0, -to.astype(np.int64))[None, :] * np.abs(A).sum(1)[:, None]
+             + 3000 * np.ldexp(1.0, -(so[:, None].astype(np.int64) + to[None, :])) + np.spacing(np.abs(R)))
+    assert np.all(np.abs(Cb - R) <= bound)
+    assert beta >= target
+
+
 def test_dgemm_square256_normal_n14():
     w = workloads.WORKLOADS["square256_normal"]
     A, B = workloads.workload_operands(w)
