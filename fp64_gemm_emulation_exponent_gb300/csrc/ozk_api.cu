@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -130,11 +131,18 @@ struct DevInfo {
 };
 std::map<int, DevInfo> g_dev;
 std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_ws;  // cached workspaces
+// Per device: the device copies of the host operands, the copy streams and
+// events of the host path, and a lock held for a whole host call (one host
+// call per device at a time).
+constexpr int kMaxHostBlocks = 8;
 struct HostBufs {
   double* A = nullptr;
   double* B = nullptr;
   double* C = nullptr;
   size_t a = 0, b = 0, c = 0;
+  cudaStream_t in = nullptr, out = nullptr;        // host-to-device and device-to-host copies
+  cudaEvent_t ev[2 * kMaxHostBlocks + 1] = {};      // B in, A blocks in, C blocks computed
+  std::mutex call;
 };
 std::map<int, HostBufs> g_host;
 
@@ -234,6 +242,28 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   off = align_up(off + o_plane * static_cast<size_t>(L.planes), 256);
   L.total = off;
   return L;
+}
+
+// The workspace cached for (current device, stream), grown to `need` bytes.
+int cached_workspace(cudaStream_t st, size_t need, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  auto& slot = g_ws[{dev, st}];
+  if (slot.second < need) {
+    if (slot.first) {
+      if (cudaStreamSynchronize(st) != cudaSuccess) return OZK_ERR_CUDA;
+      cudaFree(slot.first);
+      slot = {nullptr, 0};
+    }
+    if (cudaMalloc(&slot.first, need) != cudaSuccess) {
+      slot = {nullptr, 0};
+      return OZK_ERR_WORKSPACE;
+    }
+    slot.second = need;
+  }
+  *out = slot.first;
+  return OZK_OK;
 }
 
 int record(ozk_event_t* ev, int idx, cudaStream_t stream) {
@@ -381,26 +411,7 @@ int ozk_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if ((rc = check_device(nullptr))) return rc;
   const size_t need = K > 0 ? layout_for(M, N, K, n_moduli).total : 0;
   void* ws = nullptr;
-  if (need) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    std::lock_guard<std::mutex> lock(g_mutex);
-    auto& slot = g_ws[{dev, st}];
-    if (slot.second < need) {
-      if (slot.first) {
-        if (cudaStreamSynchronize(st) != cudaSuccess) return OZK_ERR_CUDA;
-        cudaFree(slot.first);
-        slot = {nullptr, 0};
-      }
-      if (cudaMalloc(&slot.first, need) != cudaSuccess) {
-        slot = {nullptr, 0};
-        return OZK_ERR_WORKSPACE;
-      }
-      slot.second = need;
-    }
-    ws = slot.first;
-  }
+  if (need && (rc = cached_workspace(reinterpret_cast<cudaStream_t>(stream), need, &ws))) return rc;
   return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, ws, need,
                    reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
@@ -410,42 +421,100 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
   int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli);
   if (rc) return rc;
   if (M == 0 || N == 0) return OZK_OK;
-  if ((rc = check_device(nullptr))) return rc;
+  int sms = 0;
+  if ((rc = check_device(&sms))) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
-  double *dA, *dB, *dC;
+  HostBufs* hp;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    HostBufs& h = g_host[dev];
-    auto grow = [&](double*& p, size_t& have, size_t need) -> bool {
-      if (have >= need) return true;
-      if (p) {
-        cudaDeviceSynchronize();
-        cudaFree(p);
-      }
-      p = nullptr;
-      have = 0;
-      if (need && cudaMalloc(&p, need) != cudaSuccess) return false;
-      have = need;
-      return true;
-    };
-    if (!grow(h.A, h.a, sizeof(double) * static_cast<size_t>(M * K)) ||
-        !grow(h.B, h.b, sizeof(double) * static_cast<size_t>(K * N)) ||
-        !grow(h.C, h.c, sizeof(double) * static_cast<size_t>(M * N)))
-      return OZK_ERR_WORKSPACE;
-    dA = h.A;
-    dB = h.B;
-    dC = h.C;
+    hp = &g_host[dev];
   }
-  if (K > 0) {
-    OZK_CUDA(cudaMemcpy2DAsync(dA, sizeof(double) * K, A, sizeof(double) * lda, sizeof(double) * K, M,
-                               cudaMemcpyHostToDevice, st));
+  HostBufs& h = *hp;
+  std::lock_guard<std::mutex> call_lock(h.call);
+  auto grow = [&](double*& p, size_t& have, size_t need) -> bool {
+    if (have >= need) return true;
+    if (p) {
+      cudaDeviceSynchronize();
+      cudaFree(p);
+    }
+    p = nullptr;
+    have = 0;
+    if (need && cudaMalloc(&p, need) != cudaSuccess) return false;
+    have = need;
+    return true;
+  };
+  if (!grow(h.A, h.a, sizeof(double) * static_cast<size_t>(M * K)) ||
+      !grow(h.B, h.b, sizeof(double) * static_cast<size_t>(K * N)) ||
+      !grow(h.C, h.c, sizeof(double) * static_cast<size_t>(M * N)))
+    return OZK_ERR_WORKSPACE;
+  if (!h.in) {
+    if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
+      return OZK_ERR_CUDA;
+    for (auto& e : h.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
+  }
+  double *dA = h.A, *dB = h.B, *dC = h.C;
+  if (K == 0) {
+    OZK_CUDA(cudaMemset2DAsync(dC, sizeof(double) * N, 0, sizeof(double) * N, M, st));
+  } else {
+    // Copies in on h.in, the stages on the caller's stream, copies out on
+    // h.out.  B comes first (every row block's GEMM needs all of it); A and
+    // C move in row blocks, so the copies of one block overlap the
+    // computation of its neighbours.  Stage by stage this is run_dgemm on
+    // each row block, sharing B's scales and slices.
+    const Layout L = layout_for(M, N, K, n_moduli);
+    void* ws = nullptr;
+    if ((rc = cached_workspace(st, L.total, &ws))) return rc;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
+    int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
+    int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
+    uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
+    uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
+    uint8_t* out = base + L.out;
+    const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
+    const int beta = beta_for(K, n_moduli);
+    // row blocks: four of whole 256-row tiles (the CTA-pair GEMM's height)
+    // once M is large enough to keep every block's GEMM busy, else one
+    const int64_t rows = M >= 2048 ? round_up((M + 3) / 4, 256) : M;
+    const int nb = static_cast<int>((M + rows - 1) / rows);  // <= 4 <= kMaxHostBlocks
+    cudaEvent_t ev_b = h.ev[0];
     OZK_CUDA(cudaMemcpy2DAsync(dB, sizeof(double) * N, B, sizeof(double) * ldb, sizeof(double) * N, K,
-                               cudaMemcpyHostToDevice, st));
+                               cudaMemcpyHostToDevice, h.in));
+    OZK_CUDA(cudaEventRecord(ev_b, h.in));
+    for (int b = 0; b < nb; ++b) {
+      const int64_t r0 = b * rows, mr = std::min(rows, M - r0);
+      OZK_CUDA(cudaMemcpy2DAsync(dA + r0 * K, sizeof(double) * K, A + r0 * lda, sizeof(double) * lda,
+                                 sizeof(double) * K, mr, cudaMemcpyHostToDevice, h.in));
+      OZK_CUDA(cudaEventRecord(h.ev[1 + b], h.in));
+    }
+    OZK_CUDA(cudaStreamWaitEvent(st, ev_b, 0));
+    OZK_CUDA(launch_scale(0, N, K, nullptr, 0, dB, N, beta, nullptr, t, amax + M, st));
+    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, n_moduli, beta, nullptr, 0, bs,
+                             L.b_plane, st));
+    for (int b = 0; b < nb; ++b) {
+      const int64_t r0 = b * rows, mr = std::min(rows, M - r0);
+      void* ob = out + static_cast<size_t>(r0 * L.ldo) * esize;
+      OZK_CUDA(cudaStreamWaitEvent(st, h.ev[1 + b], 0));
+      OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, st));
+      OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
+                               as + r0 * L.kpad, L.a_plane, nullptr, 0, st));
+      OZK_CUDA(launch_residue_gemm(mr, N, L.kpad, as + r0 * L.kpad, L.a_plane, bs, L.b_plane, n_moduli, L.kind,
+                                   ob, L.ldo, L.out_plane, L.splits, sms, st));
+      OZK_CUDA(launch_crt(mr, N, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + r0, t, dC + r0 * N, N,
+                          nullptr, st));
+      OZK_CUDA(cudaEventRecord(h.ev[1 + kMaxHostBlocks + b], st));
+      OZK_CUDA(cudaStreamWaitEvent(h.out, h.ev[1 + kMaxHostBlocks + b], 0));
+      OZK_CUDA(cudaMemcpy2DAsync(C + r0 * ldc, sizeof(double) * ldc, dC + r0 * N, sizeof(double) * N,
+                                 sizeof(double) * N, mr, cudaMemcpyDeviceToHost, h.out));
+    }
+    OZK_CUDA(cudaStreamSynchronize(h.out));
+    OZK_CUDA(cudaStreamSynchronize(st));
+    return OZK_OK;
   }
-  rc = ozk_dgemm(M, N, K, dA, K > 0 ? K : 1, dB, N, dC, N, n_moduli, stream);
-  if (rc) return rc;
   OZK_CUDA(cudaMemcpy2DAsync(C, sizeof(double) * ldc, dC, sizeof(double) * N, sizeof(double) * N, M,
                              cudaMemcpyDeviceToHost, st));
   OZK_CUDA(cudaStreamSynchronize(st));

@@ -128,10 +128,13 @@ int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A,
                        size_t workspace_bytes, ozk_stream_t stream,
                        ozk_event_t* events);
 
-/* C = A * B for HOST matrices (pinned memory gives the fastest copies).
- * Copies A and B to the device, runs ozk_dgemm on the stream, copies C back
- * and synchronises the stream before returning.  Device buffers are cached
- * per device and grow as needed. */
+/* C = A * B for HOST matrices (pinned memory gives the fastest copies and
+ * the overlap).  B is copied first, then A in row blocks on a copy stream of
+ * the library; each block's stages run on `stream` as soon as its rows have
+ * arrived, and its rows of C go back on a second copy stream while the next
+ * block computes.  Returns after C is complete in host memory.  Device
+ * buffers, streams and events are cached per device; concurrent calls on one
+ * device are serialised. */
 int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                    const double* B, int64_t ldb, double* C, int64_t ldc,
                    int n_moduli, ozk_stream_t stream);

@@ -392,6 +392,29 @@ def test_caller_workspace_and_host_buffers_agree():
     assert ozk.ozk_stream_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K", [(2100, 300, 700), (2048, 72, 8200)])
+def test_host_buffers_in_row_blocks(M, N, K):
+    """ozk_dgemm_host on row blocks (M >= 2048: four blocks of whole 256-row
+    tiles, copies overlapping the stages) with padded host leading
+    dimensions: equal to the device path bit for bit, and to the oracle on
+    sampled outputs (byte residues at K = 700, pair residues at K = 8200)."""
+    A, B = inputs(M, N, K, seed=M + K)
+    hA = torch.zeros((M, K + 3), dtype=torch.float64).pin_memory()
+    hB = torch.zeros((K, N + 5), dtype=torch.float64).pin_memory()
+    hC = torch.full((M, N + 2), np.nan, dtype=torch.float64).pin_memory()
+    hA[:, :K] = torch.from_numpy(A)
+    hB[:, :N] = torch.from_numpy(B)
+    ozk.ozk_dgemm_host(M, N, K, hA, K + 3, hB, N + 5, hC, N + 2, 14)
+    C = hC.numpy()[:, :N]
+    assert same_bits(C, dgemm(A, B, 14))
+    assert np.isnan(hC.numpy()[:, N:]).all()  # padding untouched
+    rng = np.random.default_rng(M)
+    ii = np.concatenate([rng.integers(0, M, 200), [0, 767, 768, 1535, 1536, M - 1]])
+    jj = np.concatenate([rng.integers(0, N, 200), [0, N - 1, 0, N - 1, 0, N - 1]])
+    assert same_bits(C[ii, jj], oracle.sample(A, B, 14, ii, jj)[0])
+    assert ozk.ozk_stream_status() == 0
+
+
 def test_deterministic_and_stream_ordered():
     A, B = inputs(300, 700, 900, seed=4)
     dA, dB = dev(A), dev(B)
