@@ -245,7 +245,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(uint32_t rlo, uint32_t rhi) {
   constexpr uint32_t p = modulus_at(k);
   constexpr uint32_t h = p == 256u ? 128u : (p - 1) / 2;
   constexpr uint32_t bias = (kHalfMagicBits - h) * 0x10001u;
-  const uint32_t w = rhi * 0x10000u + rlo + bias;
+  const uint32_t w = __byte_perm(rlo, rhi, 0x5410) + bias;  // (rhi << 16) | rlo, both < 2^16
   uint32_t out;
   asm("add.rn.f16x2 %0, %1, %2;" : "=r"(out) : "r"(w), "r"(kNegHalfMagic2));
   return out;
