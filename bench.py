@@ -345,7 +345,8 @@ def run_gpu(args, ranks: Ranks):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config(w, n),
             "tensor_path": "residues in [-128,127] as fp16 on tcgen05 kind::f16 (sm_103a has no kind::i8); "
-                           "fp32 TMEM sums exact per 256-term chunk",
+                           "fp32 TMEM sums exact per 1024-term chunk (256 below K = 1024); CTA-pair "
+                           "tcgen05.mma.cta_group::2 for K >= 2048",
             "int8_equiv_tops_issued": algo_flops / gemm_s / 1e12,
             "stages_ms": stage_ms, "stage_hbm_roofline": stage_roofline,
             "roofline": roofline, "cpu_baseline": cpu,

@@ -412,6 +412,7 @@ struct Unit {
   int p, q, passes, sk, mt, nt, kb0, kb1;
 };
 
+template <bool PAIRS>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   Unit r;
   r.nt = u % prm.tiles_n;
@@ -420,7 +421,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   u /= prm.tiles_m;
   r.sk = u % prm.splits;
   r.q = u / prm.splits;
-  if (prm.out_kind == 2) {
+  if (PAIRS) {  // out_kind 2
     r.p = 2 * r.q;
     r.passes = min(2, prm.n - r.p);
   } else {
@@ -484,11 +485,12 @@ __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic,
 // thread's stash slots (stash[v * kEpiThreads]), pass 1 combines it with its
 // own residue into the pair residue, written as uint16 in plane q (an odd
 // last modulus writes its own residue there).
+template <bool PAIRS>
 __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Unit& w, int ps, int64_t gi,
                                            int64_t gj0, const GemmParams& prm, uint4* stash) {
   const int p = w.p + ps;
   const uint32_t pp = c_mod.p[p], mg = c_mod.magic[p], bs = c_mod.bias[p];
-  if (prm.out_kind == 2 && ps == 0 && w.passes == 2) {
+  if (PAIRS && ps == 0 && w.passes == 2) {
 #pragma unroll
     for (int v = 0; v < kCols / 16; ++v) {
       uint32_t word[4];
@@ -503,7 +505,7 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
     return;
   }
   if (gi >= prm.M) return;
-  if (prm.out_kind == 0) {
+  if (!PAIRS && prm.out_kind == 0) {
     uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(p) * prm.out_plane + gi * prm.ldo + gj0;
 #pragma unroll
     for (int v = 0; v < kCols / 16; ++v) {
@@ -518,7 +520,7 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
         *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
       }
     }
-  } else if (prm.out_kind == 1) {
+  } else if (!PAIRS) {  // out_kind 1
     int32_t* dst = static_cast<int32_t*>(prm.out) + (static_cast<int64_t>(w.sk) * prm.n + p) * prm.out_plane +
                    gi * prm.ldo + gj0;
 #pragma unroll
@@ -554,7 +556,7 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
   }
 }
 
-template <bool LONG>
+template <bool LONG, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(u, prm);
+        const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
@@ -645,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit(u, prm);
+        const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
           const int c1 = min(w.kb1, c0 + kChunkKB);
@@ -694,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kStages * kStageBytes + kBarBytes) + (threadIdx.x - 128);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit w = decode_unit(u, prm);
+      const Unit w = decode_unit<PAIRS>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
       const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
@@ -724,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t offset = LONG ? 0u : static_cast<uint32_t>(nchunks) * kMagicBits;  // the 1.5 * 2^23 adds
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
-        store_tile(acc, w, ps, gi, gj0, prm, stash);
+        store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
       }
     }
   }
@@ -742,6 +744,7 @@ constexpr int kPairChunkKB = chunk_kb<true>();
 
 // The CTA-pair kernel: tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
 // even CTA of a cluster of two; long (1024-term) chunks only.
+template <bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
@@ -804,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kPairStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit(u, prm);
+        const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
@@ -841,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit(u, prm);
+        const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
           const int c1 = min(w.kb1, c0 + kPairChunkKB);
@@ -890,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kPairStages * kPairStageBytes + kBarBytes) + (threadIdx.x - 128);
     for (int u = pair; u < units && ok; u += npairs) {
-      const Unit w = decode_unit(u, prm);
+      const Unit w = decode_unit<PAIRS>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kPairChunkKB - 1) / kPairChunkKB;
       const int64_t gi = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + row_in_tile;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
@@ -917,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ab == 0) aphase ^= 1u;
         }
         if (!ok) break;
-        store_tile(acc, w, ps, gi, gj0, prm, stash);
+        store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
       }
     }
   }
@@ -1029,8 +1032,11 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
     return cudaErrorInvalidValue;
   const int64_t units = static_cast<int64_t>(prm.mod_units) * splits * prm.tiles_m * prm.tiles_n;
   const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK >= 1024;
-  auto kernel = pairs ? residue_gemm_pair_kernel
-                      : (long_chunks ? residue_gemm_kernel<true> : residue_gemm_kernel<false>);
+  // PAIRS: the pair-residue output (out_kind 2) is compiled in only where used
+  const bool po = out_kind == 2;
+  auto kernel = pairs ? (po ? residue_gemm_pair_kernel<true> : residue_gemm_pair_kernel<false>)
+                      : (long_chunks ? (po ? residue_gemm_kernel<true, true> : residue_gemm_kernel<true, false>)
+                                     : (po ? residue_gemm_kernel<false, true> : residue_gemm_kernel<false, false>));
   const size_t smem = (pairs ? kPairSmemBytes : kSmemBytes) + kStashBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
