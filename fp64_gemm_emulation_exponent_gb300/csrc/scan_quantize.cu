@@ -162,7 +162,9 @@ __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_
 // top bit flipped.  Then, for every modulus,
 //   a' + h = sum_j l_j (2^22j mod p) + (h - 2^(22 NL - 1))   (mod p),
 // one integer below 2^32 whose canonical residue minus h is the balanced
-// residue.  Three limbs hold every beta <= 64; four the rest.
+// residue.  Three limbs hold every beta <= 64; four the rest.  For beta <= 62
+// (NL = 2 below) a'' = a' + 2^63 fits one 64-bit word, and its eight bytes
+// against (2^8b mod p) give x in two 4-byte dot products (dp4a), x < 2^20.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kMask22 = (1u << 22) - 1;
 
@@ -196,11 +198,23 @@ __device__ __forceinline__ void scale_round(uint64_t bits, int32_t sc, uint32_t 
     hi = ~hi + (lo == 0 ? 1u : 0u);
     lo = 0ull - lo;
   }
-  l[0] = static_cast<uint32_t>(lo) & kMask22;
-  l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
-  l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
-  if constexpr (NL == 4) l[3] = (hi >> 2) & kMask22;
-  l[NL - 1] ^= 1u << 21;  // + 2^(22 NL - 1)
+  if constexpr (NL == 2) {  // |a'| <= 2^62: the low word of the two's complement, + 2^63
+    const uint64_t w = lo ^ (1ull << 63);
+    l[0] = static_cast<uint32_t>(w);
+    l[1] = static_cast<uint32_t>(w >> 32);
+  } else {
+    l[0] = static_cast<uint32_t>(lo) & kMask22;
+    l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
+    l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
+    if constexpr (NL == 4) l[3] = (hi >> 2) & kMask22;
+    l[NL - 1] ^= 1u << 21;  // + 2^(22 NL - 1)
+  }
+}
+
+// The four residues 2^(8 (b0 + i)) mod p, one per byte.
+__host__ __device__ constexpr uint32_t byte_weights(int b0, uint32_t p) {
+  return pow2_mod(8 * b0, p) | (pow2_mod(8 * b0 + 8, p) << 8) | (pow2_mod(8 * b0 + 16, p) << 16) |
+         (pow2_mod(8 * b0 + 24, p) << 24);
 }
 
 // Canonical residue of a' + h for the k-th modulus (h = floor(p/2); the
@@ -212,6 +226,14 @@ __device__ __forceinline__ uint32_t shifted_residue(const uint32_t (&l)[NL]) {
     return (l[0] ^ 0x80u) & 0xFFu;  // (a' + 128) mod 256 from the low byte
   } else {
     constexpr uint32_t h = (p - 1) / 2;
+    if constexpr (NL == 2) {
+      // x = sum of the bytes of a'' times 2^8b mod p, plus h - 2^63 mod p:
+      // x < 8 * 255 * 254 + 2 p < 2^20, where umulhi by ceil(2^32/p) divides exactly
+      constexpr uint32_t off = (p - pow2_mod(63, p)) % p + h;
+      constexpr uint32_t m32 = static_cast<uint32_t>(((1ull << 32) + p - 1) / p);
+      const uint32_t x = __dp4a(l[1], byte_weights(4, p), __dp4a(l[0], byte_weights(0, p), off));
+      return x - __umulhi(x, m32) * p;
+    }
     constexpr uint32_t c1 = pow2_mod(22, p), c2 = pow2_mod(44, p);
     constexpr uint32_t off = (p - pow2_mod(22 * NL - 1, p)) % p + h;
     if constexpr (NL == 3) {
@@ -421,8 +443,11 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   const int64_t threads = qp.a_threads + qp.b_threads;
   if (threads == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((threads + kQThreads - 1) / kQThreads);
-  // |a'| <= 2^beta: three 22-bit limbs of two's complement hold beta <= 64
-  if (beta <= 64)
+  // |a'| <= 2^beta: one 64-bit word for beta <= 62, three 22-bit limbs of
+  // two's complement for beta <= 64, four beyond
+  if (beta <= 62)
+    quantize_kernel<2><<<blocks, kQThreads, 0, stream>>>(qp);
+  else if (beta <= 64)
     quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
   else
     quantize_kernel<4><<<blocks, kQThreads, 0, stream>>>(qp);

@@ -118,6 +118,14 @@ def test_stages_other_moduli_counts(n):
     check_stages(A, B, n)
 
 
+@pytest.mark.parametrize("n,K", [(17, 100), (17, 16), (17, 5), (18, 300), (18, 1000), (16, 1), (20, 700)])
+def test_stages_across_the_integer_widths(n, K):
+    """beta 62 (one 64-bit word per scaled element, dp4a residues), 63-64
+    (three 22-bit limbs), 65 and 72 (four limbs): every stage bit-exact."""
+    A, B = inputs(70, 90, K, seed=n * 1000 + K, kind="special")
+    check_stages(A, B, n)
+
+
 @pytest.mark.parametrize("splits", [2, 3, 7])
 def test_split_k_partials_sum_to_the_exact_product(splits):
     A, B = inputs(70, 300, 4000, seed=splits)
