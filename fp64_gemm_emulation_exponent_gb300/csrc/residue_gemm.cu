@@ -11,6 +11,10 @@
 // accumulator in TMEM holds the chunk's exact integer sum.  The epilogue
 // warps read each chunk out of TMEM, convert it exactly (cvt.rni) and add it
 // into int32 registers (exact for K < 2^17), then reduce mod p once per tile.
+// Outputs: the residues mod p as uint8 planes (out_kind 0); the exact int32
+// sums of a K split (1); or, with the two moduli of a pair run back to back
+// on one tile, the uint16 residue of the pair modulus p_2j p_2j+1 (2, the
+// first CRT step), the first modulus's residues parked in shared memory.
 //
 // Two kernels, chosen by the K of a split:
 //  * K >= 2048: CTA pairs (clusters of two).  The even CTA issues
