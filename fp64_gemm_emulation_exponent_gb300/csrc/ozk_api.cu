@@ -134,14 +134,15 @@ std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_ws;  // cache
 // Per device: the device copies of the host operands, the copy streams and
 // events of the host path, and a lock held for a whole host call (one host
 // call per device at a time).
-constexpr int kMaxHostBlocks = 8;
+constexpr int kMaxHostBlocks = 4;
 struct HostBufs {
   double* A = nullptr;
   double* B = nullptr;
   double* C = nullptr;
   size_t a = 0, b = 0, c = 0;
   cudaStream_t in = nullptr, out = nullptr;        // host-to-device and device-to-host copies
-  cudaEvent_t ev[2 * kMaxHostBlocks + 1] = {};      // B in, A blocks in, C blocks computed
+  cudaEvent_t ev_in[2 * kMaxHostBlocks] = {};                  // a block of A or B has arrived
+  cudaEvent_t ev_tile[kMaxHostBlocks * kMaxHostBlocks] = {};  // a tile of C is computed
   std::mutex call;
 };
 std::map<int, HostBufs> g_host;
@@ -453,7 +454,9 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
       return OZK_ERR_CUDA;
-    for (auto& e : h.ev)
+    for (auto& e : h.ev_in)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
+    for (auto& e : h.ev_tile)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
   }
   double *dA = h.A, *dB = h.B, *dC = h.C;
@@ -461,10 +464,13 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     OZK_CUDA(cudaMemset2DAsync(dC, sizeof(double) * N, 0, sizeof(double) * N, M, st));
   } else {
     // Copies in on h.in, the stages on the caller's stream, copies out on
-    // h.out.  B comes first (every row block's GEMM needs all of it); A and
-    // C move in row blocks, so the copies of one block overlap the
-    // computation of its neighbours.  Stage by stage this is run_dgemm on
-    // each row block, sharing B's scales and slices.
+    // h.out.  A moves in row blocks and B in column blocks, interleaved
+    // (B_0, A_0, A_1, B_1, A_2, B_2, ...); each block is scanned and
+    // quantised as soon as it has arrived, and every tile of C whose row and
+    // column blocks are both in is computed next and sent back while later
+    // blocks are still on their way in.  Stage by stage each tile is
+    // run_dgemm on a block of rows and a block of columns, sharing the
+    // scales and slices of its blocks.
     const Layout L = layout_for(M, N, K, n_moduli);
     void* ws = nullptr;
     if ((rc = cached_workspace(st, L.total, &ws))) return rc;
@@ -477,39 +483,68 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     uint8_t* out = base + L.out;
     const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
     const int beta = beta_for(K, n_moduli);
-    // row blocks: four of whole 256-row tiles (the CTA-pair GEMM's height)
-    // once M is large enough to keep every block's GEMM busy, else one
+    // blocks of whole 256-row / 256-column tiles (the CTA-pair GEMM's tile),
+    // four per dimension once it is long enough to keep every tile's GEMM busy
     const int64_t rows = M >= 2048 ? round_up((M + 3) / 4, 256) : M;
-    const int nb = static_cast<int>((M + rows - 1) / rows);  // <= 4 <= kMaxHostBlocks
-    cudaEvent_t ev_b = h.ev[0];
-    OZK_CUDA(cudaMemcpy2DAsync(dB, sizeof(double) * N, B, sizeof(double) * ldb, sizeof(double) * N, K,
-                               cudaMemcpyHostToDevice, h.in));
-    OZK_CUDA(cudaEventRecord(ev_b, h.in));
-    for (int b = 0; b < nb; ++b) {
-      const int64_t r0 = b * rows, mr = std::min(rows, M - r0);
-      OZK_CUDA(cudaMemcpy2DAsync(dA + r0 * K, sizeof(double) * K, A + r0 * lda, sizeof(double) * lda,
-                                 sizeof(double) * K, mr, cudaMemcpyHostToDevice, h.in));
-      OZK_CUDA(cudaEventRecord(h.ev[1 + b], h.in));
+    const int64_t cols = N >= 2048 ? round_up((N + 3) / 4, 256) : N;
+    const int nbr = static_cast<int>((M + rows - 1) / rows);  // <= kMaxHostBlocks
+    const int nbc = static_cast<int>((N + cols - 1) / cols);  // <= kMaxHostBlocks
+    int order[2 * kMaxHostBlocks];  // copy order: +1 + i for A_i, -1 - j for B_j
+    int no = 0;
+    order[no++] = -1;
+    order[no++] = 1;
+    for (int i = 1, j = 1; i < nbr || j < nbc; ++i, ++j) {
+      if (i < nbr) order[no++] = 1 + i;
+      if (j < nbc) order[no++] = -1 - j;
     }
-    OZK_CUDA(cudaStreamWaitEvent(st, ev_b, 0));
-    OZK_CUDA(launch_scale(0, N, K, nullptr, 0, dB, N, beta, nullptr, t, amax + M, st));
-    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, n_moduli, beta, nullptr, 0, bs,
-                             L.b_plane, st));
-    for (int b = 0; b < nb; ++b) {
-      const int64_t r0 = b * rows, mr = std::min(rows, M - r0);
-      void* ob = out + static_cast<size_t>(r0 * L.ldo) * esize;
-      OZK_CUDA(cudaStreamWaitEvent(st, h.ev[1 + b], 0));
-      OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, st));
-      OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
-                               as + r0 * L.kpad, L.a_plane, nullptr, 0, st));
-      OZK_CUDA(launch_residue_gemm(mr, N, L.kpad, as + r0 * L.kpad, L.a_plane, bs, L.b_plane, n_moduli, L.kind,
-                                   ob, L.ldo, L.out_plane, L.splits, sms, st));
-      OZK_CUDA(launch_crt(mr, N, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + r0, t, dC + r0 * N, N,
-                          nullptr, st));
-      OZK_CUDA(cudaEventRecord(h.ev[1 + kMaxHostBlocks + b], st));
-      OZK_CUDA(cudaStreamWaitEvent(h.out, h.ev[1 + kMaxHostBlocks + b], 0));
-      OZK_CUDA(cudaMemcpy2DAsync(C + r0 * ldc, sizeof(double) * ldc, dC + r0 * N, sizeof(double) * N,
-                                 sizeof(double) * N, mr, cudaMemcpyDeviceToHost, h.out));
+    for (int k = 0; k < no; ++k) {
+      if (order[k] > 0) {
+        const int64_t r0 = (order[k] - 1) * rows, mr = std::min(rows, M - r0);
+        OZK_CUDA(cudaMemcpy2DAsync(dA + r0 * K, sizeof(double) * K, A + r0 * lda, sizeof(double) * lda,
+                                   sizeof(double) * K, mr, cudaMemcpyHostToDevice, h.in));
+      } else {
+        const int64_t c0 = (-order[k] - 1) * cols, nc = std::min(cols, N - c0);
+        OZK_CUDA(cudaMemcpy2DAsync(dB + c0, sizeof(double) * N, B + c0, sizeof(double) * ldb, sizeof(double) * nc,
+                                   K, cudaMemcpyHostToDevice, h.in));
+      }
+      OZK_CUDA(cudaEventRecord(h.ev_in[k], h.in));
+    }
+    bool have_a[kMaxHostBlocks] = {}, have_b[kMaxHostBlocks] = {};
+    for (int k = 0; k < no; ++k) {
+      OZK_CUDA(cudaStreamWaitEvent(st, h.ev_in[k], 0));
+      const bool is_a = order[k] > 0;
+      const int blk = is_a ? order[k] - 1 : -order[k] - 1;
+      if (is_a) {
+        const int64_t r0 = blk * rows, mr = std::min(rows, M - r0);
+        OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, st));
+        OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
+                                 as + r0 * L.kpad, L.a_plane, nullptr, 0, st));
+        have_a[blk] = true;
+      } else {
+        const int64_t c0 = blk * cols, nc = std::min(cols, N - c0);
+        OZK_CUDA(launch_scale(0, nc, K, nullptr, 0, dB + c0, N, beta, nullptr, t + c0, amax + M + c0, st));
+        OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, n_moduli, beta, nullptr,
+                                 0, bs + c0 * L.kpad, L.b_plane, st));
+        have_b[blk] = true;
+      }
+      // the tiles this block completes: its row (or column) against every
+      // column (or row) block already in
+      for (int o = 0; o < (is_a ? nbc : nbr); ++o) {
+        const int bi = is_a ? blk : o, bj = is_a ? o : blk;
+        if (!(is_a ? have_b[bj] : have_a[bi])) continue;
+        const int64_t r0 = bi * rows, mr = std::min(rows, M - r0);
+        const int64_t c0 = bj * cols, nc = std::min(cols, N - c0);
+        void* ob = out + static_cast<size_t>(r0 * L.ldo + c0) * esize;
+        OZK_CUDA(launch_residue_gemm(mr, nc, L.kpad, as + r0 * L.kpad, L.a_plane, bs + c0 * L.kpad, L.b_plane,
+                                     n_moduli, L.kind, ob, L.ldo, L.out_plane, L.splits, sms, st));
+        OZK_CUDA(launch_crt(mr, nc, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + r0, t + c0,
+                            dC + r0 * N + c0, N, nullptr, st));
+        cudaEvent_t done = h.ev_tile[bi * kMaxHostBlocks + bj];
+        OZK_CUDA(cudaEventRecord(done, st));
+        OZK_CUDA(cudaStreamWaitEvent(h.out, done, 0));
+        OZK_CUDA(cudaMemcpy2DAsync(C + r0 * ldc + c0, sizeof(double) * ldc, dC + r0 * N + c0, sizeof(double) * N,
+                                   sizeof(double) * nc, mr, cudaMemcpyDeviceToHost, h.out));
+      }
     }
     OZK_CUDA(cudaStreamSynchronize(h.out));
     OZK_CUDA(cudaStreamSynchronize(st));
@@ -531,8 +566,30 @@ int ozk_stream_status(ozk_stream_t stream) {
 int ozk_release_cached(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZK_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
   if (cudaDeviceSynchronize() != cudaSuccess) return OZK_ERR_CUDA;
+  HostBufs* hp = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_host.find(dev);
+    if (it != g_host.end()) hp = &it->second;
+  }
+  if (hp) {  // the entry stays (a call may be waiting on its lock); what it holds goes
+    HostBufs& h = *hp;
+    std::lock_guard<std::mutex> call_lock(h.call);
+    cudaFree(h.A);
+    cudaFree(h.B);
+    cudaFree(h.C);
+    h.A = h.B = h.C = nullptr;
+    h.a = h.b = h.c = 0;
+    if (h.in) {
+      cudaStreamDestroy(h.in);
+      cudaStreamDestroy(h.out);
+      for (auto& e : h.ev_in) cudaEventDestroy(e);
+      for (auto& e : h.ev_tile) cudaEventDestroy(e);
+      h.in = h.out = nullptr;
+    }
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
   for (auto it = g_ws.begin(); it != g_ws.end();) {
     if (it->first.first == dev) {
       cudaFree(it->second.first);
@@ -540,13 +597,6 @@ int ozk_release_cached(void) {
     } else {
       ++it;
     }
-  }
-  auto h = g_host.find(dev);
-  if (h != g_host.end()) {
-    cudaFree(h->second.A);
-    cudaFree(h->second.B);
-    cudaFree(h->second.C);
-    g_host.erase(h);
   }
   return OZK_OK;
 }

@@ -129,12 +129,14 @@ int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A,
                        ozk_event_t* events);
 
 /* C = A * B for HOST matrices (pinned memory gives the fastest copies and
- * the overlap).  B is copied first, then A in row blocks on a copy stream of
- * the library; each block's stages run on `stream` as soon as its rows have
- * arrived, and its rows of C go back on a second copy stream while the next
- * block computes.  Returns after C is complete in host memory.  Device
- * buffers, streams and events are cached per device; concurrent calls on one
- * device are serialised. */
+ * the overlap).  A goes to the device in row blocks and B in column blocks
+ * (four of each once M, resp. N, reaches 2048), interleaved on a copy
+ * stream of the library; each block is scanned and quantised on `stream` as
+ * soon as it has arrived, each tile of C as soon as its two blocks are in,
+ * and the tile goes back on a second copy stream while later blocks are
+ * still moving.  Returns after C is complete in host memory; C is the same,
+ * bit for bit, as ozk_dgemm's.  Device buffers, streams and events are
+ * cached per device; concurrent calls on one device are serialised. */
 int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                    const double* B, int64_t ldb, double* C, int64_t ldc,
                    int n_moduli, ozk_stream_t stream);

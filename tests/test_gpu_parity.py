@@ -400,13 +400,15 @@ def test_caller_workspace_and_host_buffers_agree():
     assert ozk.ozk_stream_status() == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(2100, 300, 700), (2048, 72, 8200)])
-def test_host_buffers_in_row_blocks(M, N, K):
-    """ozk_dgemm_host on row blocks (M >= 2048: four blocks of whole 256-row
-    tiles, copies overlapping the stages) with padded host leading
-    dimensions: equal to the device path bit for bit, and to the oracle on
-    sampled outputs (byte residues at K = 700, pair residues at K = 8200)."""
-    A, B = inputs(M, N, K, seed=M + K)
+@pytest.mark.parametrize("M,N,K", [(2100, 300, 700), (2100, 2300, 700), (3000, 2048, 300), (2048, 72, 8200)])
+def test_host_buffers_in_blocks(M, N, K):
+    """ozk_dgemm_host on row and column blocks (a dimension >= 2048 goes in
+    four blocks of whole 256-row or 256-column tiles, copies overlapping the
+    stages; ragged last blocks here) with padded host leading dimensions:
+    equal to the device path bit for bit, and to the oracle on sampled
+    outputs, block edges included (byte residues at K <= 700, pair residues
+    at K = 8200)."""
+    A, B = inputs(M, N, K, seed=M + N + K)
     hA = torch.zeros((M, K + 3), dtype=torch.float64).pin_memory()
     hB = torch.zeros((K, N + 5), dtype=torch.float64).pin_memory()
     hC = torch.full((M, N + 2), np.nan, dtype=torch.float64).pin_memory()
@@ -417,8 +419,11 @@ def test_host_buffers_in_row_blocks(M, N, K):
     assert same_bits(C, dgemm(A, B, 14))
     assert np.isnan(hC.numpy()[:, N:]).all()  # padding untouched
     rng = np.random.default_rng(M)
-    ii = np.concatenate([rng.integers(0, M, 200), [0, 767, 768, 1535, 1536, M - 1]])
-    jj = np.concatenate([rng.integers(0, N, 200), [0, N - 1, 0, N - 1, 0, N - 1]])
+    edges_i = [e for e in [0, 767, 768, 1535, 1536, 2303, 2304, M - 1] if e < M]
+    edges_j = [e for e in [0, 511, 512, 767, 768, 1023, 1024, 1535, 1536, 2303, N - 1] if e < N]
+    ei, ej = np.meshgrid(edges_i, edges_j, indexing="ij")
+    ii = np.concatenate([rng.integers(0, M, 200), ei.ravel()])
+    jj = np.concatenate([rng.integers(0, N, 200), ej.ravel()])
     assert same_bits(C[ii, jj], oracle.sample(A, B, 14, ii, jj)[0])
     assert ozk.ozk_stream_status() == 0
 
