@@ -142,7 +142,7 @@ struct HostBufs {
   size_t a = 0, b = 0, c = 0;
   cudaStream_t in = nullptr, out = nullptr;        // host-to-device and device-to-host copies
   cudaEvent_t ev_in[2 * kMaxHostBlocks] = {};                  // a block of A or B has arrived
-  cudaEvent_t ev_tile[kMaxHostBlocks * kMaxHostBlocks] = {};  // a tile of C is computed
+  cudaEvent_t ev_out[kMaxHostBlocks * kMaxHostBlocks] = {};    // a piece of C is computed
   std::mutex call;
 };
 std::map<int, HostBufs> g_host;
@@ -456,7 +456,7 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
       return OZK_ERR_CUDA;
     for (auto& e : h.ev_in)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
-    for (auto& e : h.ev_tile)
+    for (auto& e : h.ev_out)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
   }
   double *dA = h.A, *dB = h.B, *dC = h.C;
@@ -466,11 +466,10 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     // Copies in on h.in, the stages on the caller's stream, copies out on
     // h.out.  A moves in row blocks and B in column blocks, interleaved
     // (B_0, A_0, A_1, B_1, A_2, B_2, ...); each block is scanned and
-    // quantised as soon as it has arrived, and every tile of C whose row and
-    // column blocks are both in is computed next and sent back while later
-    // blocks are still on their way in.  Stage by stage each tile is
-    // run_dgemm on a block of rows and a block of columns, sharing the
-    // scales and slices of its blocks.
+    // quantised as soon as it has arrived, the part of C it completes is
+    // computed next and goes back while later blocks are still on their way
+    // in.  Stage by stage that part is run_dgemm on a rectangle of rows and
+    // columns, sharing the scales and slices of its blocks.
     const Layout L = layout_for(M, N, K, n_moduli);
     void* ws = nullptr;
     if ((rc = cached_workspace(st, L.total, &ws))) return rc;
@@ -509,41 +508,55 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
       }
       OZK_CUDA(cudaEventRecord(h.ev_in[k], h.in));
     }
-    bool have_a[kMaxHostBlocks] = {}, have_b[kMaxHostBlocks] = {};
+    // Blocks of each matrix arrive in order, so the blocks in form a prefix
+    // of the rows (or columns): the tiles a new block completes make one
+    // rectangle.  It is computed in pieces of up to `span` tiles, one GEMM
+    // and one CRT launch each: merged where a tile is little work (fewer
+    // launches), one tile at a time where it is much (each tile's copy back
+    // overlaps the next one's computation, which shortens the tail).
+    const double tile_work = static_cast<double>(rows) * static_cast<double>(cols) * static_cast<double>(K);
+    const int64_t span = std::max<int64_t>(1, static_cast<int64_t>(1.0e10 / tile_work));
+    int64_t rows_in = 0, cols_in = 0;
+    int piece = 0;
     for (int k = 0; k < no; ++k) {
       OZK_CUDA(cudaStreamWaitEvent(st, h.ev_in[k], 0));
       const bool is_a = order[k] > 0;
       const int blk = is_a ? order[k] - 1 : -order[k] - 1;
+      int64_t r0, mr, c0, nc;  // the rectangle of C this block completes
       if (is_a) {
-        const int64_t r0 = blk * rows, mr = std::min(rows, M - r0);
+        r0 = blk * rows;
+        mr = std::min(rows, M - r0);
         OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, st));
         OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
                                  as + r0 * L.kpad, L.a_plane, nullptr, 0, st));
-        have_a[blk] = true;
+        rows_in = r0 + mr;
+        c0 = 0;
+        nc = cols_in;
       } else {
-        const int64_t c0 = blk * cols, nc = std::min(cols, N - c0);
+        c0 = blk * cols;
+        nc = std::min(cols, N - c0);
         OZK_CUDA(launch_scale(0, nc, K, nullptr, 0, dB + c0, N, beta, nullptr, t + c0, amax + M + c0, st));
         OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, n_moduli, beta, nullptr,
                                  0, bs + c0 * L.kpad, L.b_plane, st));
-        have_b[blk] = true;
+        cols_in = c0 + nc;
+        r0 = 0;
+        mr = rows_in;
       }
-      // the tiles this block completes: its row (or column) against every
-      // column (or row) block already in
-      for (int o = 0; o < (is_a ? nbc : nbr); ++o) {
-        const int bi = is_a ? blk : o, bj = is_a ? o : blk;
-        if (!(is_a ? have_b[bj] : have_a[bi])) continue;
-        const int64_t r0 = bi * rows, mr = std::min(rows, M - r0);
-        const int64_t c0 = bj * cols, nc = std::min(cols, N - c0);
-        void* ob = out + static_cast<size_t>(r0 * L.ldo + c0) * esize;
-        OZK_CUDA(launch_residue_gemm(mr, nc, L.kpad, as + r0 * L.kpad, L.a_plane, bs + c0 * L.kpad, L.b_plane,
+      // pieces along the rectangle's long side (the blocks already in)
+      const int64_t step = is_a ? span * cols : span * rows;
+      for (int64_t p0 = 0; p0 < (is_a ? nc : mr); p0 += step) {
+        const int64_t pr0 = is_a ? r0 : p0, pmr = is_a ? mr : std::min(step, mr - p0);
+        const int64_t pc0 = is_a ? p0 : c0, pnc = is_a ? std::min(step, nc - p0) : nc;
+        void* ob = out + static_cast<size_t>(pr0 * L.ldo + pc0) * esize;
+        OZK_CUDA(launch_residue_gemm(pmr, pnc, L.kpad, as + pr0 * L.kpad, L.a_plane, bs + pc0 * L.kpad, L.b_plane,
                                      n_moduli, L.kind, ob, L.ldo, L.out_plane, L.splits, sms, st));
-        OZK_CUDA(launch_crt(mr, nc, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + r0, t + c0,
-                            dC + r0 * N + c0, N, nullptr, st));
-        cudaEvent_t done = h.ev_tile[bi * kMaxHostBlocks + bj];
+        OZK_CUDA(launch_crt(pmr, pnc, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + pr0, t + pc0,
+                            dC + pr0 * N + pc0, N, nullptr, st));
+        cudaEvent_t done = h.ev_out[piece++];
         OZK_CUDA(cudaEventRecord(done, st));
         OZK_CUDA(cudaStreamWaitEvent(h.out, done, 0));
-        OZK_CUDA(cudaMemcpy2DAsync(C + r0 * ldc + c0, sizeof(double) * ldc, dC + r0 * N + c0, sizeof(double) * N,
-                                   sizeof(double) * nc, mr, cudaMemcpyDeviceToHost, h.out));
+        OZK_CUDA(cudaMemcpy2DAsync(C + pr0 * ldc + pc0, sizeof(double) * ldc, dC + pr0 * N + pc0, sizeof(double) * N,
+                                   sizeof(double) * pnc, pmr, cudaMemcpyDeviceToHost, h.out));
       }
     }
     OZK_CUDA(cudaStreamSynchronize(h.out));
@@ -585,7 +598,7 @@ int ozk_release_cached(void) {
       cudaStreamDestroy(h.in);
       cudaStreamDestroy(h.out);
       for (auto& e : h.ev_in) cudaEventDestroy(e);
-      for (auto& e : h.ev_tile) cudaEventDestroy(e);
+      for (auto& e : h.ev_out) cudaEventDestroy(e);
       h.in = h.out = nullptr;
     }
   }

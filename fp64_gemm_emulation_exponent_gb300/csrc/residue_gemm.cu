@@ -41,6 +41,9 @@
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
+#include <map>
+#include <mutex>
+
 #include "ozk_internal.h"
 
 namespace ozk {
@@ -1008,6 +1011,64 @@ int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   return best;
 }
 
+namespace {
+
+// Cluster launch of the CTA-pair kernel: clusters of two CTAs.
+void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, size_t smem, cudaStream_t stream) {
+  cfg->blockDim = dim3(kThreads, 1, 1);
+  cfg->gridDim = dim3(2, 1, 1);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+// Once per device and kernel: the dynamic shared-memory opt-in, the check
+// that the compiled launch register count covers the setmaxnreg split
+// exactly (setmaxnreg.inc waits until the pool has the registers, so a
+// mismatch is refused rather than launched), and for the CTA-pair kernel the
+// number of co-resident clusters.  Cached so that a call issuing many
+// launches (the blocked host path) does not query the driver for each.
+cudaError_t kernel_setup(const void* kernel, size_t smem, bool pairs, int* resident) {
+  struct Setup {
+    cudaError_t err;
+    int resident;
+  };
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, Setup> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({dev, kernel});
+  if (it == done.end()) {
+    Setup su{cudaSuccess, 0};
+    cudaFuncAttributes fa;
+    if ((su.err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem))) == cudaSuccess &&
+        (su.err = cudaFuncGetAttributes(&fa, kernel)) == cudaSuccess) {
+      if (fa.numRegs != kLaunchRegs) {
+        su.err = cudaErrorInvalidKernelImage;
+      } else if (pairs) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        pair_launch_config(&cfg, attr, smem, nullptr);
+        su.err = cudaOccupancyMaxActiveClusters(&su.resident, kernel, &cfg);
+        if (su.err == cudaSuccess && su.resident < 1) su.err = cudaErrorInvalidConfiguration;
+      }
+    }
+    it = done.emplace(std::make_pair(dev, kernel), su).first;
+  }
+  *resident = it->second.resident;
+  return it->second.err;
+}
+
+}  // namespace
+
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
                                 int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
                                 int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
@@ -1042,35 +1103,19 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
                       : (long_chunks ? (po ? residue_gemm_kernel<true, true> : residue_gemm_kernel<true, false>)
                                      : (po ? residue_gemm_kernel<false, true> : residue_gemm_kernel<false, false>));
   const size_t smem = (pairs ? kPairSmemBytes : kSmemBytes) + kStashBytes;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int resident = 0;
+  cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kernel), smem, pairs, &resident);
   if (e != cudaSuccess) return e;
-  // setmaxnreg.inc waits until the pool has the registers: refuse to launch
-  // unless the compiled launch register count covers the split exactly.
-  cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   if (!pairs) {
     const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
     kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, prm);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  pair_launch_config(&cfg, attr, smem, stream);
   // persistent: one CTA pair per co-resident cluster slot, at most one per SM pair
   int64_t npairs = num_sms / 2;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);
-  int resident = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg)) != cudaSuccess) return e;
-  if (resident < 1) return cudaErrorInvalidConfiguration;
   if (resident < npairs) npairs = resident;
   if (units < npairs) npairs = units;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);  // clusters of two CTAs
