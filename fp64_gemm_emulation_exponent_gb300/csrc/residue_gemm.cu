@@ -419,13 +419,24 @@ struct Unit {
   int p, q, passes, sk, mt, nt, kb0, kb1;
 };
 
+// Within one modulus (and split) the tiles run in groups of kGroupM tile
+// rows, column by column: the units of one persistent wave then share a few
+// tile rows of A and a band of B columns, which stay in L2, instead of
+// sweeping every column tile of B (the whole slice, 134 MB per modulus at
+// N = K = 8192) once per couple of tile rows.
+constexpr int kGroupM = 8;
+
 template <bool PAIRS>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   Unit r;
-  r.nt = u % prm.tiles_n;
-  u /= prm.tiles_n;
-  r.mt = u % prm.tiles_m;
-  u /= prm.tiles_m;
+  const int tiles = prm.tiles_m * prm.tiles_n;
+  const int idx = u % tiles;
+  u /= tiles;
+  const int first = idx / (kGroupM * prm.tiles_n) * kGroupM;  // first tile row of the group
+  const int gm = min(prm.tiles_m - first, kGroupM);            // tile rows in the group
+  const int in = idx - first * prm.tiles_n;
+  r.mt = first + in % gm;
+  r.nt = in / gm;
   r.sk = u % prm.splits;
   r.q = u / prm.splits;
   if (PAIRS) {  // out_kind 2
