@@ -190,10 +190,12 @@ def test_dgemm_bit_exact_cta_pairs(M, N, K):
     assert same_bits(dgemm(A, B, 14), oracle.dgemm(A, B, 14))
 
 
-@pytest.mark.parametrize("M,N,K,n", [(5, 9, 2**17 + 3, 14), (3, 5, 2**20 + 7, 14), (17, 3, 300000, 20)])
+@pytest.mark.parametrize("M,N,K,n", [(5, 9, 2**17 + 3, 14), (3, 5, 2**20 + 7, 14), (17, 3, 300000, 20),
+                                     (2, 3, ozk.OZK_MAX_K, 14)])
 def test_dgemm_k_beyond_one_int32_sum(M, N, K, n):
     """K >= 2^17: the residue GEMM splits K into int32-exact shares (at most
-    OZK_SPLIT_MAX_K terms) and the combine reduces each share mod p."""
+    OZK_SPLIT_MAX_K terms) and the combine reduces each share mod p; up to the
+    largest K the library takes (OZK_MAX_K, 33 shares)."""
     A, B = inputs(M, N, K, seed=K % 1000)
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 

@@ -1,0 +1,80 @@
+"""The precision contract, reported: for every workload and moduli count the
+method is measured on, the error of the GPU result against a compensated
+(Dot2) CPU DGEMM, next to the moduli count and the bits per operand.
+
+The "Day 12" page (ithelp.ithome.com.tw), section "先定義公平比較", asks for
+every timing to come with its precision contract: target bits, modulus count
+and the errors (max abs, max rel, RMS).  Each test prints one table row
+(run with ``-s`` to see them) and asserts the tolerance that applies:
+eta <= 1e-14 from 14 moduli on, eta <= 2^-30 at 11, and at 8 moduli (whose
+beta of 23-26 bits cannot reach 2^-30) the a-priori bound of rounding the
+operands to integers.
+
+eta = max_ij |C_ij - R_ij| / (|A| |B|)_ij (normwise relative per output),
+max rel = max_ij |C_ij - R_ij| / |R_ij| over R_ij != 0, RMS = root mean square
+of C_ij - R_ij.  Workloads of up to 1024^3 multiply-adds are measured on every
+output, the larger ones on a seeded sample that includes tile corners.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp64_gemm_emulation_exponent_gb300 import ozk, workloads
+from gpu_helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+LABEL = {8: "~34-bit", 11: "~34-bit (2^-30 at n >= 11)", 14: "53-bit"}
+
+CASES = [(name, n) for name, w in workloads.WORKLOADS.items() for n in w.moduli]
+
+
+def outputs(w, count, seed):
+    if w.M * w.N * w.K <= 1024**3:
+        ii, jj = np.meshgrid(np.arange(w.M), np.arange(w.N), indexing="ij")
+        return ii.ravel(), jj.ravel()
+    rng = np.random.default_rng(seed)
+    ii = list(rng.integers(0, w.M, count))
+    jj = list(rng.integers(0, w.N, count))
+    for i in (0, 127, 128, 255, 256, w.M - 1):
+        for j in (0, 255, 256, w.N - 1):
+            ii.append(i)
+            jj.append(j)
+    return np.array(ii, dtype=np.int64), np.array(jj, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name,n", CASES)
+def test_precision_contract(name, n):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.workload_operands(w)
+    dA, dB = dev(A), dev(B)
+    C = ozk.dgemm(dA, dB, n)
+    torch.cuda.synchronize()
+    assert ozk.ozk_stream_status() == 0
+    ii, jj = outputs(w, 2048 if w.K <= 8192 else 512, seed=17 * n)
+    Cg = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().numpy()
+    del dA, dB, C
+    torch.cuda.empty_cache()
+    R, absAB = oracle.dot2_sample(A, B, ii, jj)
+    err = np.abs(Cg - R)
+    eta = float(np.max(err / absAB))
+    nz = R != 0
+    max_rel = float(np.max(err[nz] / np.abs(R[nz])))
+    rms = float(np.sqrt(np.mean(err**2)))
+    beta = ozk.ozk_beta(w.K, n)
+    if n >= 14:
+        assert eta <= 1e-14
+        verdict = "eta <= 1e-14"
+    elif n >= 11:
+        assert eta <= 2.0**-30
+        verdict = "eta <= 2^-30"
+    else:
+        s, t = oracle.scale(A, B, n)
+        s, t = s[ii].astype(np.int64), t[jj].astype(np.int64)
+        bound = (np.abs(A).sum(1)[ii] * np.ldexp(1.0, -t - 1) + np.ldexp(1.0, -s - 1) * np.abs(B).sum(0)[jj]
+                 + w.K * np.ldexp(1.0, -(s + t + 2)))
+        assert np.all(err <= bound * (1 + 1e-12) + np.spacing(np.abs(Cg)))
+        verdict = "a-priori bound"
+    print(f"\nPRECISION | {name} | {w.M}x{w.N}x{w.K} | {n} | {LABEL.get(n, '-')} | {beta} | {ii.size} | "
+          f"{float(err.max()):.3e} | {max_rel:.3e} | {rms:.3e} | {eta:.3e} | {verdict} |")
