@@ -112,7 +112,10 @@ int ozk_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
 /* As ozk_dgemm, with caller-provided device workspace of at least
  * ozk_workspace_size(M, N, K, n_moduli) bytes (256-byte aligned).  The
  * library allocates nothing.  Calls that share a workspace must be ordered
- * on one stream. */
+ * on one stream.  After one call of the same shape on the device (which
+ * sets up the kernels), a call only enqueues work on `stream`: it neither
+ * synchronises nor allocates, so it can be captured into a CUDA graph
+ * (worth it for small products, where launch latency is a large share). */
 int ozk_dgemm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                  const double* B, int64_t ldb, double* C, int64_t ldc,
                  int n_moduli, void* workspace, size_t workspace_bytes,

@@ -430,6 +430,36 @@ def test_host_buffers_in_blocks(M, N, K):
     assert ozk.ozk_stream_status() == 0
 
 
+def test_caller_workspace_call_captures_into_a_cuda_graph():
+    """ozk_dgemm_ws only enqueues work (no synchronisation, no allocation), so
+    a warmed-up call can be captured into a CUDA graph; replays reproduce it
+    bit for bit and follow new input values in the same buffers."""
+    M, N, K, n = 300, 260, 2100, 14
+    A, B = inputs(M, N, K, seed=77)
+    dA, dB = dev(A), dev(B)
+    C = torch.empty((M, N), dtype=torch.float64, device="cuda")
+    need = ozk.ozk_workspace_size(M, N, K, n)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        ozk.ozk_dgemm_ws(M, N, K, dA, K, dB, N, C, N, n, ws, need, stream=st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        ozk.ozk_dgemm_ws(M, N, K, dA, K, dB, N, C, N, n, ws, need, stream=st)
+    C.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert same_bits(C.cpu().numpy(), oracle.dgemm(A, B, n))
+    A2, B2 = inputs(M, N, K, seed=78, kind="special")
+    dA.copy_(torch.from_numpy(A2))
+    dB.copy_(torch.from_numpy(B2))
+    g.replay()
+    torch.cuda.synchronize()
+    assert same_bits(C.cpu().numpy(), oracle.dgemm(A2, B2, n))
+    assert ozk.ozk_stream_status() == 0
+
+
 def test_deterministic_and_stream_ordered():
     A, B = inputs(300, 700, 900, seed=4)
     dA, dB = dev(A), dev(B)
