@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -95,10 +96,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -270,7 +271,7 @@ def run_gpu(args, ranks: Ranks):
 
     events = [[ozk.Event() for _ in range(5)] for _ in range(args.steps)]
     t_start, t_stop = ozk.Event(), ozk.Event()
-    sampler = ClockSampler(ranks.local)
+    sampler = ClockSampler(ranks.local, args.clock_log)
     sampler.start()
     time.sleep(0.3)
     ranks.barrier()
@@ -370,6 +371,8 @@ def main():
                     help="GEMM shape to time (the headline line uses the default)")
     ap.add_argument("--moduli", type=int, default=N_MODULI)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--clock-log", default=tempfile.gettempdir(),
+                    help="folder for the nvidia-smi clock samples taken during the timed region")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     ranks = Ranks(world)

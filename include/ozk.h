@@ -167,8 +167,8 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
 /* The exponent scan of ozk_scale for callers that cannot give the library
  * device memory: a library embedded in an application whose allocator owns
  * all device memory, or a latency-critical loop that must not call
- * cudaMalloc (which may synchronise the device).  The paper has no
- * counterpart; it is the same scan with its (M + N) uint64 of scratch held
+ * cudaMalloc (which may synchronise the device).  The method's pages have
+ * no such entry point; it is the same scan with its (M + N) uint64 of scratch held
  * in a fixed 2 MiB array compiled into the library (each GPU that loads the
  * library keeps it until the process exits), so it allocates nothing.
  * Same arguments and results as ozk_scale without `scratch`.
