@@ -135,15 +135,27 @@ std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_ws;  // cache
 // events of the host path, and a lock held for a whole host call (one host
 // call per device at a time).
 constexpr int kMaxHostBlocks = 4;
-struct HostBufs {
+// Device copies of host operands for ozk_dgemm_host(_async).  Two slots, used
+// in turn, so that one call's inputs can move in while the previous call
+// computes; a slot is reused once the call that last used it has copied its
+// C out (`free`).
+constexpr int kHostSlots = 2;
+struct HostSlot {
   double* A = nullptr;
   double* B = nullptr;
   double* C = nullptr;
   size_t a = 0, b = 0, c = 0;
-  cudaStream_t in = nullptr, out = nullptr;        // host-to-device and device-to-host copies
+  cudaEvent_t free = nullptr;
+};
+struct HostBufs {
+  HostSlot slot[kHostSlots];
+  int next = 0;
+  cudaStream_t in = nullptr, out = nullptr;                     // host-to-device and device-to-host copies
+  cudaStream_t comp = nullptr;                                  // the stages of every call, in call order
+  cudaEvent_t computed = nullptr;                               // the last call's stages are done
   cudaEvent_t ev_in[2 * kMaxHostBlocks] = {};                  // a block of A or B has arrived
   cudaEvent_t ev_out[kMaxHostBlocks * kMaxHostBlocks] = {};    // a piece of C is computed
-  std::mutex call;
+  std::mutex call;                                             // enqueueing is serialised per device
 };
 std::map<int, HostBufs> g_host;
 
@@ -417,8 +429,9 @@ int ozk_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
                    reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
-int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
-                   int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+// Enqueues C = A B for host A, B, C (the work of ozk_dgemm_host_async).
+static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B, int64_t ldb,
+                 double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
   int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli);
   if (rc) return rc;
   if (M == 0 || N == 0) return OZK_OK;
@@ -434,10 +447,12 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
   }
   HostBufs& h = *hp;
   std::lock_guard<std::mutex> call_lock(h.call);
+  HostSlot& sl = h.slot[h.next];
+  h.next = (h.next + 1) % kHostSlots;
   auto grow = [&](double*& p, size_t& have, size_t need) -> bool {
     if (have >= need) return true;
     if (p) {
-      cudaDeviceSynchronize();
+      cudaDeviceSynchronize();  // a call in flight may still use the old buffer
       cudaFree(p);
     }
     p = nullptr;
@@ -446,33 +461,89 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     have = need;
     return true;
   };
-  if (!grow(h.A, h.a, sizeof(double) * static_cast<size_t>(M * K)) ||
-      !grow(h.B, h.b, sizeof(double) * static_cast<size_t>(K * N)) ||
-      !grow(h.C, h.c, sizeof(double) * static_cast<size_t>(M * N)))
+  if (!grow(sl.A, sl.a, sizeof(double) * static_cast<size_t>(M * K)) ||
+      !grow(sl.B, sl.b, sizeof(double) * static_cast<size_t>(K * N)) ||
+      !grow(sl.C, sl.c, sizeof(double) * static_cast<size_t>(M * N)))
     return OZK_ERR_WORKSPACE;
   if (!h.in) {
     if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
+        cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h.comp, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h.computed, cudaEventDisableTiming) != cudaSuccess)
       return OZK_ERR_CUDA;
     for (auto& e : h.ev_in)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
     for (auto& e : h.ev_out)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
+    for (auto& x : h.slot)
+      if (cudaEventCreateWithFlags(&x.free, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
   }
-  double *dA = h.A, *dB = h.B, *dC = h.C;
-  if (K == 0) {
-    OZK_CUDA(cudaMemset2DAsync(dC, sizeof(double) * N, 0, sizeof(double) * N, M, st));
-  } else {
-    // Copies in on h.in, the stages on the caller's stream, copies out on
-    // h.out.  A moves in row blocks and B in column blocks, interleaved
-    // (B_0, A_0, A_1, B_1, A_2, B_2, ...); each block is scanned and
-    // quantised as soon as it has arrived, the part of C it completes is
-    // computed next and goes back while later blocks are still on their way
-    // in.  Stage by stage that part is run_dgemm on a rectangle of rows and
-    // columns, sharing the scales and slices of its blocks.
+  double *dA = sl.A, *dB = sl.B, *dC = sl.C;
+  // Copies in on h.in, the stages on h.comp (every host-buffer call of the
+  // device in call order), copies out on h.out.  The call reads and writes
+  // only host memory and the library's own buffers, so nothing in it waits
+  // for the caller's stream: the copies in start at once, this slot's
+  // buffers only once the call that used them last has copied its C out (a
+  // never-recorded event does not hold a stream).  Is a previous call still
+  // computing?  Then this call's stages start after it, by which time its
+  // copies in are done.
+  const cudaError_t q = cudaEventQuery(h.computed);
+  if (q != cudaSuccess && q != cudaErrorNotReady) return OZK_ERR_CUDA;
+  if (q == cudaErrorNotReady) (void)cudaGetLastError();  // "not ready" is no error
+  const bool pipelined = q == cudaErrorNotReady;
+  OZK_CUDA(cudaStreamWaitEvent(h.in, sl.free, 0));
+  OZK_CUDA(cudaStreamWaitEvent(h.comp, sl.free, 0));
+  cudaStream_t cs = h.comp;
+  if (K > 0 && pipelined) {
+    // Behind another call: copy A and B in whole, run the stages on the
+    // whole product (the fastest schedule once the inputs are there), and
+    // combine and copy C out in row blocks, so that most of C is on its way
+    // back before the last block is combined.
     const Layout L = layout_for(M, N, K, n_moduli);
     void* ws = nullptr;
-    if ((rc = cached_workspace(st, L.total, &ws))) return rc;
+    if ((rc = cached_workspace(cs, L.total, &ws))) return rc;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
+    int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
+    int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
+    uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
+    uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
+    uint8_t* out = base + L.out;
+    const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
+    const int beta = beta_for(K, n_moduli);
+    OZK_CUDA(cudaMemcpy2DAsync(dA, sizeof(double) * K, A, sizeof(double) * lda, sizeof(double) * K, M,
+                               cudaMemcpyHostToDevice, h.in));
+    OZK_CUDA(cudaMemcpy2DAsync(dB, sizeof(double) * N, B, sizeof(double) * ldb, sizeof(double) * N, K,
+                               cudaMemcpyHostToDevice, h.in));
+    OZK_CUDA(cudaEventRecord(h.ev_in[0], h.in));
+    OZK_CUDA(cudaStreamWaitEvent(cs, h.ev_in[0], 0));
+    OZK_CUDA(launch_scale(M, N, K, dA, K, dB, N, beta, s, t, amax, cs));
+    OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, n_moduli, beta, as, L.a_plane, bs, L.b_plane, cs));
+    OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n_moduli, L.kind, out, L.ldo,
+                                 L.out_plane, L.splits, sms, cs));
+    const int64_t rows = M >= 2048 ? round_up((M + 7) / 8, 256) : M;  // at most 8 <= kMaxHostBlocks^2 pieces
+    int piece = 0;
+    for (int64_t r0 = 0; r0 < M; r0 += rows) {
+      const int64_t mr = std::min(rows, M - r0);
+      OZK_CUDA(launch_crt(mr, N, n_moduli, out + static_cast<size_t>(r0 * L.ldo) * esize, L.kind, L.ldo,
+                          L.out_plane, L.splits, s + r0, t, dC + r0 * N, N, nullptr, cs));
+      cudaEvent_t done = h.ev_out[piece++];
+      OZK_CUDA(cudaEventRecord(done, cs));
+      OZK_CUDA(cudaStreamWaitEvent(h.out, done, 0));
+      OZK_CUDA(cudaMemcpy2DAsync(C + r0 * ldc, sizeof(double) * ldc, dC + r0 * N, sizeof(double) * N,
+                                 sizeof(double) * N, mr, cudaMemcpyDeviceToHost, h.out));
+    }
+  } else if (K > 0) {
+    // Nothing ahead (the latency case): A moves in row blocks and B in
+    // column blocks, interleaved (B_0, A_0, A_1, B_1, A_2, B_2, ...); each
+    // block is scanned and quantised as soon as it has arrived, the part of
+    // C it completes is computed next and goes back while later blocks are
+    // still on their way in.  Stage by stage that part is run_dgemm on a
+    // rectangle of rows and columns, sharing the scales and slices of its
+    // blocks.
+    const Layout L = layout_for(M, N, K, n_moduli);
+    void* ws = nullptr;
+    if ((rc = cached_workspace(cs, L.total, &ws))) return rc;
     uint8_t* base = static_cast<uint8_t*>(ws);
     uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
     int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
@@ -519,25 +590,25 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
     int64_t rows_in = 0, cols_in = 0;
     int piece = 0;
     for (int k = 0; k < no; ++k) {
-      OZK_CUDA(cudaStreamWaitEvent(st, h.ev_in[k], 0));
+      OZK_CUDA(cudaStreamWaitEvent(cs, h.ev_in[k], 0));
       const bool is_a = order[k] > 0;
       const int blk = is_a ? order[k] - 1 : -order[k] - 1;
       int64_t r0, mr, c0, nc;  // the rectangle of C this block completes
       if (is_a) {
         r0 = blk * rows;
         mr = std::min(rows, M - r0);
-        OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, st));
+        OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, cs));
         OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
-                                 as + r0 * L.kpad, L.a_plane, nullptr, 0, st));
+                                 as + r0 * L.kpad, L.a_plane, nullptr, 0, cs));
         rows_in = r0 + mr;
         c0 = 0;
         nc = cols_in;
       } else {
         c0 = blk * cols;
         nc = std::min(cols, N - c0);
-        OZK_CUDA(launch_scale(0, nc, K, nullptr, 0, dB + c0, N, beta, nullptr, t + c0, amax + M + c0, st));
+        OZK_CUDA(launch_scale(0, nc, K, nullptr, 0, dB + c0, N, beta, nullptr, t + c0, amax + M + c0, cs));
         OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, n_moduli, beta, nullptr,
-                                 0, bs + c0 * L.kpad, L.b_plane, st));
+                                 0, bs + c0 * L.kpad, L.b_plane, cs));
         cols_in = c0 + nc;
         r0 = 0;
         mr = rows_in;
@@ -549,24 +620,40 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
         const int64_t pc0 = is_a ? p0 : c0, pnc = is_a ? std::min(step, nc - p0) : nc;
         void* ob = out + static_cast<size_t>(pr0 * L.ldo + pc0) * esize;
         OZK_CUDA(launch_residue_gemm(pmr, pnc, L.kpad, as + pr0 * L.kpad, L.a_plane, bs + pc0 * L.kpad, L.b_plane,
-                                     n_moduli, L.kind, ob, L.ldo, L.out_plane, L.splits, sms, st));
+                                     n_moduli, L.kind, ob, L.ldo, L.out_plane, L.splits, sms, cs));
         OZK_CUDA(launch_crt(pmr, pnc, n_moduli, ob, L.kind, L.ldo, L.out_plane, L.splits, s + pr0, t + pc0,
-                            dC + pr0 * N + pc0, N, nullptr, st));
+                            dC + pr0 * N + pc0, N, nullptr, cs));
         cudaEvent_t done = h.ev_out[piece++];
-        OZK_CUDA(cudaEventRecord(done, st));
+        OZK_CUDA(cudaEventRecord(done, cs));
         OZK_CUDA(cudaStreamWaitEvent(h.out, done, 0));
         OZK_CUDA(cudaMemcpy2DAsync(C + pr0 * ldc + pc0, sizeof(double) * ldc, dC + pr0 * N + pc0, sizeof(double) * N,
                                    sizeof(double) * pnc, pmr, cudaMemcpyDeviceToHost, h.out));
       }
     }
-    OZK_CUDA(cudaStreamSynchronize(h.out));
-    OZK_CUDA(cudaStreamSynchronize(st));
-    return OZK_OK;
+  } else {
+    OZK_CUDA(cudaMemset2DAsync(dC, sizeof(double) * N, 0, sizeof(double) * N, M, cs));
+    OZK_CUDA(cudaEventRecord(h.ev_out[0], cs));
+    OZK_CUDA(cudaStreamWaitEvent(h.out, h.ev_out[0], 0));
+    OZK_CUDA(cudaMemcpy2DAsync(C, sizeof(double) * ldc, dC, sizeof(double) * N, sizeof(double) * N, M,
+                               cudaMemcpyDeviceToHost, h.out));
   }
-  OZK_CUDA(cudaMemcpy2DAsync(C, sizeof(double) * ldc, dC, sizeof(double) * N, sizeof(double) * N, M,
-                             cudaMemcpyDeviceToHost, st));
-  OZK_CUDA(cudaStreamSynchronize(st));
+  OZK_CUDA(cudaEventRecord(h.computed, cs));
+  // the call is complete, in the caller's stream order, once C is in host memory
+  OZK_CUDA(cudaEventRecord(sl.free, h.out));
+  OZK_CUDA(cudaStreamWaitEvent(st, sl.free, 0));
   return OZK_OK;
+}
+
+int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                   int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+  const int rc = host_enqueue(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream);
+  if (rc) return rc;
+  return cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? OZK_OK : OZK_ERR_CUDA;
+}
+
+int ozk_dgemm_host_async(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                         int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+  return host_enqueue(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream);
 }
 
 int ozk_stream_status(ozk_stream_t stream) {
@@ -589,17 +676,22 @@ int ozk_release_cached(void) {
   if (hp) {  // the entry stays (a call may be waiting on its lock); what it holds goes
     HostBufs& h = *hp;
     std::lock_guard<std::mutex> call_lock(h.call);
-    cudaFree(h.A);
-    cudaFree(h.B);
-    cudaFree(h.C);
-    h.A = h.B = h.C = nullptr;
-    h.a = h.b = h.c = 0;
+    for (auto& sl : h.slot) {
+      cudaFree(sl.A);
+      cudaFree(sl.B);
+      cudaFree(sl.C);
+      sl.A = sl.B = sl.C = nullptr;
+      sl.a = sl.b = sl.c = 0;
+    }
     if (h.in) {
       cudaStreamDestroy(h.in);
       cudaStreamDestroy(h.out);
+      cudaStreamDestroy(h.comp);
+      cudaEventDestroy(h.computed);
       for (auto& e : h.ev_in) cudaEventDestroy(e);
       for (auto& e : h.ev_out) cudaEventDestroy(e);
-      h.in = h.out = nullptr;
+      for (auto& sl : h.slot) cudaEventDestroy(sl.free);
+      h.in = h.out = h.comp = nullptr;
     }
   }
   std::lock_guard<std::mutex> lock(g_mutex);

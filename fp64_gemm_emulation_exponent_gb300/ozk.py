@@ -42,6 +42,7 @@ SIGNATURES = {
     "ozk_dgemm_ws": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp]),
     "ozk_dgemm_ws_timed": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp, _vp]),
     "ozk_dgemm_host": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
+    "ozk_dgemm_host_async": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_stream_status": (_i32, [_vp]),
     "ozk_release_cached": (_i32, []),
     "ozk_scale": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
@@ -159,6 +160,12 @@ def ozk_dgemm_ws_timed(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, wor
 def ozk_dgemm_host(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream=None):
     """Host (CPU, ideally pinned) float64 tensors in and out; synchronous."""
     return _call("ozk_dgemm_host", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli, _stream(stream))
+
+
+def ozk_dgemm_host_async(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream=None):
+    """Host (pinned) float64 tensors; returns once enqueued, C is complete when the stream gets there."""
+    return _call("ozk_dgemm_host_async", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli,
+                 _stream(stream))
 
 
 def ozk_stream_status(stream=None):

@@ -144,6 +144,32 @@ int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
                    const double* B, int64_t ldb, double* C, int64_t ldc,
                    int n_moduli, ozk_stream_t stream);
 
+/* ozk_dgemm_host without the wait: returns once the copies and stages are
+ * enqueued.  The call is complete, in `stream`'s order, when C is in host
+ * memory: synchronise `stream` (or an event recorded on it after the call)
+ * before reading C, and keep A and B unchanged and C untouched until then.
+ * Only the completion is ordered on `stream`: the call touches no device
+ * memory of the caller, and its copies of A and B start at once, so A and B
+ * must hold their values when the call is made (device work that writes
+ * them must have finished).
+ * The library keeps two sets of device buffers per device and uses them in
+ * turn, so the next call's A and B move in while this call computes; a
+ * third call's copies wait on the device (not on the host) until the first
+ * call's C has been copied out.  The stages of all host-buffer calls of a
+ * device run in call order on a stream of the library: a call made while
+ * an earlier one is still
+ * computing copies A and B in whole and runs the stages on the whole
+ * product (its inputs are in by the time it starts), then combines and
+ * copies C out in row blocks; a call with nothing ahead of it uses the
+ * blocked schedule of ozk_dgemm_host.  Calls made on one stream complete in order;
+ * concurrent calls on one device are serialised while they enqueue.  Host
+ * memory should be pinned: with pageable memory the copies (and so the
+ * call) are synchronous.  Same arguments, results and errors as
+ * ozk_dgemm_host; device faults are reported by ozk_stream_status. */
+int ozk_dgemm_host_async(int64_t M, int64_t N, int64_t K, const double* A,
+                         int64_t lda, const double* B, int64_t ldb, double* C,
+                         int64_t ldc, int n_moduli, ozk_stream_t stream);
+
 /* Synchronises the stream, then reports and clears a fault latched by a
  * kernel (OZK_ERR_TIMEOUT), or OZK_ERR_CUDA if the stream reported an error. */
 int ozk_stream_status(ozk_stream_t stream);

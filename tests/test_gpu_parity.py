@@ -430,6 +430,27 @@ def test_host_buffers_in_blocks(M, N, K):
     assert ozk.ozk_stream_status() == 0
 
 
+def test_host_async_calls_in_flight():
+    """Four ozk_dgemm_host_async calls in flight on one stream, more than the
+    library's two sets of device buffers, each with its own host operands and
+    output (the last of another shape): after one synchronisation every C
+    equals the device path bit for bit."""
+    shapes = [(2100, 2300, 700), (2100, 2300, 700), (2100, 2300, 700), (300, 260, 2100)]
+    st = torch.cuda.Stream()
+    calls = []
+    for idx, (M, N, K) in enumerate(shapes):
+        A, B = inputs(M, N, K, seed=200 + idx)
+        hA = torch.from_numpy(A).pin_memory()
+        hB = torch.from_numpy(B).pin_memory()
+        hC = torch.full((M, N), np.nan, dtype=torch.float64).pin_memory()
+        ozk.ozk_dgemm_host_async(M, N, K, hA, K, hB, N, hC, N, 14, stream=st)
+        calls.append((A, B, hA, hB, hC))
+    st.synchronize()
+    assert ozk.ozk_stream_status(st) == 0
+    for A, B, _, _, hC in calls:
+        assert same_bits(hC.numpy(), dgemm(A, B, 14))
+
+
 def test_caller_workspace_call_captures_into_a_cuda_graph():
     """ozk_dgemm_ws only enqueues work (no synchronisation, no allocation), so
     a warmed-up call can be captured into a CUDA graph; replays reproduce it
