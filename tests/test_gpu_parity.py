@@ -451,6 +451,44 @@ def test_host_async_calls_in_flight():
         assert same_bits(hC.numpy(), dgemm(A, B, 14))
 
 
+def test_host_async_from_two_threads():
+    """Two host threads, each with its own stream, enqueue three
+    ozk_dgemm_host_async calls apiece (the library serialises the enqueueing
+    and shares its two buffer sets among them): every C is right."""
+    import threading
+
+    results, errors = {}, []
+
+    def worker(tid):
+        try:
+            st = torch.cuda.Stream()
+            mine = []
+            for c in range(3):
+                M, N, K = 640 + 64 * tid, 2100, 300 + 100 * c
+                A, B = inputs(M, N, K, seed=1000 * tid + c)
+                hA = torch.from_numpy(A).pin_memory()
+                hB = torch.from_numpy(B).pin_memory()
+                hC = torch.full((M, N), np.nan, dtype=torch.float64).pin_memory()
+                ozk.ozk_dgemm_host_async(M, N, K, hA, K, hB, N, hC, N, 14, stream=st)
+                mine.append((A, B, hA, hB, hC))
+            st.synchronize()
+            results[tid] = (mine, ozk.ozk_stream_status(st))
+        except Exception as e:  # reported in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(tid,)) for tid in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors
+    for tid in range(2):
+        mine, status = results[tid]
+        assert status == 0
+        for A, B, _, _, hC in mine:
+            assert same_bits(hC.numpy(), dgemm(A, B, 14))
+
+
 def test_caller_workspace_call_captures_into_a_cuda_graph():
     """ozk_dgemm_ws only enqueues work (no synchronisation, no allocation), so
     a warmed-up call can be captured into a CUDA graph; replays reproduce it
