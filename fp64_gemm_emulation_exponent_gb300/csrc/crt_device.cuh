@@ -385,15 +385,17 @@ __global__ void __launch_bounds__(256, NFIX ? 3 : 1) crt_kernel(const void* __re
             wb = gg == x ? cw[2 * j + 1][x] : wb;
           }
         }
+        const uint32_t pu01 = K.pu[j][0] | (K.pu[j][1] << 16);  // both below 2^16
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
           uint32_t r;
           if constexpr (IN_KIND == 2) {
             r = ((o < 2 ? wa : wb) >> (16 * (o & 1))) & 0xFFFFu;
           } else {
-            const uint32_t ca = __byte_perm(wa, 0u, 0x4440 + o);
-            const uint32_t cb = __byte_perm(wb, 0u, 0x4440 + o);
-            const uint32_t t = ca * K.pu[j][0] + cb * K.pu[j][1];  // < 2^25
+            // bytes o of the two moduli's words side by side, then
+            // c_2j u_j0 + c_2j+1 u_j1 (< 2^25) in one two-way dot product
+            const uint32_t cacb = __byte_perm(wa, wb, o | ((4 + o) << 4));
+            const uint32_t t = __dp2a_lo(pu01, cacb, 0u);
             r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
           }
           qacc[o] += static_cast<uint64_t>(r) * K.pfrac[j];
