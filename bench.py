@@ -37,7 +37,20 @@ METRIC = "emulated-DGEMM effective FP64 TFLOP/s at 4096^3 (53-bit) and % INT8 te
 WORKLOAD = "square4096_normal"
 N_MODULI = 14
 STAGES = ["scan", "quantize", "residue_gemm", "crt_combine"]
-KERNELS_PER_STEP = 5  # scan, finalize_scales, quantize, residue_gemm, crt
+
+
+def rows_fused(M: int, kpad: int) -> bool:
+    """Whether ozk_dgemm scans the rows of A inside their quantisation (the
+    library's rule: a row fits one block, kpad <= 4096, and M * kpad >= 2^22)."""
+    return kpad <= 4096 and M * kpad >= 1 << 22
+
+
+def kernels_per_step(M: int, kpad: int) -> int:
+    """Our kernels per ozk_dgemm call: scan, finalize_scales, quantize, residue_gemm,
+    crt, and the fused scan-and-quantize of A's rows when that is used."""
+    return 6 if rows_fused(M, kpad) else 5
+
+
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "residue_gemm_traffic.json")
 
 
@@ -346,8 +359,11 @@ def run_gpu(args, ranks: Ranks):
         "algorithmic": f"2*M*N*K*n = {algo_flops:.4g} flop per launch",
     }
     hbm = pk["hbm_gbs"]
+    # with the fused row kernel A is read once, in the quantize stage, and the
+    # scan stage reads B alone
+    fused = rows_fused(M, ozk.ozk_kpad(K))
     mem_stages = {
-        "scan": 8.0 * (M * K + K * N),
+        "scan": 8.0 * (K * N if fused else M * K + K * N),
         "quantize": 8.0 * (M * K + K * N) + 2.0 * n * (M + N) * ozk.ozk_kpad(K),
         "crt_combine": (n + 8.0) * M * N,
     }
@@ -374,7 +390,7 @@ def run_gpu(args, ranks: Ranks):
             "e2e_pipelined": {"value": pipe_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 8 * (M * K + K * N),
                               "d2h_bytes_per_step": 8 * M * N, "steps": e2e_steps, "matches_device_result": ok_pipe,
                               "mode": "ozk_dgemm_host_async, calls back to back on one stream, one final sync"},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": kernels_per_step(M, ozk.ozk_kpad(K)) * args.steps,
             "clocks": clocks,
             "context": {"pages_rtx4060_laptop_4096_custom_partial_crt_ms": 123.54,
                         "pages_rtx4060_laptop_4096_native_dgemm_ms": 669.75},

@@ -290,6 +290,13 @@ int record(ozk_event_t* ev, int idx, cudaStream_t stream) {
     if ((expr) != cudaSuccess) return OZK_ERR_CUDA; \
   } while (0)
 
+// Scan the rows of A inside their quantisation (one block per row, A read
+// once) when a row fits one block and there are enough rows to fill the GPU;
+// small products keep the separate scan, which spreads rows over more threads.
+bool fuse_rows(int64_t M, int64_t kpad) {
+  return quantize_rows_fits(kpad) && M <= 0x7FFFFFFF && M * kpad >= (int64_t{1} << 22);
+}
+
 int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
               int64_t ldb, double* C, int64_t ldc, int n, void* ws, size_t ws_bytes,
               cudaStream_t stream, ozk_event_t* ev) {
@@ -314,10 +321,20 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   const int beta = beta_for(K, n);
 
   if ((rc = record(ev, 0, stream))) return rc;
-  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
-  if ((rc = record(ev, 1, stream))) return rc;
-  OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, L.a_plane, bs,
-                           L.b_plane, stream));
+  if (fuse_rows(M, L.kpad)) {
+    // K up to 4096: each row of A is scanned inside its own quantisation
+    // (read once); only B's columns need the separate scan
+    OZK_CUDA(launch_scale(0, N, K, nullptr, 0, B, ldb, beta, nullptr, t, amax + M, stream));
+    if ((rc = record(ev, 1, stream))) return rc;
+    OZK_CUDA(launch_quantize_rows(M, K, L.kpad, A, lda, n, beta, s, as, L.a_plane, stream));
+    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, B, ldb, nullptr, t, n, beta, nullptr, 0, bs,
+                             L.b_plane, stream));
+  } else {
+    OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
+    if ((rc = record(ev, 1, stream))) return rc;
+    OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, L.a_plane, bs,
+                             L.b_plane, stream));
+  }
   if ((rc = record(ev, 2, stream))) return rc;
   OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n, L.kind, out, L.ldo, L.out_plane,
                                L.splits, sms, stream));
@@ -517,8 +534,16 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
                                cudaMemcpyHostToDevice, h.in));
     OZK_CUDA(cudaEventRecord(h.ev_in[0], h.in));
     OZK_CUDA(cudaStreamWaitEvent(cs, h.ev_in[0], 0));
-    OZK_CUDA(launch_scale(M, N, K, dA, K, dB, N, beta, s, t, amax, cs));
-    OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, n_moduli, beta, as, L.a_plane, bs, L.b_plane, cs));
+    if (fuse_rows(M, L.kpad)) {
+      OZK_CUDA(launch_scale(0, N, K, nullptr, 0, dB, N, beta, nullptr, t, amax + M, cs));
+      OZK_CUDA(launch_quantize_rows(M, K, L.kpad, dA, K, n_moduli, beta, s, as, L.a_plane, cs));
+      OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, n_moduli, beta, nullptr, 0, bs,
+                               L.b_plane, cs));
+    } else {
+      OZK_CUDA(launch_scale(M, N, K, dA, K, dB, N, beta, s, t, amax, cs));
+      OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, n_moduli, beta, as, L.a_plane, bs,
+                               L.b_plane, cs));
+    }
     OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n_moduli, L.kind, out, L.ldo,
                                  L.out_plane, L.splits, sms, cs));
     const int64_t rows = M >= 2048 ? round_up((M + 7) / 8, 256) : M;  // at most 8 <= kMaxHostBlocks^2 pieces
@@ -597,9 +622,14 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
       if (is_a) {
         r0 = blk * rows;
         mr = std::min(rows, M - r0);
-        OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, cs));
-        OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
-                                 as + r0 * L.kpad, L.a_plane, nullptr, 0, cs));
+        if (fuse_rows(mr, L.kpad)) {
+          OZK_CUDA(launch_quantize_rows(mr, K, L.kpad, dA + r0 * K, K, n_moduli, beta, s + r0,
+                                        as + r0 * L.kpad, L.a_plane, cs));
+        } else {
+          OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, cs));
+          OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
+                                   as + r0 * L.kpad, L.a_plane, nullptr, 0, cs));
+        }
         rows_in = r0 + mr;
         c0 = 0;
         nc = cols_in;

@@ -98,6 +98,13 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
                             int64_t lda, const double* B, int64_t ldb, const int32_t* s,
                             const int32_t* t, int n, int beta, uint16_t* a_out, int64_t a_plane,
                             uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
+// Rows of A scanned and quantised in one pass (one block per row): writes
+// s[0..M) and A's slices as launch_scale + launch_quantize would.  Only for
+// K up to 4096 (quantize_rows_fits(kpad)); cudaErrorInvalidValue beyond.
+bool quantize_rows_fits(int64_t kpad);
+cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const double* A, int64_t lda, int n,
+                                 int beta, int32_t* s, uint16_t* a_out, int64_t a_plane,
+                                 cudaStream_t stream);
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
                                 int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
                                 int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,

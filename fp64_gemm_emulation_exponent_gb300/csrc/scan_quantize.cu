@@ -130,23 +130,21 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
 }
 
 // s = beta - E with max|x| = f 2^E, f in [0.5, 1) (frexp's exponent, read off
-// the bits; subnormals via the leading-zero count).
+// the bits of the maximum b; subnormals via the leading-zero count).
+__device__ __forceinline__ int32_t scale_of_max(uint64_t b, int beta) {
+  if (b >= kInfBits) return OZK_SCALE_NONFINITE;
+  if (b == 0) return 0;
+  const int ex = static_cast<int>(b >> 52);
+  const int E = ex ? ex - 1022 : (63 - __clzll(static_cast<long long>(b))) - 1073;
+  return beta - E;
+}
+
 __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_t M, int64_t N,
                                        int beta, int32_t* __restrict__ s,
                                        int32_t* __restrict__ t) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= M + N) return;
-  const uint64_t b = amax[idx];
-  int32_t r;
-  if (b >= kInfBits) {
-    r = OZK_SCALE_NONFINITE;
-  } else if (b == 0) {
-    r = 0;
-  } else {
-    const int ex = static_cast<int>(b >> 52);
-    const int E = ex ? ex - 1022 : (63 - __clzll(static_cast<long long>(b))) - 1073;
-    r = beta - E;
-  }
+  const int32_t r = scale_of_max(amax[idx], beta);
   if (idx < M)
     s[idx] = r;
   else
@@ -361,6 +359,70 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
   });
 }
 
+// Rows of A with the exponent scan fused in: one block per row (K up to
+// kRowsMaxK), kQK consecutive entries per thread.  The row's max |a| is
+// reduced in the block and turned into its scale while the entries are
+// still in registers, so A is read once instead of twice; the quantisation
+// itself is quantize_kernel's.
+constexpr int kRowsMaxThreads = 256;
+static_assert(kRowsMaxThreads % 32 == 0 && kRowsMaxThreads <= 1024, "whole warps");
+
+template <int NL>
+__global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const QuantParams qp, int beta,
+                                                                        int32_t* __restrict__ s_out) {
+  __shared__ uint64_t wmax[kRowsMaxThreads / 32];
+  const int64_t row = blockIdx.x;
+  const int64_t k0 = static_cast<int64_t>(threadIdx.x) * kQK;
+  const bool active = k0 < qp.kpad;  // the block is rounded up to whole warps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t v[kQK];
+  const double* a = qp.A + row * qp.lda + k0;
+  if (active && qp.a_vec && k0 + kQK <= qp.K) {
+#pragma unroll
+    for (int e = 0; e < kQK / 4; ++e) {
+      uint64_t w[4];
+      load4_u64(a + 4 * e, w);
+      v[4 * e] = w[0];
+      v[4 * e + 1] = w[1];
+      v[4 * e + 2] = w[2];
+      v[4 * e + 3] = w[3];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kQK; ++e) v[e] = (active && k0 + e < qp.K) ? load1_u64(a + e) : 0ull;
+  }
+  uint64_t m = 0;
+#pragma unroll
+  for (int e = 0; e < kQK; ++e) m = umax64(m, v[e] & kAbsMask);
+  m = warp_max_u64(m);
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  m = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = umax64(m, wmax[w]);
+  const int32_t sc = scale_of_max(m, beta);
+  if (threadIdx.x == 0) s_out[row] = sc;
+  if (!active) return;
+  if (sc == OZK_SCALE_NONFINITE) {
+#pragma unroll
+    for (int e = 0; e < kQK; ++e) v[e] = 0;
+  }
+  uint32_t x[kQK][NL];
+#pragma unroll
+  for (int e = 0; e < kQK; ++e) scale_round<NL>(v[e], sc, x[e]);
+  uint16_t* dst = qp.a_out + row * qp.kpad + k0;
+  const int n = qp.n;
+  static_for<0, kMaxModuli>([&](auto kc) {
+    constexpr int k = decltype(kc)::value;
+    if (k < n) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        w[e] = pack_f16x2<k>(shifted_residue<k, NL>(x[2 * e]), shifted_residue<k, NL>(x[2 * e + 1]));
+      store8_u32(dst + k * qp.a_plane, w);
+    }
+  });
+}
+
 }  // namespace
 
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
@@ -451,6 +513,34 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
     quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
   else
     quantize_kernel<4><<<blocks, kQThreads, 0, stream>>>(qp);
+  return cudaGetLastError();
+}
+
+bool quantize_rows_fits(int64_t kpad) { return kpad / kQK <= kRowsMaxThreads; }
+
+cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const double* A, int64_t lda, int n,
+                                 int beta, int32_t* s, uint16_t* a_out, int64_t a_plane,
+                                 cudaStream_t stream) {
+  if (M == 0 || kpad == 0) return cudaSuccess;
+  if (!quantize_rows_fits(kpad) || M > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  QuantParams qp = {};
+  qp.A = A;
+  qp.a_out = a_out;
+  qp.a_plane = a_plane;
+  qp.lda = lda;
+  qp.M = M;
+  qp.K = K;
+  qp.kpad = kpad;
+  qp.n = n;
+  qp.a_vec = (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
+  const unsigned threads = static_cast<unsigned>((kpad / kQK + 31) / 32 * 32);
+  const unsigned blocks = static_cast<unsigned>(M);
+  if (beta <= 62)
+    quantize_rows_kernel<2><<<blocks, threads, 0, stream>>>(qp, beta, s);
+  else if (beta <= 64)
+    quantize_rows_kernel<3><<<blocks, threads, 0, stream>>>(qp, beta, s);
+  else
+    quantize_rows_kernel<4><<<blocks, threads, 0, stream>>>(qp, beta, s);
   return cudaGetLastError();
 }
 

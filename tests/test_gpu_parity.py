@@ -182,6 +182,22 @@ def test_dgemm_bit_exact_pair_residue_path(M, N, K, n):
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
 
+@pytest.mark.parametrize("M,N,K,n", [(2048, 96, 2000, 14), (1024, 64, 4033, 14), (2048, 40, 2100, 18),
+                                     (4096, 40, 1030, 20)])
+def test_dgemm_bit_exact_fused_row_scan(M, N, K, n):
+    """Enough rows of at most 4096 entries: each row of A is scanned inside its
+    own quantisation (one block per row).  Special rows (zero, subnormal,
+    2^900, wide range, Inf, NaN) and ragged K against the oracle, all outputs,
+    for each integer width (beta 48: one 64-bit word; 63: three limbs; 71:
+    four)."""
+    A, B = inputs(M, N, K, seed=M + N + K, kind="special")
+    A[5, K // 3] = np.inf
+    A[9, K - 1] = np.nan
+    C = dgemm(A, B, n)
+    assert same_bits(C, oracle.dgemm(A, B, n))
+    assert np.isnan(C[5]).all() and np.isnan(C[9]).all()
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 2100), (1, 700, 4096), (300, 1, 2049), (257, 520, 6000)])
 def test_dgemm_bit_exact_cta_pairs(M, N, K):
     """K of 2048 or more runs the residue GEMM on CTA pairs (256-row tiles,
