@@ -137,14 +137,16 @@ std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_ws;  // cache
 constexpr int kMaxHostBlocks = 4;
 // Device copies of host operands for ozk_dgemm_host(_async).  Two slots, used
 // in turn, so that one call's inputs can move in while the previous call
-// computes; a slot is reused once the call that last used it has copied its
-// C out (`free`).
+// computes.  A slot's A and B take new inputs once the stages of the call
+// that used them last are done (`computed`); its C takes a new result once
+// that call has copied C out (`free`).
 constexpr int kHostSlots = 2;
 struct HostSlot {
   double* A = nullptr;
   double* B = nullptr;
   double* C = nullptr;
   size_t a = 0, b = 0, c = 0;
+  cudaEvent_t computed = nullptr;
   cudaEvent_t free = nullptr;
 };
 struct HostBufs {
@@ -493,22 +495,24 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
     for (auto& e : h.ev_out)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
     for (auto& x : h.slot)
-      if (cudaEventCreateWithFlags(&x.free, cudaEventDisableTiming) != cudaSuccess) return OZK_ERR_CUDA;
+      if (cudaEventCreateWithFlags(&x.free, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&x.computed, cudaEventDisableTiming) != cudaSuccess)
+        return OZK_ERR_CUDA;
   }
   double *dA = sl.A, *dB = sl.B, *dC = sl.C;
   // Copies in on h.in, the stages on h.comp (every host-buffer call of the
   // device in call order), copies out on h.out.  The call reads and writes
   // only host memory and the library's own buffers, so nothing in it waits
-  // for the caller's stream: the copies in start at once, this slot's
-  // buffers only once the call that used them last has copied its C out (a
-  // never-recorded event does not hold a stream).  Is a previous call still
-  // computing?  Then this call's stages start after it, by which time its
-  // copies in are done.
+  // for the caller's stream: the copies in start once the stages of the
+  // call that used this slot last are done, the stages once that call has
+  // copied its C out (a never-recorded event does not hold a stream).  Is a
+  // previous call still computing?  Then this call's stages start after it,
+  // by which time its copies in are done.
   const cudaError_t q = cudaEventQuery(h.computed);
   if (q != cudaSuccess && q != cudaErrorNotReady) return OZK_ERR_CUDA;
   if (q == cudaErrorNotReady) (void)cudaGetLastError();  // "not ready" is no error
   const bool pipelined = q == cudaErrorNotReady;
-  OZK_CUDA(cudaStreamWaitEvent(h.in, sl.free, 0));
+  OZK_CUDA(cudaStreamWaitEvent(h.in, sl.computed, 0));
   OZK_CUDA(cudaStreamWaitEvent(h.comp, sl.free, 0));
   cudaStream_t cs = h.comp;
   if (K > 0 && pipelined) {
@@ -668,6 +672,7 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
                                cudaMemcpyDeviceToHost, h.out));
   }
   OZK_CUDA(cudaEventRecord(h.computed, cs));
+  OZK_CUDA(cudaEventRecord(sl.computed, cs));
   // the call is complete, in the caller's stream order, once C is in host memory
   OZK_CUDA(cudaEventRecord(sl.free, h.out));
   OZK_CUDA(cudaStreamWaitEvent(st, sl.free, 0));
@@ -720,7 +725,10 @@ int ozk_release_cached(void) {
       cudaEventDestroy(h.computed);
       for (auto& e : h.ev_in) cudaEventDestroy(e);
       for (auto& e : h.ev_out) cudaEventDestroy(e);
-      for (auto& sl : h.slot) cudaEventDestroy(sl.free);
+      for (auto& sl : h.slot) {
+        cudaEventDestroy(sl.free);
+        cudaEventDestroy(sl.computed);
+      }
       h.in = h.out = h.comp = nullptr;
     }
   }
