@@ -287,16 +287,21 @@ struct QuantParams {
   int64_t a_plane, b_plane;
   int64_t lda, ldb, M, N, K, kpad;
   int64_t groups;     // kpad / 16
-  int64_t a_threads;  // M * groups; B threads follow
-  int64_t b_threads;  // N * groups
+  int64_t a_threads;  // M * groups
+  int64_t a_span;     // a_threads rounded up to whole blocks; B threads follow
+  int64_t b_threads;  // cgroups * ceil(groups / warps per block) blocks of threads
+  int64_t cgroups;    // groups of 32 columns of B
   int n;
   int a_vec;  // rows of A are 32-byte aligned
 };
 
 // One thread: 16 consecutive K entries of one row of A (thread order: k fastest,
-// so loads and stores of a warp are contiguous) or of one column of B (thread
-// order: columns fastest, so each of the 16 row loads of a warp is contiguous).
-// Each writes one 32-byte run of every modulus' slice.
+// so loads and stores of a warp are contiguous) or of one column of B.  For B
+// a block is 32 columns (the lanes) x 4 consecutive 16-entry K groups (the
+// warps): each of a warp's 16 row loads is 256 contiguous bytes, and the
+// block writes each column's slice 128 contiguous bytes (a whole L2 line)
+// per modulus at once; consecutive blocks take the next 32 columns of the
+// same 64 rows.  Each thread writes one 32-byte run of every modulus' slice.
 template <int NL>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams qp) {
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
@@ -304,7 +309,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
   int64_t row, k0, plane;
   int32_t sc;
   uint16_t* out;
-  if (g < qp.a_threads) {
+  if (g < qp.a_span) {
+    if (g >= qp.a_threads) return;
     row = g / qp.groups;
     k0 = (g - row * qp.groups) * kQK;
     plane = qp.a_plane;
@@ -326,10 +332,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
       for (int e = 0; e < kQK; ++e) v[e] = (k0 + e < qp.K) ? load1_u64(a + e) : 0ull;
     }
   } else {
-    const int64_t gb = g - qp.a_threads;
+    const int64_t gb = g - qp.a_span;
     if (gb >= qp.b_threads) return;
-    const int64_t kg = gb / qp.N;
-    row = gb - kg * qp.N;  // column j of B
+    constexpr int kWarps = kQThreads / 32;
+    const int64_t blk = gb / kQThreads;
+    const int64_t cg = blk % qp.cgroups;
+    const int64_t kg = (blk / qp.cgroups) * kWarps + ((gb % kQThreads) >> 5);
+    row = cg * 32 + (gb & 31);  // column j of B
+    if (row >= qp.N || kg >= qp.groups) return;
     k0 = kg * kQK;
     plane = qp.b_plane;
     out = qp.b_out;
@@ -499,10 +509,12 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   qp.kpad = kpad;
   qp.groups = kpad / kQK;
   qp.a_threads = qp.M * qp.groups;
-  qp.b_threads = qp.N * qp.groups;
+  qp.a_span = (qp.a_threads + kQThreads - 1) / kQThreads * kQThreads;
+  qp.cgroups = (qp.N + 31) / 32;
+  qp.b_threads = qp.cgroups * ((qp.groups + kQThreads / 32 - 1) / (kQThreads / 32)) * kQThreads;
   qp.n = n;
   qp.a_vec = A && (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
-  const int64_t threads = qp.a_threads + qp.b_threads;
+  const int64_t threads = qp.a_span + qp.b_threads;
   if (threads == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((threads + kQThreads - 1) / kQThreads);
   // |a'| <= 2^beta: one 64-bit word for beta <= 62, three 22-bit limbs of
