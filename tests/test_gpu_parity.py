@@ -505,6 +505,32 @@ def test_host_async_from_two_threads():
             assert same_bits(hC.numpy(), dgemm(A, B, 14))
 
 
+def test_release_cached_and_reuse():
+    """ozk_release_cached frees the cached workspaces, the host-path buffers,
+    streams and events; the next calls set them up again and agree with the
+    results from before the release bit for bit."""
+    M, N, K = 2100, 300, 700
+    A, B = inputs(M, N, K, seed=501)
+    before = dgemm(A, B, 14)
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float64).pin_memory()
+    ozk.ozk_dgemm_host(M, N, K, hA, K, hB, N, hC, N, 14)
+    assert same_bits(hC.numpy(), before)
+    ozk.ozk_release_cached()
+    assert same_bits(dgemm(A, B, 14), before)
+    hC.zero_()
+    st = torch.cuda.Stream()
+    ozk.ozk_dgemm_host_async(M, N, K, hA, K, hB, N, hC, N, 14, stream=st)
+    st.synchronize()
+    assert same_bits(hC.numpy(), before)
+    ozk.ozk_release_cached()
+    hC.zero_()
+    ozk.ozk_dgemm_host(M, N, K, hA, K, hB, N, hC, N, 14)
+    assert same_bits(hC.numpy(), before)
+    assert ozk.ozk_stream_status() == 0
+
+
 def test_caller_workspace_call_captures_into_a_cuda_graph():
     """ozk_dgemm_ws only enqueues work (no synchronisation, no allocation), so
     a warmed-up call can be captured into a CUDA graph; replays reproduce it
