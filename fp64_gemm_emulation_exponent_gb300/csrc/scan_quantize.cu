@@ -6,7 +6,9 @@
 //
 // All arithmetic on the operands is integer work on IEEE-754 bit patterns:
 // GB300's FP64 pipe is slow, and rounding m * 2^sh to an integer is a shift
-// plus a rounding increment.  Both kernels cover A and B in one launch.
+// plus a rounding increment.  The scan and the quantisation each cover A and
+// B in one launch; a third kernel scans and quantises rows of A in one pass
+// where a row fits one block.
 #include <map>
 #include <mutex>
 
