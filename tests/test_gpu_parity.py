@@ -533,9 +533,10 @@ def test_release_cached_and_reuse():
 
 def test_caller_workspace_call_captures_into_a_cuda_graph():
     """ozk_dgemm_ws only enqueues work (no synchronisation, no allocation), so
-    a warmed-up call can be captured into a CUDA graph; replays reproduce it
-    bit for bit and follow new input values in the same buffers."""
-    M, N, K, n = 300, 260, 2100, 14
+    a warmed-up call can be captured into a CUDA graph (here one large enough
+    for the fused row kernel, whose side stream joins the capture); replays
+    reproduce it bit for bit and follow new input values in the same buffers."""
+    M, N, K, n = 2048, 72, 2100, 14
     A, B = inputs(M, N, K, seed=77)
     dA, dB = dev(A), dev(B)
     C = torch.empty((M, N), dtype=torch.float64, device="cuda")
