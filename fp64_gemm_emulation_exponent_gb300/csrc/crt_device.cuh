@@ -246,14 +246,17 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[G]) {
 
 // One thread per 4G consecutive columns of one row, in G groups of 4.
 // NFIX > 0 fixes the moduli count at compile time (it must equal K.n); those
-// kernels are held to three 256-thread blocks per SM (80 registers, a few
-// spilled), which hides more of the multiply-add latency than two.
+// kernels are held to four 256-thread blocks per SM (64 registers, some
+// spilled) up to four limbs and to three (80 registers) beyond: measured on
+// GB300, four blocks hide more of the multiply-add latency than three at 8
+// and 14 moduli (combine 3.5-8% faster) while the six-limb kernels spill too
+// much at 64 registers (4.5% slower at 20 moduli).
 //  IN_KIND 0: uint8 residues, modulus k at in + k * plane, row i at + i * ldi;
 //  IN_KIND 1: int32 partial sums, split sp and modulus k at (sp * n + k) * plane.
 // All residue words are loaded before any arithmetic so that the loads of a
 // thread are in flight together.
 template <int NL, int IN_KIND, bool LIMBS, int G, int NFIX>
-__global__ void __launch_bounds__(256, NFIX ? 3 : 1) crt_kernel(const void* __restrict__ in, int64_t ldi,
+__global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(const void* __restrict__ in, int64_t ldi,
                                                   int64_t plane, int64_t M, int64_t N, int splits,
                                                   const int32_t* __restrict__ s,
                                                   const int32_t* __restrict__ t,
