@@ -20,7 +20,7 @@ namespace {
 constexpr uint64_t kAbsMask = 0x7FFFFFFFFFFFFFFFull;
 constexpr uint64_t kInfBits = 0x7FF0000000000000ull;
 constexpr int kScanThreads = 256;
-constexpr int kQThreads = 128;
+constexpr int kQThreads = 256;
 constexpr int kQK = 16;  // K elements per quantisation thread: one 32-byte store per modulus
 
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
@@ -299,11 +299,11 @@ struct QuantParams {
 
 // One thread: 16 consecutive K entries of one row of A (thread order: k fastest,
 // so loads and stores of a warp are contiguous) or of one column of B.  For B
-// a block is 32 columns (the lanes) x 4 consecutive 16-entry K groups (the
+// a block is 32 columns (the lanes) x 8 consecutive 16-entry K groups (the
 // warps): each of a warp's 16 row loads is 256 contiguous bytes, and the
-// block writes each column's slice 128 contiguous bytes (a whole L2 line)
+// block writes each column's slice 256 contiguous bytes (two whole L2 lines)
 // per modulus at once; consecutive blocks take the next 32 columns of the
-// same 64 rows.  Each thread writes one 32-byte run of every modulus' slice.
+// same 128 rows.  Each thread writes one 32-byte run of every modulus' slice.
 template <int NL>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams qp) {
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
