@@ -467,6 +467,27 @@ def test_host_async_calls_in_flight():
         assert same_bits(hC.numpy(), dgemm(A, B, 14))
 
 
+def test_host_async_pair_residue_and_split_k_outputs():
+    """Back-to-back ozk_dgemm_host_async calls whose later ones find an earlier
+    call still computing (the whole-product schedule), with K >= 8192 (the
+    GEMM writes uint16 pair residues) and K >= 2^17 (int32 split-K partials):
+    every C equals the device path bit for bit."""
+    shapes = [(1024, 1024, 8200), (1024, 520, 8200), (96, 40, 140000), (96, 40, 140000)]
+    st = torch.cuda.Stream()
+    calls = []
+    for idx, (M, N, K) in enumerate(shapes):
+        A, B = inputs(M, N, K, seed=300 + idx)
+        hA = torch.from_numpy(A).pin_memory()
+        hB = torch.from_numpy(B).pin_memory()
+        hC = torch.full((M, N), np.nan, dtype=torch.float64).pin_memory()
+        ozk.ozk_dgemm_host_async(M, N, K, hA, K, hB, N, hC, N, 14, stream=st)
+        calls.append((A, B, hA, hB, hC))
+    st.synchronize()
+    assert ozk.ozk_stream_status(st) == 0
+    for A, B, _, _, hC in calls:
+        assert same_bits(hC.numpy(), dgemm(A, B, 14))
+
+
 def test_host_async_from_two_threads():
     """Two host threads, each with its own stream, enqueue three
     ozk_dgemm_host_async calls apiece (the library serialises the enqueueing
