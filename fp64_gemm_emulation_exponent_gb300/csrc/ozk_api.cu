@@ -281,6 +281,25 @@ int cached_workspace(cudaStream_t st, size_t need, void** out) {
   return OZK_OK;
 }
 
+// The regions of one call's workspace (caller-provided or cached).
+struct WsViews {
+  uint64_t* amax;
+  int32_t* s;
+  int32_t* t;
+  uint16_t* as;
+  uint16_t* bs;
+  uint8_t* out;
+  size_t esize;  // bytes per element of the residue or partial-sum planes
+};
+
+WsViews views_of(void* ws, const Layout& L) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  return {reinterpret_cast<uint64_t*>(base + L.amax), reinterpret_cast<int32_t*>(base + L.s),
+          reinterpret_cast<int32_t*>(base + L.t),     reinterpret_cast<uint16_t*>(base + L.a),
+          reinterpret_cast<uint16_t*>(base + L.b),    base + L.out,
+          static_cast<size_t>(L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4))};
+}
+
 int record(ozk_event_t* ev, int idx, cudaStream_t stream) {
   if (!ev) return OZK_OK;
   return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[idx]), stream) == cudaSuccess ? OZK_OK
@@ -313,13 +332,8 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   }
   const Layout L = layout_for(M, N, K, n);
   if (!ws || ws_bytes < L.total || reinterpret_cast<uintptr_t>(ws) % 256) return OZK_ERR_WORKSPACE;
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
-  int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
-  int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
-  uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
-  uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
-  void* out = base + L.out;
+  const auto [amax, s, t, as, bs, out, esize] = views_of(ws, L);
+  (void)esize;
   const int beta = beta_for(K, n);
 
   if ((rc = record(ev, 0, stream))) return rc;
@@ -523,14 +537,7 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
     const Layout L = layout_for(M, N, K, n_moduli);
     void* ws = nullptr;
     if ((rc = cached_workspace(cs, L.total, &ws))) return rc;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
-    int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
-    int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
-    uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
-    uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
-    uint8_t* out = base + L.out;
-    const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
+    const auto [amax, s, t, as, bs, out, esize] = views_of(ws, L);
     const int beta = beta_for(K, n_moduli);
     OZK_CUDA(cudaMemcpy2DAsync(dA, sizeof(double) * K, A, sizeof(double) * lda, sizeof(double) * K, M,
                                cudaMemcpyHostToDevice, h.in));
@@ -573,14 +580,7 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
     const Layout L = layout_for(M, N, K, n_moduli);
     void* ws = nullptr;
     if ((rc = cached_workspace(cs, L.total, &ws))) return rc;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    uint64_t* amax = reinterpret_cast<uint64_t*>(base + L.amax);
-    int32_t* s = reinterpret_cast<int32_t*>(base + L.s);
-    int32_t* t = reinterpret_cast<int32_t*>(base + L.t);
-    uint16_t* as = reinterpret_cast<uint16_t*>(base + L.a);
-    uint16_t* bs = reinterpret_cast<uint16_t*>(base + L.b);
-    uint8_t* out = base + L.out;
-    const size_t esize = L.kind == 0 ? 1 : (L.kind == 2 ? 2 : 4);
+    const auto [amax, s, t, as, bs, out, esize] = views_of(ws, L);
     const int beta = beta_for(K, n_moduli);
     // blocks of whole 256-row / 256-column tiles (the CTA-pair GEMM's tile),
     // four per dimension once it is long enough to keep every tile's GEMM busy
