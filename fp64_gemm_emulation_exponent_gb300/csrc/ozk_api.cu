@@ -682,7 +682,7 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
 int ozk_dgemm_host(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
                    int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
   const int rc = host_enqueue(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream);
-  if (rc) return rc;
+  if (rc || M == 0 || N == 0) return rc;  // an empty C: nothing was enqueued
   return cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? OZK_OK : OZK_ERR_CUDA;
 }
 

@@ -2,6 +2,7 @@
 include/ozk.h declares, and its host-side logic (moduli, bit budget, slice
 padding, workspace size, status text) agrees with the oracle and with itself.
 No compute call is made here (no GPU)."""
+import ctypes
 import os
 import re
 
@@ -110,3 +111,28 @@ def test_status_strings():
     for code in range(0, 7):
         assert ozk.status_string(code)
     assert ozk.status_string(99) == "unknown status"
+
+
+def test_argument_errors_come_back_before_any_cuda_call():
+    """Every GEMM entry point checks its arguments on the host and returns
+    the error before touching CUDA, so these calls run on a machine without a
+    GPU; an empty C is a no-op that succeeds there too."""
+    L = ozk.lib()
+    p = ctypes.c_void_p
+    bufs = [(ctypes.c_double * 64)() for _ in range(3)]
+    a, b, c = (ctypes.cast(x, p) for x in bufs)
+    for name in ("ozk_dgemm", "ozk_dgemm_host", "ozk_dgemm_host_async"):
+        f = getattr(L, name)
+        assert f(-1, 2, 2, a, 2, b, 2, c, 2, 14, None) == ozk.OZK_ERR_INVALID_ARG
+        assert f(2, 2, 2, a, 2, b, 2, c, 2, 1, None) == ozk.OZK_ERR_UNSUPPORTED        # n_moduli < 2
+        assert f(2, 2, 2, a, 2, b, 2, c, 2, 21, None) == ozk.OZK_ERR_UNSUPPORTED       # n_moduli > 20
+        assert f(2, 2, ozk.OZK_MAX_K + 1, a, ozk.OZK_MAX_K + 1, b, 2, c, 2, 14, None) == ozk.OZK_ERR_UNSUPPORTED
+        assert f(2, 2, 2, None, 2, b, 2, c, 2, 14, None) == ozk.OZK_ERR_INVALID_ARG    # null A
+        assert f(2, 2, 2, a, 1, b, 2, c, 2, 14, None) == ozk.OZK_ERR_INVALID_ARG       # lda < K
+        assert f(2, 2, 2, a, 2, b, 2, c, 1, 14, None) == ozk.OZK_ERR_INVALID_ARG       # ldc < N
+        assert f(2, 2, 2, a, 2, b, 2, a, 2, 14, None) == ozk.OZK_ERR_INVALID_ARG       # C overlaps A
+        assert f(2, 2, 60000, a, 60000, b, 2, c, 2, 2, None) == ozk.OZK_ERR_UNSUPPORTED  # beta < 1
+        assert f(0, 5, 3, None, 3, None, 5, None, 5, 14, None) == ozk.OZK_OK           # empty C
+    assert L.ozk_dgemm_ws(2, 2, 2, a, 2, b, 2, c, 2, 1, None, 0, None) == ozk.OZK_ERR_UNSUPPORTED
+    assert L.ozk_dgemm_bits(2, 2, 2, a, 2, b, 2, c, 2, 0, None) == ozk.OZK_ERR_INVALID_ARG   # target < 1
+    assert L.ozk_dgemm_bits(2, 2, 2, a, 2, b, 2, c, 2, 200, None) == ozk.OZK_ERR_UNSUPPORTED
