@@ -221,22 +221,23 @@ def run_reference(args, ranks: Ranks):
         return None
     import oracle
 
-    w = workloads.WORKLOADS[WORKLOAD]
+    w = workloads.WORKLOADS[args.workload]
+    n = args.moduli
     A, B = workloads.workload_operands(w)
-    rows, cols = 2, 64  # per step: a 2 x 64 block of C over the full K
+    rows, cols = min(2, w.M), min(64, w.N)  # per step: a rows x cols block of C over the full K
     for _ in range(args.warmup):
-        oracle_block_rate(A, B, N_MODULI, rows, cols)
+        oracle_block_rate(A, B, n, rows, cols)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_block_rate(A, B, N_MODULI, rows, cols)
+        oracle_block_rate(A, B, n, rows, cols)
     dt = time.perf_counter() - t0
     value = 2.0 * rows * cols * w.K * args.steps / dt / 1e12
-    sample = f"per step C[0:{rows}, 0:{cols}] of {w.M}x{w.N}x{w.K} (full K, {N_MODULI} moduli)"
+    sample = f"per step C[0:{rows}, 0:{cols}] of {w.M}x{w.N}x{w.K} (full K, {n} moduli)"
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config(w, N_MODULI),
+        "data": "synthetic", "config": config(w, n),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
