@@ -749,7 +749,7 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
               ozk_stream_t stream) {
   if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
   const int beta = beta_for(K, n_moduli);
-  if (beta < 1 || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
+  if (beta < 1 || K > OZK_MAX_K || M > kMaxDim || N > kMaxDim) return OZK_ERR_UNSUPPORTED;
   if (M + N == 0) return OZK_OK;
   if (!scratch || (M && !s) || (N && !t)) return OZK_ERR_INVALID_ARG;
   if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;

@@ -606,7 +606,8 @@ extern "C" int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* 
   if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
   const int beta = beta_for(K, n_moduli);
   if (beta < 1 || K > OZK_MAX_K) return OZK_ERR_UNSUPPORTED;
-  if (M + N > OZK_SCALE_NOALLOC_MAX) return OZK_ERR_WORKSPACE;  // beyond the fixed scratch
+  // beyond the fixed scratch (compared without forming M + N, which could overflow)
+  if (M > OZK_SCALE_NOALLOC_MAX || N > OZK_SCALE_NOALLOC_MAX - M) return OZK_ERR_WORKSPACE;
   if (M + N == 0) return OZK_OK;
   if ((M && !s) || (N && !t)) return OZK_ERR_INVALID_ARG;
   if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;

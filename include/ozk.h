@@ -42,7 +42,7 @@ typedef struct CUevent_st* ozk_event_t;   /* identical to cudaEvent_t */
 typedef enum {
   OZK_OK = 0,
   OZK_ERR_INVALID_ARG = 1, /* bad pointer, size, leading dimension or overlap */
-  OZK_ERR_UNSUPPORTED = 2, /* K > OZK_MAX_K, n_moduli outside 2..20, or too few moduli for K */
+  OZK_ERR_UNSUPPORTED = 2, /* K > OZK_MAX_K, M or N > 2^30 - 1, n_moduli outside 2..20, or too few moduli for K */
   OZK_ERR_WORKSPACE = 3,   /* caller workspace too small, or allocation failed */
   OZK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   OZK_ERR_TIMEOUT = 5,     /* a kernel's bounded pipeline wait ran out (device-side) */

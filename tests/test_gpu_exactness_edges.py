@@ -1,0 +1,244 @@
+"""GPU parity at the edges the kernels' exactness rests on, against the oracle.
+
+1. The residue GEMM runs on fp16 tensor cores with fp32 accumulators in TMEM.
+   It is exact only because every fp32 partial sum of a chunk is an integer
+   that fp32 holds exactly: at most 1024 * 2^14 = 2^24 in magnitude on the
+   1024-term chunks (converted with cvt.rni), at most 256 * 2^14 = 2^22 on
+   the 256-term chunks (converted by adding 1.5 * 2^23).  Residues drawn from
+   data keep chunk sums near 2^17, so these tests feed crafted slices that
+   drive every chunk to the bound (all products (-128)(-128) = 2^14: a chunk
+   sum of exactly 2^24, or 2^22), one odd small term short of it (1023
+   products of 2^14 and one of +-1, +-3, 127, ...), and the negative side
+   (products of -16256).  The int32 sums (out_kind 1) and the residues mod p
+   (out_kind 0) must equal the oracle's exact int64 sums bit for bit, on the
+   single-CTA kernel (K < 2048: 256-term chunks below K = 1024, 1024-term
+   from there) and on the CTA-pair kernel (K >= 2048).
+
+2. The combine's unscale rounds X 2^-(s+t) to nearest, ties to even, from
+   integer bits (a funnel-shift path for normal results, a general one for
+   subnormals and overflow).  Random residues give X with ~100 significant
+   bits, so an exact halfway case never occurs by chance.  These tests feed
+   residues of X = +-(odd 54-bit integer) 2^k (halfway between two doubles at
+   any normal scale), of X = +-odd 2^k with S = k + 1075 (halfway between two
+   subnormals), and the ties at the subnormal/normal boundary and at the
+   overflow threshold, through all three input kinds and both combine kernels
+   (runtime moduli count for narrow outputs, compile-time count for wide
+   ones), against the oracle's Garner CRT and correctly rounded unscale.
+
+Method: Ozaki scheme II on the "Day 12" page (ithelp.ithome.com.tw), sections
+"Profile 不能只看 Tensor Core" (the integer GEMM per modulus, mod reduction,
+CRT reconstruction, undo scaling) and "先定義公平比較" (the precision
+contract: the integer stage is exact, the FP64 output one correct rounding).
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp64_gemm_emulation_exponent_gb300 import ozk
+from gpu_helpers import dev, run_combine, run_gemm, run_lift, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+# --------------------------------------------------------------------------
+# 1. fp32 chunk sums at their bounds
+# --------------------------------------------------------------------------
+def f16_slices(r: np.ndarray, kpad: int) -> torch.Tensor:
+    """int8 residues n x rows x K -> fp16 bit patterns n x rows x kpad (zero padded)."""
+    n, rows, K = r.shape
+    out = np.zeros((n, rows, kpad), dtype=np.float16)
+    out[:, :, :K] = r.astype(np.float16)
+    return dev(out.view(np.int16))
+
+
+def crafted_operands(M, N, K, seed):
+    """Two moduli's residues: modulus 0 with products (-128)(-128) = 2^14,
+    modulus 1 with products (-128)(127) = -16256, each row of A and column of
+    B holding at most one entry that breaks the pattern (a small or extreme
+    value at the start, the end or a chunk edge of K).  Rows/columns whose
+    special value is -128 (resp. 127 in B of modulus 1) keep the pattern, so
+    their chunk sums sit exactly on the bound."""
+    rng = np.random.default_rng(seed)
+    ra = np.full((2, M, K), -128, dtype=np.int8)
+    rb = np.empty((2, K, N), dtype=np.int8)
+    rb[0] = -128
+    rb[1] = 127
+    spots = sorted({0, K - 1, min(K - 1, 255), min(K - 1, 256), min(K - 1, 1023), min(K - 1, 1024), K // 2})
+    vals = np.array([-128, 1, -1, 3, -3, 127, 0, 2, -127, 64], dtype=np.int8)
+    for i in range(M):
+        v = vals[i % len(vals)]
+        ra[:, i, spots[(i // len(vals)) % len(spots)]] = v
+    for j in range(N):
+        v = vals[(j * 7) % len(vals)]
+        k = spots[(j // 3) % len(spots)]
+        rb[0, k, j] = v
+        rb[1, k, j] = v if v != -128 else 127
+    # a few rows and columns with the pattern everywhere, whatever the table gave them
+    ra[:, rng.integers(0, M, 4)] = -128
+    for j in rng.integers(0, N, 4):
+        rb[0, :, j] = -128
+        rb[1, :, j] = 127
+    return ra, rb
+
+
+@pytest.mark.parametrize("K", [1024, 1088, 2048, 3072, 4096])
+def test_gemm_chunk_sums_at_two_to_the_24(K):
+    """1024-term chunks (single CTA at K = 1024 and 1088, CTA pairs from 2048):
+    chunk sums of exactly 2^24, 2^24 - 2^14 + small odd terms, and their
+    negative counterparts, bit-exact."""
+    M, N, n = 300, 260, 2
+    ra, rb = crafted_operands(M, N, K, seed=K)
+    raw, cmod = oracle.gemm_mod(ra, rb, n)
+    # the crafted sums really reach the bound: some chunk of modulus 0 is 2^24 exactly
+    assert int(raw[0].max()) == K * 2**14  # every 1024-term chunk of a full row/column is 2^24
+    kpad = ozk.ozk_kpad(K)
+    a_sl = f16_slices(ra, kpad)
+    b_sl = f16_slices(rb.transpose(0, 2, 1), kpad)
+    out32, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=1)
+    assert np.array_equal(out32.cpu().numpy()[0, :, :, :N], raw)
+    out8, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
+    assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    assert ozk.ozk_stream_status() == 0
+
+
+@pytest.mark.parametrize("K", [255, 256, 512, 768, 960])
+def test_gemm_chunk_sums_at_two_to_the_22(K):
+    """K below 1024: 256-term chunks converted by the 1.5 * 2^23 add; chunk
+    sums of exactly 2^22 (the add lands on 2^24) and just below, bit-exact."""
+    M, N, n = 300, 260, 2
+    ra, rb = crafted_operands(M, N, K, seed=K)
+    raw, cmod = oracle.gemm_mod(ra, rb, n)
+    assert int(raw[0].max()) == K * 2**14  # every 256-term chunk of a full row/column is 2^22
+    kpad = ozk.ozk_kpad(K)
+    a_sl = f16_slices(ra, kpad)
+    b_sl = f16_slices(rb.transpose(0, 2, 1), kpad)
+    out32, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=1)
+    assert np.array_equal(out32.cpu().numpy()[0, :, :, :N], raw)
+    out8, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
+    assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    assert ozk.ozk_stream_status() == 0
+
+
+def test_gemm_chunk_bound_split_k():
+    """Split-K shares of the CTA-pair kernel, each share's chunks at 2^24."""
+    M, N, n, K, splits = 260, 300, 2, 6144, 3
+    ra, rb = crafted_operands(M, N, K, seed=5)
+    raw, _ = oracle.gemm_mod(ra, rb, n)
+    kpad = ozk.ozk_kpad(K)
+    out32, _ = run_gemm(f16_slices(ra, kpad), f16_slices(rb.transpose(0, 2, 1), kpad), M, N, K, n,
+                        out_kind=1, splits=splits)
+    got = out32.cpu().numpy()[:, :, :, :N].astype(np.int64).sum(axis=0)
+    assert np.array_equal(got, raw.astype(np.int64))
+    assert ozk.ozk_stream_status() == 0
+
+
+# --------------------------------------------------------------------------
+# 2. round-to-even ties in the unscale
+# --------------------------------------------------------------------------
+def tie_problem(n, M, N, seed):
+    """Exact halfway cases X 2^-S, S = s_i (t_j = 0).  Returns the byte
+    residues (n x M x N), the pair residues ((n+1)/2 x M x N), s, t and the
+    constructed X as Python ints for a spot check."""
+    rng = np.random.default_rng(seed)
+    ps = [int(p) for p in oracle.moduli(n)]
+    P = 1
+    for p in ps:
+        P *= p
+    kmax = (P // 2).bit_length() - 1 - 54  # odd54 2^k < 2^(54 + k) <= P/2
+    assert kmax >= 0
+    odd = np.zeros((M, N), dtype=np.int64)
+    k = np.zeros((M, N), dtype=np.int64)
+    s = np.zeros(M, dtype=np.int64)
+    kind = rng.integers(0, 8, M)
+    kind[:4] = [0, 1, 2, 3]
+    for i in range(M):
+        if kind[i] in (0, 4, 5, 6, 7):  # normal result: odd 54-bit significand, any k
+            odd[i] = (1 << 53) | (rng.integers(0, 1 << 52, N) << 1) | 1
+            k[i] = rng.integers(0, kmax + 1, N)
+            s[i] = rng.integers(-850, 900)  # 53 + k - S stays in the normal exponent range
+        elif kind[i] == 1:  # halfway between two subnormals: value = odd 2^-1075, odd < 2^53
+            kr = int(rng.integers(0, kmax + 1))
+            bits = rng.integers(2, 53, N)
+            odd[i] = (np.int64(1) << (bits - 1)) | (rng.integers(0, 1 << 50, N) % (np.int64(1) << (bits - 1))) | 1
+            k[i] = kr
+            s[i] = kr + 1075
+        elif kind[i] == 2:  # the largest subnormal tie: rounds up to the smallest normal
+            kr = int(rng.integers(0, kmax + 1))
+            odd[i] = (1 << 53) - 1
+            k[i] = kr
+            s[i] = kr + 1075
+        else:  # (2^54 - 1) 2^970: halfway between the largest double and 2^1024 -> Inf
+            kr = int(rng.integers(0, kmax + 1))
+            odd[i] = (1 << 54) - 1
+            k[i] = kr
+            s[i] = kr - 970
+    sign = rng.choice(np.array([-1, 1], dtype=np.int64), size=(M, N))
+
+    def residues_mod(m):
+        pk = np.array([pow(2, int(e), m) for e in range(int(k.max()) + 1)], dtype=np.int64)
+        r = (odd % m) * pk[k] % m
+        return np.where(sign < 0, (m - r) % m, r)
+
+    cmod = np.stack([residues_mod(p) for p in ps]).astype(np.uint8)
+    pairs = [residues_mod(ps[2 * j] * ps[2 * j + 1]) if 2 * j + 1 < n else residues_mod(ps[2 * j])
+             for j in range((n + 1) // 2)]
+    pair = np.stack(pairs).astype(np.uint16)
+    spot = [(int(i), int(j)) for i, j in zip(rng.integers(0, M, 40), rng.integers(0, N, 40))]
+    X = {(i, j): int(sign[i, j]) * int(odd[i, j]) * 2 ** int(k[i, j]) for i, j in spot}
+    return cmod, pair, s.astype(np.int32), np.zeros(N, dtype=np.int32), X
+
+
+def is_tie(x: int, S: int, got: float) -> bool:
+    """x 2^-S lies exactly halfway between `got` and a neighbouring double."""
+    exact = Fraction(x, 1) / Fraction(2) ** S if S >= 0 else Fraction(x * 2 ** (-S))
+    if np.isinf(got):
+        return exact == Fraction((2**54 - 1) * (1 if x > 0 else -1)) * Fraction(2) ** 970
+    g = Fraction(got)
+    other = Fraction(float(np.nextafter(got, np.inf if exact > g else -np.inf)))
+    return exact == (g + other) / 2
+
+
+@pytest.mark.parametrize("n", [8, 14, 20])
+@pytest.mark.parametrize("M,N", [(96, 200), (1024, 1248)])
+def test_crt_round_to_even_ties(n, M, N):
+    """All outputs halfway cases, both parities of the kept bit, both signs;
+    byte residues (in_kind 0), pair residues (2) and split int32 sums (1);
+    the runtime-count kernel at 96 x 200, the compile-time-count kernel at
+    1024 x 1248 (in_kind 0 and 2)."""
+    cmod, pair, s, t, Xspot = tie_problem(n, M, N, seed=1000 * n + M)
+    Xo = oracle.crt(cmod, n)
+    for (i, j), x in Xspot.items():  # the oracle's CRT recovers the constructed X
+        assert oracle.limbs_to_int(Xo[i, j]) == x
+    S = np.broadcast_to(s[:, None].astype(np.int64) + t[None, :], (M, N)).astype(np.int32)
+    want = oracle.round_scaled(Xo.reshape(-1, oracle.LIMBS), S.ravel().copy()).reshape(M, N)
+    for (i, j), x in Xspot.items():  # and they are exact ties
+        assert is_tie(x, int(S[i, j]), float(want[i, j]))
+    ds, dt = dev(s), dev(t)
+    ld8 = (N + 15) // 16 * 16
+    planes8 = np.zeros((n, M, ld8), dtype=np.uint8)
+    planes8[:, :, :N] = cmod
+    C8 = run_combine(dev(planes8), 0, ld8, 1, ds, dt, M, N, n).cpu().numpy()
+    assert same_bits(C8, want)
+    ld16 = (N + 7) // 8 * 8
+    planes16 = np.zeros((pair.shape[0], M, ld16), dtype=np.uint16)
+    planes16[:, :, :N] = pair
+    C16 = run_combine(dev(planes16.view(np.int16)), 2, ld16, 1, ds, dt, M, N, n).cpu().numpy()
+    assert same_bits(C16, want)
+    # int32 partial sums of two K shares whose residues add up to c mod p
+    rng = np.random.default_rng(n + M)
+    ps = oracle.moduli(n).astype(np.int64)[:, None, None]
+    ld32 = (N + 3) // 4 * 4
+    part0 = rng.integers(-(2**29), 2**29, (n, M, N))
+    part1 = (cmod.astype(np.int64) - part0) % ps + ps * rng.integers(-(2**20), 2**20, (n, M, N))
+    planes32 = np.zeros((2, n, M, ld32), dtype=np.int32)
+    planes32[0, :, :, :N] = part0
+    planes32[1, :, :, :N] = part1
+    C32 = run_combine(dev(planes32), 1, ld32, 2, ds, dt, M, N, n).cpu().numpy()
+    assert same_bits(C32, want)
+    # the lifted integers themselves
+    X8 = run_lift(dev(planes8), 0, ld8, 1, M, N, n).cpu().numpy().view(np.uint32)
+    assert np.array_equal(X8, Xo)
+    assert ozk.ozk_stream_status() == 0
