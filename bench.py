@@ -46,9 +46,10 @@ def rows_fused(M: int, kpad: int) -> bool:
 
 
 def kernels_per_step(M: int, kpad: int) -> int:
-    """Our kernels per ozk_dgemm call: scan, finalize_scales, quantize, residue_gemm,
-    crt, and the fused scan-and-quantize of A's rows when that is used."""
-    return 6 if rows_fused(M, kpad) else 5
+    """Our kernels per ozk_dgemm call: scan, quantize (which derives the scales
+    from the scanned maxima), residue_gemm, crt, and the fused scan-and-quantize
+    of A's rows when that is used (the maxima's memset is a runtime call)."""
+    return 5 if rows_fused(M, kpad) else 4
 
 
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "residue_gemm_traffic.json")

@@ -1,8 +1,8 @@
 // Launchers of the CRT combine (the arithmetic is in crt_device.cuh): the
 // kernels with a runtime moduli count for byte residues, split-K int32
-// partial sums, the exact-integer (limb) output and narrow outputs, and the
-// dispatch to the compile-time-count kernels of crt_fixed.cu for the common
-// case (pair residues, FP64 output, wide).
+// partial sums, pair residues, the exact-integer (limb) output and narrow
+// outputs, and the dispatch to the compile-time-count kernels of
+// crt_fixed.cu for the common case (byte or pair residues, FP64 output, wide).
 #include "crt_device.cuh"
 
 namespace ozk {
@@ -27,8 +27,10 @@ cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64
     OZK_CRT_LAUNCH(0);
   else if (in_kind == 1)
     OZK_CRT_LAUNCH(1);
+  else if (X)
+    crt_pairs_kernel<NL, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K);
   else
-    OZK_CRT_LAUNCH(2);
+    crt_pairs_kernel<NL, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K);
 #undef OZK_CRT_LAUNCH
   return cudaGetLastError();
 }

@@ -1,25 +1,25 @@
 // Device code of the CRT combine: CRT reconstruction, symmetric lift, undo
 // scaling and FP64 write (the last three stages of the Ozaki-II pipeline on
-// the "Day 12" page, section
-// "Profile 不能只看 Tensor Core").  That page's section "Combine kernel
-// 的瓶頸又不一樣" measures its own combine at ~85% of the FP64 pipe and warns
-// that more registers per thread made it slower; on GB300 the FP64 pipe is
-// slow, so this kernel is integer-only:
+// the "Day 12" page, section "Profile 不能只看 Tensor Core").  That page's
+// section "Combine kernel 的瓶頸又不一樣" measures its own combine at ~85% of
+// the FP64 pipe and warns that more registers per thread made it slower; on
+// GB300 the FP64 pipe is slow, so this kernel is integer-only:
 //
-//   X = sum_j r_j E_j - q P  (mod 2^(32 NL)),
+//   X = S - q P  (mod 2^(32 NL)),   S = sum_k c_k e_k,   q = round(S / P),
 //
-// over the moduli taken in pairs: r_j = (c_2j u_j0 + c_2j+1 u_j1) mod m_j is
-// the residue of the pair modulus m_j = p_2j p_2j+1 (two byte residues into one
-// 16-bit one with three integer multiplies), E_j = e_2j + e_2j+1 mod P its CRT
-// basis vector; an odd last modulus enters on its own.  Pairing halves the
-// 64-bit multiply-accumulates, which bound this kernel on the FMA-heavy pipe.
-// The limb sums of r_j E_j are accumulated in 64 bits without carries and
-// -q P is folded in as q (2^(32 NL) - P).  q = round(sum_j r_j w_j / m_j) is
-// estimated in 32.32 fixed point (error below 2^18 / 2^32); the rare outputs
-// whose estimate lies within 2^20 / 2^32 of a rounding boundary get an exact
-// correction.  The lifted X in [-P/2, P/2) is then scaled by 2^-(s_i + t_j)
-// and rounded to nearest-even in integer arithmetic (a short path for normal
-// results, a general one for subnormals and overflow).
+// with e_k the CRT basis vectors (e_k = 1 mod p_k, 0 mod the other moduli).
+// S is built column by column in 16-bit limbs: every column sum
+// sum_k c_k (limb l of e_k) is below n 2^24, so the byte residues are taken
+// two at a time by a two-way 16x8-bit dot product (dp2a) against the packed
+// limbs of two basis vectors, with no modular reduction and no 64-bit
+// multiply-accumulate.  q comes from the same dot products over the ratios
+// e_k / P = w_k / p_k in 0.32 fixed point (error below 2^-20); the rare
+// outputs whose estimate lies within 2^-19 of a rounding boundary get an
+// exact symmetric lift.  The 16-bit residues of moduli pairs (the GEMM's pair
+// output) enter the same way, as two bytes with the bases E_j and 256 E_j.
+// The lifted X in [-P/2, P/2) is then scaled by 2^-(s_i + t_j) and rounded to
+// nearest-even in integer arithmetic (a short path for normal results, a
+// general one for subnormals and overflow).
 #pragma once
 
 #include "ozk_internal.h"
@@ -227,6 +227,15 @@ __device__ __forceinline__ void store4_f64(double* dst, const uint64_t (&b)[4]) 
                : "memory");
 }
 
+// w[x] for a run-time x below G, by selects (no local-memory indexing).
+template <int G>
+__device__ __forceinline__ uint32_t pick(const uint32_t (&w)[G], int x) {
+  uint32_t r = w[0];
+#pragma unroll
+  for (int y = 1; y < G; ++y) r = x == y ? w[y] : r;
+  return r;
+}
+
 template <int G>
 __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[G]) {
   if constexpr (G == 1) {
@@ -244,13 +253,27 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[G]) {
   }
 }
 
-// One thread per 4G consecutive columns of one row, in G groups of 4.
+// Below this distance (in units of 2^-32) of a rounding boundary the
+// quotient estimate q = round(S / P) may be off by one; the estimate's error
+// is at most n * 255 * 2^-33 < 2^-20 (fractions rounded to 0.32 fixed
+// point), so such outputs get the exact symmetric lift.
+constexpr uint32_t kLiftMargin = 1u << 13;
+
+
+
+// One thread per 4G consecutive columns of one row, in G groups of 4, each
+// group in two halves of two outputs.  For a half, the two byte digits of a
+// modulus pair (or the two bytes of a pair residue) sit side by side for both
+// outputs in one word: a byte permute of the two moduli's loaded words, or
+// the loaded uint16 pair residues as they are.  A two-way dot product then
+// adds both digits times limb l of their bases into column l of one output
+// (dp2a lo for the first output, hi for the second); two more columns gather
+// round(2^32 b_t / P) in 16-bit halves for q.  Columns stay below 2^29.5, so
+// 32-bit sums are exact.  X = S - q P is assembled from the columns (plus
+// q times the 16-bit limbs of 2^(32 NL) - P) into NL 32-bit limbs.
 // NFIX > 0 fixes the moduli count at compile time (it must equal K.n); those
-// kernels are held to four 256-thread blocks per SM (64 registers, some
-// spilled) up to four limbs and to three (80 registers) beyond: measured on
-// GB300, four blocks hide more of the multiply-add latency than three at 8
-// and 14 moduli (combine 3.5-8% faster) while the six-limb kernels spill too
-// much at 64 registers (4.5% slower at 20 moduli).
+// kernels are held to four 256-thread blocks per SM up to four limbs and to
+// three beyond.
 //  IN_KIND 0: uint8 residues, modulus k at in + k * plane, row i at + i * ldi;
 //  IN_KIND 1: int32 partial sums, split sp and modulus k at (sp * n + k) * plane.
 // All residue words are loaded before any arithmetic so that the loads of a
@@ -261,8 +284,16 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
                                                   const int32_t* __restrict__ s,
                                                   const int32_t* __restrict__ t,
                                                   double* __restrict__ C, int64_t ldc,
-                                                  uint32_t* __restrict__ Xout, const CrtConst K) {
+                                                  uint32_t* __restrict__ Xout,
+                                                  const __grid_constant__ CrtConst K) {
   constexpr int W = 4 * G;  // columns per thread
+  static_assert(IN_KIND != 2, "pair residues take crt_pairs_kernel");
+  // columns of a four-column group accumulated together: four share each
+  // basis constant; two keep the wider accumulators of five or six limbs small
+  constexpr int kPassCols = NL <= 4 ? 4 : 2;
+  // 16-bit limbs of the bases (a run-time count takes the most its limb count allows)
+  constexpr int NC = NFIX ? crt_cols16(NFIX) : (2 * NL < kMaxCols16 ? 2 * NL : kMaxCols16);
+  static_assert(NC <= 2 * NL, "the accumulator holds every basis limb");
   const int64_t groups = (N + W - 1) / W;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= M * groups) return;
@@ -278,22 +309,9 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
   }
   const int n = NFIX ? NFIX : K.n;  // a compile-time moduli count lets every loop unroll exactly
 
-  // IN_KIND 0/1: cw[k][gg] holds the 4 byte residues of modulus k for
-  // columns 4 gg .. 4 gg + 3.  IN_KIND 2: plane j's 2G words (two uint16
-  // residues each) sit in cw[2j][0..G-1], cw[2j+1][0..G-1].
+  // cw[k][g] holds the 4 byte residues of modulus k for columns 4g .. 4g + 3
   uint32_t cw[kMaxModuli][G];
-  if constexpr (IN_KIND == 2) {
-    const uint16_t* base = static_cast<const uint16_t*>(in) + i * ldi + jt;
-    static_for<0, kMaxModuli / 2>([&](auto jc) {
-      constexpr int j = decltype(jc)::value;
-      if (2 * j < n) {
-        uint32_t w[2 * G];
-        load_words<2 * G>(reinterpret_cast<const uint8_t*>(base + j * plane), w);
-#pragma unroll
-        for (int x = 0; x < 2 * G; ++x) cw[2 * j + x / G][x % G] = w[x];
-      }
-    });
-  } else if constexpr (IN_KIND == 0) {
+  if constexpr (IN_KIND == 0) {
     const uint8_t* base = static_cast<const uint8_t*>(in) + i * ldi + jt;
     static_for<0, kMaxModuli>([&](auto kc) {
       constexpr int k = decltype(kc)::value;
@@ -326,16 +344,6 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
     });
   }
   const int32_t si = LIMBS ? 0 : s[i];
-  uint32_t Pn[NL];  // 2^(32 NL) - P: X = sum c_k e_k + q Pn (mod 2^(32 NL))
-  {
-    uint32_t c = 1;
-#pragma unroll
-    for (int l = 0; l < NL; ++l) {
-      const uint64_t v = static_cast<uint64_t>(~K.P[l]) + c;
-      Pn[l] = static_cast<uint32_t>(v);
-      c = static_cast<uint32_t>(v >> 32);
-    }
-  }
 
 #pragma unroll 1
   for (int gg = 0; gg < G; ++gg) {
@@ -354,7 +362,171 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
         for (int o = 0; o < 4; ++o) tj[o] = (j0 + o < N) ? t[j0 + o] : 0;
       }
     }
-    // limb sums without carries; the top limb only matters modulo 2^32
+    uint64_t outbits[4] = {0, 0, 0, 0};
+    // the four columns of the group in kPassCols passes; a pass keeps its
+    // columns' accumulators live and takes each basis constant once
+#pragma unroll
+    for (int pass = 0; pass < 4 / kPassCols; ++pass) {
+      uint32_t col[kPassCols][2 * NL];
+      uint32_t qh[kPassCols], ql[kPassCols];
+#pragma unroll
+      for (int o = 0; o < kPassCols; ++o) {
+        qh[o] = ql[o] = 0;
+#pragma unroll
+        for (int l = 0; l < 2 * NL; ++l) col[o][l] = 0;
+      }
+      static_for<0, kMaxModuli / 2>([&](auto jc) {
+        constexpr int j = decltype(jc)::value;
+        if (2 * j < n) {
+          // b[h]: digits of the pair for columns 2h, 2h+1 of the pass: bytes
+          // (first, second) of the first column, then of the second
+          uint32_t b[kPassCols / 2];
+#pragma unroll
+          for (int h = 0; h < kPassCols / 2; ++h) {
+            const int sub = pass * (kPassCols / 2) + h;  // half of the group: columns 2 sub, 2 sub + 1
+            const uint32_t wa = pick<G>(cw[2 * j], gg);
+            const uint32_t wb = 2 * j + 1 < n ? pick<G>(cw[2 * j + 1 < kMaxModuli ? 2 * j + 1 : 0], gg) : 0u;
+            b[h] = __byte_perm(wa, wb, sub ? 0x7362 : 0x5140);
+          }
+#pragma unroll
+          for (int l = 0; l < NC; ++l) {
+            const uint32_t bl = K.bt[j][l];
+#pragma unroll
+            for (int h = 0; h < kPassCols / 2; ++h) {
+              col[2 * h][l] = __dp2a_lo(bl, b[h], col[2 * h][l]);
+              col[2 * h + 1][l] = __dp2a_hi(bl, b[h], col[2 * h + 1][l]);
+            }
+          }
+          const uint32_t fh = K.bfh[j];
+          const uint32_t fl = K.bfl[j];
+#pragma unroll
+          for (int h = 0; h < kPassCols / 2; ++h) {
+            qh[2 * h] = __dp2a_lo(fh, b[h], qh[2 * h]);
+            qh[2 * h + 1] = __dp2a_hi(fh, b[h], qh[2 * h + 1]);
+            ql[2 * h] = __dp2a_lo(fl, b[h], ql[2 * h]);
+            ql[2 * h + 1] = __dp2a_hi(fl, b[h], ql[2 * h + 1]);
+          }
+        }
+      });
+#pragma unroll
+      for (int o = 0; o < kPassCols; ++o) {
+        const int oc = pass * kPassCols + o;  // output column j0 + oc
+        // q = round(S / P) from qh 2^16 + ql (32.32 fixed point) plus one half
+        uint32_t q, frac;
+        asm("{\n\t.reg .u32 t;\n\t"
+            "shl.b32 t, %2, 16;\n\t"
+            "add.cc.u32 t, t, %3;\n\t"
+            "addc.u32 %0, 0, 0;\n\t"
+            "add.cc.u32 %1, t, 0x80000000;\n\t"
+            "addc.u32 %0, %0, 0;\n\t}"
+            : "=r"(q), "=r"(frac)
+            : "r"(qh[o]), "r"(ql[o]));
+        q += qh[o] >> 16;
+        // X = S + q (2^(32 NL) - P) mod 2^(32 NL), from the 16-bit columns:
+        // limb l = c_2l + c_2l+1 2^16 + the carry of limb l - 1
+        uint32_t X[NL];
+        uint32_t carry = 0;
+#pragma unroll
+        for (int l = 0; l < NL; ++l) {
+          const uint32_t c0 = col[o][2 * l] + q * K.pn16[2 * l];
+          const uint32_t c1 = col[o][2 * l + 1] + q * K.pn16[2 * l + 1];
+          uint32_t x, nc;
+          asm("{\n\t.reg .u32 t, h;\n\t"
+              "shr.u32 h, %3, 16;\n\t"
+              "shl.b32 t, %3, 16;\n\t"
+              "add.cc.u32 t, t, %2;\n\t"
+              "addc.u32 h, h, 0;\n\t"
+              "add.cc.u32 %0, t, %4;\n\t"
+              "addc.u32 %1, h, 0;\n\t}"
+              : "=r"(x), "=r"(nc)
+              : "r"(c0), "r"(c1), "r"(carry));
+          X[l] = x;
+          carry = nc;
+        }
+        if (frac < kLiftMargin || frac > ~kLiftMargin) exact_lift<NL>(X, K);
+        if constexpr (LIMBS) {
+          if (j0 + oc < N) {
+            uint32_t* dst = Xout + (i * N + j0 + oc) * OZK_LIMBS;
+            const uint32_t ext = is_negative<NL>(X) ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+            for (int l = 0; l < OZK_LIMBS; ++l) dst[l] = l < NL ? X[l] : ext;
+          }
+        } else {
+          if (si == OZK_SCALE_NONFINITE || tj[oc] == OZK_SCALE_NONFINITE)
+            outbits[oc] = kQuietNaN;
+          else if (!round_scaled_fast<NL>(X, si + tj[oc], &outbits[oc]))
+            outbits[oc] = round_scaled_bits<NL>(X, si + tj[oc]);
+        }
+      }
+    }
+    if constexpr (!LIMBS) {
+      double* dst = C + i * ldc + j0;
+      if (j0 + 3 < N && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+        store4_f64(dst, outbits);
+      } else {
+#pragma unroll
+        for (int o = 0; o < 4; ++o)
+          if (j0 + o < N) __stcs(reinterpret_cast<unsigned long long*>(dst + o), outbits[o]);
+      }
+    }
+  }
+}
+
+// The combine from the uint16 residues r_j of the moduli pairs (the GEMM's
+// pair output; an odd last plane holds c_n-1): S = sum_j r_j E_j in 32-bit
+// limbs, each product r_j (limb l of E_j) accumulated in 64 bits without
+// carries (the top limb in 32 bits: only its value mod 2^32 matters), and
+// q = round(sum_j r_j W_j / m_j) from round(2^32 W_j / m_j) in 32.32 fixed
+// point (error below 10 * 2^16 * 2^-33 < 2^-13); outputs within 2^-12 of a
+// rounding boundary get the exact lift.  One thread per 4G consecutive
+// columns of one row; pair j's residues at in + j * plane + i * ldi.
+template <int NL, bool LIMBS, int G, int NFIX>
+__global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1)
+    crt_pairs_kernel(const void* __restrict__ in, int64_t ldi, int64_t plane, int64_t M, int64_t N,
+                     const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C,
+                     int64_t ldc, uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K) {
+  constexpr int W = 4 * G;
+  constexpr uint32_t kPairLiftMargin = 1u << 20;
+  const int64_t groups = (N + W - 1) / W;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= M * groups) return;
+  int64_t i, jt;
+  if (M * groups <= 0x7FFFFFFF) {
+    const uint32_t g32 = static_cast<uint32_t>(gid), gr = static_cast<uint32_t>(groups);
+    const uint32_t i32 = g32 / gr;
+    i = i32;
+    jt = static_cast<int64_t>(g32 - i32 * gr) * W;
+  } else {
+    i = gid / groups;
+    jt = (gid - i * groups) * W;
+  }
+  const int n = NFIX ? NFIX : K.n;
+  // pw[j][x]: word x (the residues of columns 2x, 2x + 1) of pair j's plane
+  uint32_t pw[kMaxModuli / 2][2 * G];
+  const uint16_t* base = static_cast<const uint16_t*>(in) + i * ldi + jt;
+  static_for<0, kMaxModuli / 2>([&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    if (2 * j < n) load_words<2 * G>(reinterpret_cast<const uint8_t*>(base + j * plane), pw[j]);
+  });
+  const int32_t si = LIMBS ? 0 : s[i];
+
+#pragma unroll 1
+  for (int gg = 0; gg < G; ++gg) {
+    const int64_t j0 = jt + 4 * gg;
+    if (j0 >= N) break;
+    int32_t tj[4] = {0, 0, 0, 0};
+    if constexpr (!LIMBS) {
+      if (j0 + 3 < N) {
+        const int4 t4 = *reinterpret_cast<const int4*>(t + j0);
+        tj[0] = t4.x;
+        tj[1] = t4.y;
+        tj[2] = t4.z;
+        tj[3] = t4.w;
+      } else {
+#pragma unroll
+        for (int o = 0; o < 4; ++o) tj[o] = (j0 + o < N) ? t[j0 + o] : 0;
+      }
+    }
     uint64_t acc[4][NL - 1];
     uint32_t acctop[4];
     uint64_t qacc[4];
@@ -365,78 +537,22 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
 #pragma unroll
       for (int l = 0; l < NL - 1; ++l) acc[o][l] = 0;
     }
-    // moduli in pairs: one 16-bit pair residue per (pair, output)
     static_for<0, kMaxModuli / 2>([&](auto jc) {
       constexpr int j = decltype(jc)::value;
-      if (2 * j + 1 < n) {
-        // IN_KIND 2: words 2 gg, 2 gg + 1 of plane j; else the byte words of moduli 2j, 2j+1
-        uint32_t wa, wb;
-        if constexpr (IN_KIND == 2) {
-          wa = cw[2 * j + (2 * 0) / G][0];
-          wb = cw[2 * j + 1 / G][1 % G];
-#pragma unroll
-          for (int x = 1; x < G; ++x) {
-            wa = gg == x ? cw[2 * j + (2 * x) / G][(2 * x) % G] : wa;
-            wb = gg == x ? cw[2 * j + (2 * x + 1) / G][(2 * x + 1) % G] : wb;
-          }
-        } else {
-          wa = cw[2 * j][0];
-          wb = cw[2 * j + 1][0];
-#pragma unroll
-          for (int x = 1; x < G; ++x) {
-            wa = gg == x ? cw[2 * j][x] : wa;
-            wb = gg == x ? cw[2 * j + 1][x] : wb;
-          }
-        }
-        const uint32_t pu01 = K.pu[j][0] | (K.pu[j][1] << 16);  // both below 2^16
+      if (2 * j < n) {
+        const bool pair = 2 * j + 1 < n;
+        const uint32_t w01 = pick<2 * G>(pw[j], 2 * gg), w23 = pick<2 * G>(pw[j], 2 * gg + 1);
 #pragma unroll
         for (int o = 0; o < 4; ++o) {
-          uint32_t r;
-          if constexpr (IN_KIND == 2) {
-            r = ((o < 2 ? wa : wb) >> (16 * (o & 1))) & 0xFFFFu;
-          } else {
-            // bytes o of the two moduli's words side by side, then
-            // c_2j u_j0 + c_2j+1 u_j1 (< 2^25) in one two-way dot product
-            const uint32_t cacb = __byte_perm(wa, wb, o | ((4 + o) << 4));
-            const uint32_t t = __dp2a_lo(pu01, cacb, 0u);
-            r = t - (__umulhi(t, K.pmagic[j]) >> 10) * K.pm[j];
-          }
-          qacc[o] += static_cast<uint64_t>(r) * K.pfrac[j];
+          const uint32_t r = ((o < 2 ? w01 : w23) >> (16 * (o & 1))) & 0xFFFFu;
+          qacc[o] += static_cast<uint64_t>(r) * (pair ? K.pfrac[j] : K.flast);
 #pragma unroll
-          for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(r) * K.pe[j][l];
-          acctop[o] += r * K.pe[j][NL - 1];
+          for (int l = 0; l < NL - 1; ++l)
+            acc[o][l] += static_cast<uint64_t>(r) * (pair ? K.pe[j][l] : K.elast[l]);
+          acctop[o] += r * (pair ? K.pe[j][NL - 1] : K.elast[NL - 1]);
         }
       }
     });
-    if (n & 1) {  // the last modulus on its own
-      static_for<0, kMaxModuli>([&](auto kc) {
-        constexpr int k = decltype(kc)::value;
-        if (k == n - 1) {
-          uint32_t word = cw[k][0], word2 = 0;
-          if constexpr (IN_KIND == 2) {  // plane (n-1)/2 holds the last residue as uint16
-            word = cw[k][0];
-            word2 = cw[k + 1 / G][1 % G];
-#pragma unroll
-            for (int x = 1; x < G; ++x) {
-              word = gg == x ? cw[k + (2 * x) / G][(2 * x) % G] : word;
-              word2 = gg == x ? cw[k + (2 * x + 1) / G][(2 * x + 1) % G] : word2;
-            }
-          } else {
-#pragma unroll
-            for (int x = 1; x < G; ++x) word = gg == x ? cw[k][x] : word;
-          }
-#pragma unroll
-          for (int o = 0; o < 4; ++o) {
-            const uint32_t c = IN_KIND == 2 ? (((o < 2 ? word : word2) >> (16 * (o & 1))) & 0xFFFFu)
-                                            : __byte_perm(word, 0u, 0x4440 + o);
-            qacc[o] += static_cast<uint64_t>(c) * K.frac[k];
-#pragma unroll
-            for (int l = 0; l < NL - 1; ++l) acc[o][l] += static_cast<uint64_t>(c) * K.e[k][l];
-            acctop[o] += c * K.e[k][NL - 1];
-          }
-        }
-      });
-    }
     uint64_t outbits[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int o = 0; o < 4; ++o) {
@@ -447,12 +563,12 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
       uint64_t carry = 0;
 #pragma unroll
       for (int l = 0; l < NL - 1; ++l) {
-        const uint64_t v = acc[o][l] + static_cast<uint64_t>(q) * Pn[l] + carry;
+        const uint64_t v = acc[o][l] + static_cast<uint64_t>(q) * K.pn[l] + carry;
         X[l] = static_cast<uint32_t>(v);
         carry = v >> 32;
       }
-      X[NL - 1] = acctop[o] + q * Pn[NL - 1] + static_cast<uint32_t>(carry);
-      if (frac < (1u << 20) || frac > ~(1u << 20)) exact_lift<NL>(X, K);
+      X[NL - 1] = acctop[o] + q * K.pn[NL - 1] + static_cast<uint32_t>(carry);
+      if (frac < kPairLiftMargin || frac > ~kPairLiftMargin) exact_lift<NL>(X, K);
       if constexpr (LIMBS) {
         if (j0 + o < N) {
           uint32_t* dst = Xout + (i * N + j0 + o) * OZK_LIMBS;

@@ -1,9 +1,8 @@
-// The CRT combine kernel with the moduli count fixed at compile time, one
-// instantiation per count and input (byte residues or the 16-bit residues of
-// moduli pairs), for the FP64 output: with the
-// count known, the pair loop, the accumulator set-up and the limb count are
-// resolved by the compiler (about 40 fewer instructions per output than the
-// runtime-count kernel in crt_combine.cu, which serves the other cases).
+// The CRT combine kernels with the moduli count fixed at compile time, one
+// instantiation per count and input (byte residues, or the 16-bit residues of
+// moduli pairs), for the FP64 output: with the count known, the pair loop,
+// the accumulator set-up and the limb count are resolved by the compiler.
+// The run-time-count kernels in crt_combine.cu serve the other cases.
 #include "crt_device.cuh"
 
 namespace ozk {
@@ -13,12 +12,13 @@ template <int NM>
 cudaError_t launch_fixed(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,
                          const int32_t* s, const int32_t* t, double* C, int64_t ldc, const CrtConst& K,
                          cudaStream_t stream) {
-  constexpr int G = 2;
+  constexpr int G = 1;
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   if (in_kind == 2)
-    crt_kernel<crt_limbs(NM), 2, false, G, NM>
-        <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);
+    crt_pairs_kernel<crt_limbs(NM), false, 2, NM>
+        <<<static_cast<unsigned>((M * ((N + 7) / 8) + 255) / 256), 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C,
+                                                                                      ldc, nullptr, K);
   else
     crt_kernel<crt_limbs(NM), 0, false, G, NM>
         <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);

@@ -50,72 +50,83 @@ int ceil_log2(int64_t K) {
   return c;
 }
 
+// x^-1 mod m for x coprime to m (small m: a scan).
+uint32_t inverse_mod(uint64_t x, uint32_t m) {
+  x %= m;
+  for (uint32_t y = 1; y < m; ++y)
+    if (x * y % m == 1u) return y;
+  return 0;
+}
+
+// (P / m) * w as limbs, and round(2^32 w / m): a CRT basis vector of a
+// modulus m dividing P, and its ratio to P in 0.32 fixed point.
+void basis_of(int n, uint64_t m, uint32_t w, Limbs* b, uint32_t* frac) {
+  limbs_set(*b, w);
+  for (int i = 0; i < n; ++i)
+    if (m % modulus_at(i) != 0) limbs_mul_small(*b, modulus_at(i));
+  *frac = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + m / 2) / m);
+}
+
+// (P / m)^-1 mod m.
+uint32_t cofactor_inverse(int n, uint32_t m) {
+  uint64_t r = 1;
+  for (int i = 0; i < n; ++i)
+    if (m % modulus_at(i) != 0) r = r * (modulus_at(i) % m) % m;
+  return inverse_mod(r, m);
+}
+
+uint32_t limb16(const Limbs& a, int l) { return (a.w[l / 2] >> (16 * (l % 2))) & 0xFFFFu; }
+
 CrtConst build_crt_const(int n) {
   CrtConst K;
   std::memset(&K, 0, sizeof K);
   K.n = n;
+  const int NL = crt_limbs(n);
+  const int NC = crt_cols16(n);
   Limbs P;
   limbs_set(P, 1);
   for (int k = 0; k < n; ++k) limbs_mul_small(P, modulus_at(k));
   for (int l = 0; l < kMaxCrtLimbs; ++l) K.P[l] = P.w[l];
+  Limbs Pn;  // 2^(32 NL) - P
+  {
+    uint64_t c = 1;
+    std::memset(Pn.w, 0, sizeof Pn.w);
+    for (int l = 0; l < NL; ++l) {
+      c += static_cast<uint64_t>(~P.w[l]);
+      Pn.w[l] = static_cast<uint32_t>(c);
+      c >>= 32;
+    }
+  }
+  for (int l = 0; l < NL; ++l) K.pn[l] = Pn.w[l];
+  for (int l = 0; l < 2 * NL; ++l) K.pn16[l] = limb16(Pn, l);
   for (int k = 0; k < n; ++k) {
     const uint32_t p = modulus_at(k);
     K.p[k] = p;
     K.magic[k] = magic_of(p);
     K.bias[k] = bias_of(p);
-    Limbs ek;  // P/p_k, then times w_k
-    limbs_set(ek, 1);
-    uint32_t mk_mod_p = 1;
-    for (int j = 0; j < n; ++j) {
-      if (j == k) continue;
-      limbs_mul_small(ek, modulus_at(j));
-      mk_mod_p = (mk_mod_p * (modulus_at(j) % p)) % p;
-    }
-    uint32_t w = 0;
-    for (uint32_t x = 1; x < p; ++x)
-      if ((mk_mod_p * x) % p == 1u) {
-        w = x;
-        break;
-      }
-    limbs_mul_small(ek, w);  // e_k = (P/p_k) w_k < P
-    for (int l = 0; l < kMaxCrtLimbs; ++l) K.e[k][l] = ek.w[l];
-    K.frac[k] = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + p / 2) / p);
   }
-  for (int j = 0; 2 * j + 1 < n; ++j) {
-    const uint32_t pa = modulus_at(2 * j), pb = modulus_at(2 * j + 1);
-    const uint32_t m = pa * pb;
-    K.pm[j] = m;
-    uint32_t ia = 0, ib = 0;  // pb^-1 mod pa, pa^-1 mod pb
-    for (uint32_t x = 1; x < pa; ++x)
-      if ((pb % pa) * x % pa == 1u) {
-        ia = x;
-        break;
-      }
-    for (uint32_t x = 1; x < pb; ++x)
-      if ((pa % pb) * x % pb == 1u) {
-        ib = x;
-        break;
-      }
-    K.pu[j][0] = pb * ia;
-    K.pu[j][1] = pa * ib;
-    K.pmagic[j] = static_cast<uint32_t>(((uint64_t{1} << 42) + m - 1) / m);
-    Limbs E;  // P / m_j, then times w_j
-    limbs_set(E, 1);
-    uint32_t rest_mod_m = 1;
-    for (int i = 0; i < n; ++i) {
-      if (i == 2 * j || i == 2 * j + 1) continue;
-      limbs_mul_small(E, modulus_at(i));
-      rest_mod_m = static_cast<uint32_t>(static_cast<uint64_t>(rest_mod_m) * (modulus_at(i) % m) % m);
+  for (int j = 0; 2 * j < n; ++j) {
+    // byte residues: e_2j and e_2j+1 (an odd last modulus alone)
+    Limbs e[2];
+    uint32_t f[2] = {0, 0};
+    limbs_set(e[1], 0);
+    for (int h = 0; h < 2 && 2 * j + h < n; ++h) {
+      const uint32_t p = modulus_at(2 * j + h);
+      basis_of(n, p, cofactor_inverse(n, p), &e[h], &f[h]);
     }
-    uint32_t w = 0;
-    for (uint32_t x = 1; x < m; ++x)
-      if (static_cast<uint64_t>(rest_mod_m) * x % m == 1u) {
-        w = x;
-        break;
-      }
-    limbs_mul_small(E, w);  // E_j = (P/m_j) w_j < P
-    for (int l = 0; l < kMaxCrtLimbs; ++l) K.pe[j][l] = E.w[l];
-    K.pfrac[j] = static_cast<uint32_t>(((static_cast<uint64_t>(w) << 32) + m / 2) / m);
+    for (int l = 0; l < NC; ++l) K.bt[j][l] = limb16(e[0], l) | (limb16(e[1], l) << 16);
+    K.bfh[j] = (f[0] >> 16) | (f[1] & 0xFFFF0000u);
+    K.bfl[j] = (f[0] & 0xFFFFu) | (f[1] << 16);
+    // pair residues: E_j (an odd last modulus is its own residue, base e_n-1)
+    if (2 * j + 1 < n) {
+      const uint32_t m = modulus_at(2 * j) * modulus_at(2 * j + 1);
+      Limbs E;
+      basis_of(n, m, cofactor_inverse(n, m), &E, &K.pfrac[j]);
+      for (int l = 0; l < kMaxCrtLimbs; ++l) K.pe[j][l] = E.w[l];
+    } else {
+      for (int l = 0; l < kMaxCrtLimbs; ++l) K.elast[l] = e[0].w[l];
+      K.flast = f[0];
+    }
   }
   return K;
 }
@@ -339,16 +350,17 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if ((rc = record(ev, 0, stream))) return rc;
   if (fuse_rows(M, L.kpad)) {
     // K up to 4096: each row of A is scanned inside its own quantisation
-    // (read once); only B's columns need the separate scan
-    OZK_CUDA(launch_scale(0, N, K, nullptr, 0, B, ldb, beta, nullptr, t, amax + M, stream));
+    // (read once); only B's columns need the separate scan, and B's
+    // quantisation derives t from the scanned maxima
+    OZK_CUDA(launch_scan(0, N, K, nullptr, 0, B, ldb, amax + M, stream));
     if ((rc = record(ev, 1, stream))) return rc;
     OZK_CUDA(launch_quantize_rows(M, K, L.kpad, A, lda, n, beta, s, as, L.a_plane, stream));
-    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, B, ldb, nullptr, t, n, beta, nullptr, 0, bs,
-                             L.b_plane, stream));
+    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, B, ldb, nullptr, t, nullptr, amax + M, n, beta, nullptr,
+                             0, bs, L.b_plane, stream));
   } else {
-    OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, stream));
+    OZK_CUDA(launch_scan(M, N, K, A, lda, B, ldb, amax, stream));
     if ((rc = record(ev, 1, stream))) return rc;
-    OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, n, beta, as, L.a_plane, bs,
+    OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, amax, amax + M, n, beta, as, L.a_plane, bs,
                              L.b_plane, stream));
   }
   if ((rc = record(ev, 2, stream))) return rc;
@@ -546,14 +558,14 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
     OZK_CUDA(cudaEventRecord(h.ev_in[0], h.in));
     OZK_CUDA(cudaStreamWaitEvent(cs, h.ev_in[0], 0));
     if (fuse_rows(M, L.kpad)) {
-      OZK_CUDA(launch_scale(0, N, K, nullptr, 0, dB, N, beta, nullptr, t, amax + M, cs));
+      OZK_CUDA(launch_scan(0, N, K, nullptr, 0, dB, N, amax + M, cs));
       OZK_CUDA(launch_quantize_rows(M, K, L.kpad, dA, K, n_moduli, beta, s, as, L.a_plane, cs));
-      OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, n_moduli, beta, nullptr, 0, bs,
-                               L.b_plane, cs));
+      OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, nullptr, amax + M, n_moduli, beta,
+                               nullptr, 0, bs, L.b_plane, cs));
     } else {
-      OZK_CUDA(launch_scale(M, N, K, dA, K, dB, N, beta, s, t, amax, cs));
-      OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, n_moduli, beta, as, L.a_plane, bs,
-                               L.b_plane, cs));
+      OZK_CUDA(launch_scan(M, N, K, dA, K, dB, N, amax, cs));
+      OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, amax, amax + M, n_moduli, beta, as, L.a_plane,
+                               bs, L.b_plane, cs));
     }
     OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n_moduli, L.kind, out, L.ldo,
                                  L.out_plane, L.splits, sms, cs));
@@ -630,8 +642,9 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
           OZK_CUDA(launch_quantize_rows(mr, K, L.kpad, dA + r0 * K, K, n_moduli, beta, s + r0,
                                         as + r0 * L.kpad, L.a_plane, cs));
         } else {
-          OZK_CUDA(launch_scale(mr, 0, K, dA + r0 * K, K, nullptr, 0, beta, s + r0, nullptr, amax + r0, cs));
-          OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, n_moduli, beta,
+          OZK_CUDA(launch_scan(mr, 0, K, dA + r0 * K, K, nullptr, 0, amax + r0, cs));
+          OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, amax + r0, nullptr,
+                                   n_moduli, beta,
                                    as + r0 * L.kpad, L.a_plane, nullptr, 0, cs));
         }
         rows_in = r0 + mr;
@@ -640,8 +653,9 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
       } else {
         c0 = blk * cols;
         nc = std::min(cols, N - c0);
-        OZK_CUDA(launch_scale(0, nc, K, nullptr, 0, dB + c0, N, beta, nullptr, t + c0, amax + M + c0, cs));
-        OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, n_moduli, beta, nullptr,
+        OZK_CUDA(launch_scan(0, nc, K, nullptr, 0, dB + c0, N, amax + M + c0, cs));
+        OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, nullptr, amax + M + c0,
+                                 n_moduli, beta, nullptr,
                                  0, bs + c0 * L.kpad, L.b_plane, cs));
         cols_in = c0 + nc;
         r0 = 0;
@@ -771,7 +785,8 @@ int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda, const int
   if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
-  OZK_CUDA(launch_quantize(M, 0, K, ozk_kpad(K), A, lda, nullptr, 0, s, nullptr, n_moduli, beta,
+  OZK_CUDA(launch_quantize(M, 0, K, ozk_kpad(K), A, lda, nullptr, 0, const_cast<int32_t*>(s), nullptr, nullptr,
+                           nullptr, n_moduli, beta,
                            a_slices, M * ozk_kpad(K), nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
@@ -787,7 +802,8 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb, const int
   if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
-  OZK_CUDA(launch_quantize(0, N, K, ozk_kpad(K), nullptr, 0, B, ldb, nullptr, t, n_moduli, beta,
+  OZK_CUDA(launch_quantize(0, N, K, ozk_kpad(K), nullptr, 0, B, ldb, nullptr, const_cast<int32_t*>(t), nullptr,
+                           nullptr, n_moduli, beta,
                            nullptr, 0, b_slices, N * ozk_kpad(K), reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }

@@ -48,32 +48,61 @@ __host__ __device__ __forceinline__ void static_for(F&& f) {
   }
 }
 
-// Limb count of the CRT accumulator for n moduli: S = sum_k c_k e_k with
-// c_k < 256, e_k < P <= 2^(8n) stays below n 2^(8n + 8) < 2^(8n + 14).  At least 3.
+// Limb count of the CRT accumulator for n moduli: S = sum_t d_t b_t with
+// digits d_t < 256 and bases b_t < P <= 2^(8n) stays below n 2^(8n + 8) <
+// 2^(8n + 14); it is held modulo 2^(32 NL).  At least 3.
 __host__ __device__ constexpr int crt_limbs(int n) {
   return (8 * n + 14 + 31) / 32 < 3 ? 3 : (8 * n + 14 + 31) / 32;
 }
 constexpr int kMaxCrtLimbs = 6;
 
+// Bit length of the product of the first n moduli.
+__host__ __device__ constexpr int modulus_product_bits(int n) {
+  uint32_t w[kMaxCrtLimbs] = {1, 0, 0, 0, 0, 0};
+  for (int k = 0; k < n; ++k) {
+    uint64_t c = 0;
+    for (int l = 0; l < kMaxCrtLimbs; ++l) {
+      c += static_cast<uint64_t>(w[l]) * modulus_at(k);
+      w[l] = static_cast<uint32_t>(c);
+      c >>= 32;
+    }
+  }
+  for (int l = kMaxCrtLimbs - 1; l >= 0; --l)
+    for (int b = 31; b >= 0; --b)
+      if ((w[l] >> b) & 1u) return 32 * l + b + 1;
+  return 0;
+}
+// 16-bit limbs of a CRT basis vector (a number below P) for n moduli.
+__host__ __device__ constexpr int crt_cols16(int n) { return (modulus_product_bits(n) + 15) / 16; }
+constexpr int kMaxCols16 = 10;  // the product of all 20 moduli is below 2^157
+static_assert(2 * kMaxCrtLimbs >= kMaxCols16, "the accumulator holds every basis limb");
+
 // Constants of the CRT combine for one moduli count (built on the host).
 // e_k = (P/p_k) w_k with w_k = (P/p_k)^-1 mod p_k is the CRT basis vector of
 // modulus k (e_k = 1 mod p_k, 0 mod the others, e_k < P); e_k / P = w_k / p_k.
+//  * Byte residues c_k: S = sum_k c_k e_k is formed column by column in
+//    16-bit limbs, the moduli taken in pairs (2j, 2j+1) by two-way 16x8-bit
+//    dot products (dp2a): bt[j][l] = limb l of e_2j | limb l of e_2j+1 << 16
+//    (an odd last modulus alone).  q = round(S / P) from the ratios e_k / P
+//    in 0.32 fixed point, split into 16-bit halves packed the same way:
+//    bfh (high halves), bfl (low halves).
+//  * 16-bit residues r_j of the pair moduli m_j = p_2j p_2j+1 (the GEMM's pair
+//    output): S = sum_j r_j E_j with E_j = (P/m_j) W_j, W_j = (P/m_j)^-1 mod
+//    m_j, in 32-bit limbs (pe) with 64-bit multiply-accumulates, and q from
+//    round(2^32 W_j / m_j) (pfrac); an odd last modulus enters as c_n-1 e_n-1
+//    (elast, flast).
 struct CrtConst {
   uint32_t p[kMaxModuli];
   uint32_t magic[kMaxModuli];
   uint32_t bias[kMaxModuli];
-  uint32_t frac[kMaxModuli];  // round(2^32 w_k / p_k): e_k / P in 0.32 fixed point
-  uint32_t e[kMaxModuli][kMaxCrtLimbs];  // e_k, little-endian 32-bit limbs
-  uint32_t P[kMaxCrtLimbs];
-  // Moduli taken in pairs (2j, 2j+1) with m_j = p_2j p_2j+1: the pair's
-  // residue r_j = (c_2j u_j0 + c_2j+1 u_j1) mod m_j (u_j0 = 1 mod p_2j and 0 mod
-  // p_2j+1, u_j1 the other way round) has CRT basis vector E_j = e_2j + e_2j+1
-  // (mod P), and E_j / P = w_j / m_j.
-  uint32_t pm[kMaxModuli / 2];
-  uint32_t pu[kMaxModuli / 2][2];
-  uint32_t pmagic[kMaxModuli / 2];  // ceil(2^42 / m_j): floor(t / m_j) = umulhi(t, pmagic) >> 10 for t < 2^25
-  uint32_t pfrac[kMaxModuli / 2];   // round(2^32 w_j / m_j)
+  uint32_t P[kMaxCrtLimbs];              // P, little-endian 32-bit limbs
+  uint32_t pn[kMaxCrtLimbs];             // 2^(32 NL) - P (NL = crt_limbs(n)), 32-bit limbs
+  uint32_t pn16[2 * kMaxCrtLimbs];       // the same in 16-bit limbs
+  uint32_t bt[kMaxModuli / 2][kMaxCols16];
+  uint32_t bfh[kMaxModuli / 2], bfl[kMaxModuli / 2];
   uint32_t pe[kMaxModuli / 2][kMaxCrtLimbs];
+  uint32_t pfrac[kMaxModuli / 2];
+  uint32_t elast[kMaxCrtLimbs], flast;
   int n;
 };
 
@@ -84,20 +113,28 @@ int current_device_supported(int* sms);
 const CrtConst& crt_const(int n);
 
 // Launchers; each returns the first CUDA error it meets.
+// Exponent scan: the abs-bit maxima of the rows of A and the columns of B
+// into amax[0..M) and amax[M..M+N) (zeroed first), then the scales s, t.
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
                          const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
                          uint64_t* amax, cudaStream_t stream);
+// The scan alone (the maxima, no scales): launch_quantize then derives the
+// scales from the maxima and stores them.
+cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                        int64_t ldb, uint64_t* amax, cudaStream_t stream);
 // Per-modulus planes (residue slices, residue or partial-sum planes) sit
 // `plane` elements apart; the workspace spaces them an odd number of 256-byte
 // units apart so that the n streams of a kernel do not fall on the same DRAM
 // channels at the same time.
 //
 // Quantises A (when A is not null) and B (when B is not null) in one launch;
-// slices and plane strides must be 32-byte aligned.
+// slices and plane strides must be 32-byte aligned.  With a_amax (b_amax) not
+// null the scales are derived from the scanned maxima and stored in s (t);
+// otherwise s (t) are read.
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
-                            int64_t lda, const double* B, int64_t ldb, const int32_t* s,
-                            const int32_t* t, int n, int beta, uint16_t* a_out, int64_t a_plane,
-                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
+                            int64_t lda, const double* B, int64_t ldb, int32_t* s, int32_t* t,
+                            const uint64_t* a_amax, const uint64_t* b_amax, int n, int beta, uint16_t* a_out,
+                            int64_t a_plane, uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
 // Rows of A scanned and quantised in one pass (one block per row): writes
 // s[0..M) and A's slices as launch_scale + launch_quantize would.  Only for
 // K up to 4096 (quantize_rows_fits(kpad)); cudaErrorInvalidValue beyond.

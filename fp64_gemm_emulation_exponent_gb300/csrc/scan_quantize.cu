@@ -282,8 +282,11 @@ __device__ __forceinline__ void store8_u32(uint16_t* dst, const uint32_t (&w)[8]
 struct QuantParams {
   const double* A;
   const double* B;
-  const int32_t* s;
-  const int32_t* t;
+  int32_t* s;  // scales of the rows of A: read, or written when a_amax is set
+  int32_t* t;  // scales of the columns of B: read, or written when b_amax is set
+  const uint64_t* a_amax;  // scanned maxima of the rows of A (the scale is derived here), or null
+  const uint64_t* b_amax;  // the same for the columns of B
+  int beta;
   uint16_t* a_out;  // modulus k, row i at a_out + k * a_plane + i * kpad
   uint16_t* b_out;  // modulus k, column j at b_out + k * b_plane + j * kpad
   int64_t a_plane, b_plane;
@@ -317,7 +320,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
     k0 = (g - row * qp.groups) * kQK;
     plane = qp.a_plane;
     out = qp.a_out;
-    sc = qp.s[row];
+    if (qp.a_amax) {  // the scale from the row's scanned maximum; the first thread of the row stores it
+      sc = scale_of_max(qp.a_amax[row], qp.beta);
+      if (k0 == 0) qp.s[row] = sc;
+    } else {
+      sc = qp.s[row];
+    }
     const double* a = qp.A + row * qp.lda + k0;
     if (qp.a_vec && k0 + kQK <= qp.K) {
 #pragma unroll
@@ -345,7 +353,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
     k0 = kg * kQK;
     plane = qp.b_plane;
     out = qp.b_out;
-    sc = qp.t[row];
+    if (qp.b_amax) {
+      sc = scale_of_max(qp.b_amax[row], qp.beta);
+      if (k0 == 0) qp.t[row] = sc;
+    } else {
+      sc = qp.t[row];
+    }
     const double* b = qp.B + k0 * qp.ldb + row;
 #pragma unroll
     for (int e = 0; e < kQK; ++e) v[e] = (k0 + e < qp.K) ? load1_u64(b + e * qp.ldb) : 0ull;
@@ -437,9 +450,8 @@ __global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const Qu
 
 }  // namespace
 
-cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
-                         const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
-                         uint64_t* amax, cudaStream_t stream) {
+cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                        int64_t ldb, uint64_t* amax, cudaStream_t stream) {
   if (M + N == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint64_t) * static_cast<size_t>(M + N), stream);
   if (e != cudaSuccess) return e;
@@ -485,20 +497,32 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64
     scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                         const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
+                         uint64_t* amax, cudaStream_t stream) {
+  if (M + N == 0) return cudaSuccess;
+  cudaError_t e = launch_scan(M, N, K, A, lda, B, ldb, amax, stream);
+  if (e != cudaSuccess) return e;
   finalize_scales_kernel<<<static_cast<unsigned>((M + N + 255) / 256), 256, 0, stream>>>(amax, M, N, beta, s, t);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
-                            int64_t lda, const double* B, int64_t ldb, const int32_t* s,
-                            const int32_t* t, int n, int beta, uint16_t* a_out, int64_t a_plane,
-                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream) {
+                            int64_t lda, const double* B, int64_t ldb, int32_t* s, int32_t* t,
+                            const uint64_t* a_amax, const uint64_t* b_amax, int n, int beta, uint16_t* a_out,
+                            int64_t a_plane, uint16_t* b_out, int64_t b_plane, cudaStream_t stream) {
   if (kpad == 0 || (M == 0 && N == 0)) return cudaSuccess;
   QuantParams qp;
   qp.A = A;
   qp.B = B;
   qp.s = s;
   qp.t = t;
+  qp.a_amax = a_amax;
+  qp.b_amax = b_amax;
+  qp.beta = beta;
   qp.a_out = a_out;
   qp.b_out = b_out;
   qp.a_plane = a_plane;
