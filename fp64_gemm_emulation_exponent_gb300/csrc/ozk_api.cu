@@ -842,6 +842,27 @@ int ozk_residue_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
   return OZK_OK;
 }
 
+int ozk_residue_gemm_withheld(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
+                              const uint16_t* b_slices, int n_moduli, uint8_t* out, int64_t ldo,
+                              int withhold_kb, uint32_t timeout_us, ozk_stream_t stream) {
+  if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim) return OZK_ERR_INVALID_ARG;
+  if (n_moduli < 2 || n_moduli > kMaxModuli) return OZK_ERR_UNSUPPORTED;
+  const int64_t kpad = ozk_kpad(K);
+  if (kpad >= 2048 || withhold_kb < 0 || withhold_kb >= kpad / kKBlock) return OZK_ERR_INVALID_ARG;
+  if (timeout_us < 1 || timeout_us > 1000000) return OZK_ERR_INVALID_ARG;
+  if (!a_slices || !b_slices || !out || ldo < N || ldo % 16) return OZK_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a_slices) % 16 || reinterpret_cast<uintptr_t>(b_slices) % 16 ||
+      reinterpret_cast<uintptr_t>(out) % 16)
+    return OZK_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = check_device(&sms);
+  if (rc) return rc;
+  OZK_CUDA(launch_residue_gemm_withheld(M, N, kpad, a_slices, M * kpad, b_slices, N * kpad, n_moduli, out, ldo,
+                                        M * ldo, sms, 1000ull * timeout_us, withhold_kb,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
 static int check_crt_args(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind,
                           int64_t ldi, int splits) {
   if (M < 0 || N < 0) return OZK_ERR_INVALID_ARG;

@@ -146,6 +146,16 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
                                 int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
                                 int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
                                 int num_sms, cudaStream_t stream);
+// The single-CTA residue GEMM (byte residues, one split; K below 2048) with
+// every pipeline wait limited to timeout_ns and the copy of k-block
+// withhold_kb of CTA 0's first unit never issued: the MMA issuer's wait for
+// it runs out, the kernel latches OZK_ERR_TIMEOUT and every role stops.
+// cudaErrorInvalidValue where the CTA-pair kernel would run or the k-block
+// does not exist.
+cudaError_t launch_residue_gemm_withheld(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
+                                         int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
+                                         void* out, int64_t ldo, int64_t out_plane, int num_sms,
+                                         uint64_t timeout_ns, int withhold_kb, cudaStream_t stream);
 // The same for in_kind 0 or 2 and an FP64 output, through a kernel compiled
 // for this moduli count (crt_fixed.cu).
 cudaError_t launch_crt_fixed(int64_t M, int64_t N, const void* in, int in_kind, int64_t ldi, int64_t plane,

@@ -104,7 +104,7 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr size_t kStashBytes = static_cast<size_t>(kEpiThreads) * kCols;
 static_assert(kSmemBytes + kStashBytes <= 232448 && kPairSmemBytes + kStashBytes <= 232448,
               "ring, barriers and stash exceed the shared memory of a CTA");
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // limit of every pipeline wait in normal runs
 constexpr uint64_t kDrainNs = 50000000ull;
 
 // fp32 bits of 1.5 * 2^23: x + 1.5*2^23 for an integer |x| <= 2^22 has the
@@ -158,6 +158,12 @@ __constant__ ModTable c_mod = make_mod_table();
 
 struct GemmParams {
   int M, N, n, kblocks, tiles_m, tiles_n, splits, kb_per_split, out_kind;
+  // the limit of every mbarrier wait, and (single-CTA kernel only; -1 in
+  // normal runs) a k-block of CTA 0's first unit whose copy the producer
+  // withholds, so that the MMA issuer's wait for it runs out: the test of the
+  // timeout path
+  uint64_t timeout_ns;
+  int withhold_kb;
   int mod_units;           // n, or ceil(n/2) pairs of moduli for out_kind 2
   int64_t ldo, out_plane;  // row stride and per-(split, modulus) plane stride, in elements
   void* out;
@@ -202,16 +208,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of the given parity to complete.  Returns false when
-// another role has aborted, or after kTimeoutNs (then latches the fault and
+// another role has aborted, or after timeout_ns (then latches the fault and
 // tells the other roles to stop).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns) {
         *abort_flag = 1;
         atomicOr(&g_status, 1);
         return false;
@@ -222,8 +229,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // Every lane of the warp waits; the outcome is made warp-uniform so that the
 // .sync.aligned tcgen05 instructions after it see a converged warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const bool got = mbar_wait(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns) {
+  const bool got = mbar_wait(bar, parity, abort_flag, timeout_ns);
   return __all_sync(0xffffffffu, got);
 }
 
@@ -634,9 +642,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
               ok = false;
               break;
+            }
+            if (prm.withhold_kb >= 0 && blockIdx.x == 0 && u == 0 && ps == 0 && kb == w.kb0 + prm.withhold_kb) {
+              // the timeout test: this stage's copy is never issued (its full
+              // barrier never completes), the ring moves on
+              if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
             }
             mbar_expect_tx(full0 + 8 * stage, kStageBytes);
             tma_load_3d(smem_u32(sA + stage * kABytes), &tmA, kb * BK, w.mt * BM, w.p + ps, full0 + 8 * stage);
@@ -669,14 +686,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
           const int c1 = min(w.kb1, c0 + kChunkKB);
-          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
+          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag, prm.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
           for (int kb = c0; kb < c1; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, prm.timeout_ns)) {
               ok = false;
               break;
             }
@@ -723,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0;
         for (int c = 0; c < nchunks; ++c) {
-          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
             ok = false;
             break;
           }
@@ -828,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = decode_unit<PAIRS>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
             ok = false;
             break;
           }
@@ -866,14 +883,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
           const int c1 = min(w.kb1, c0 + kPairChunkKB);
-          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag)) {
+          if (!mbar_wait(acce0 + 8 * ab, aphase ^ 1u, abort_flag, prm.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
           for (int kb = c0; kb < c1; ++kb) {
-            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, prm.timeout_ns)) {
               ok = false;
               break;
             }
@@ -920,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0;
         for (int c = 0; c < nchunks; ++c) {
-          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag)) {
+          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
             ok = false;
             break;
           }
@@ -1080,12 +1097,16 @@ cudaError_t kernel_setup(const void* kernel, size_t smem, bool pairs, int* resid
 
 }  // namespace
 
-cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
-                                int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
-                                int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
-                                int num_sms, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices, int64_t a_plane,
+                        const uint16_t* b_slices, int64_t b_plane, int n, int out_kind, void* out, int64_t ldo,
+                        int64_t out_plane, int splits, int num_sms, uint64_t timeout_ns, int withhold_kb,
+                        cudaStream_t stream) {
   if (M == 0 || N == 0) return cudaSuccess;
   GemmParams prm;
+  prm.timeout_ns = timeout_ns;
+  prm.withhold_kb = withhold_kb;
   prm.M = static_cast<int>(M);
   prm.N = static_cast<int>(N);
   prm.n = n;
@@ -1114,6 +1135,7 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
                       : (long_chunks ? (po ? residue_gemm_kernel<true, true> : residue_gemm_kernel<true, false>)
                                      : (po ? residue_gemm_kernel<false, true> : residue_gemm_kernel<false, false>));
   const size_t smem = (pairs ? kPairSmemBytes : kSmemBytes) + kStashBytes;
+  if (withhold_kb >= 0 && (pairs || withhold_kb >= prm.kb_per_split)) return cudaErrorInvalidValue;
   int resident = 0;
   cudaError_t e = kernel_setup(reinterpret_cast<const void*>(kernel), smem, pairs, &resident);
   if (e != cudaSuccess) return e;
@@ -1133,6 +1155,25 @@ cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
+                                int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
+                                int out_kind, void* out, int64_t ldo, int64_t out_plane, int splits,
+                                int num_sms, cudaStream_t stream) {
+  return launch_gemm(M, N, kpad, a_slices, a_plane, b_slices, b_plane, n, out_kind, out, ldo, out_plane, splits,
+                     num_sms, kTimeoutNs, -1, stream);
+}
+
+cudaError_t launch_residue_gemm_withheld(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
+                                         int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,
+                                         void* out, int64_t ldo, int64_t out_plane, int num_sms,
+                                         uint64_t timeout_ns, int withhold_kb, cudaStream_t stream) {
+  if (withhold_kb < 0 || timeout_ns == 0 || timeout_ns > kTimeoutNs) return cudaErrorInvalidValue;
+  return launch_gemm(M, N, kpad, a_slices, a_plane, b_slices, b_plane, n, 0, out, ldo, out_plane, 1, num_sms,
+                     timeout_ns, withhold_kb, stream);
 }
 
 int take_device_status(cudaStream_t stream, int* status) {

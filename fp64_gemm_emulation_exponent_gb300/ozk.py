@@ -50,6 +50,7 @@ SIGNATURES = {
     "ozk_quantize_a": (_i32, [_i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp]),
     "ozk_quantize_b": (_i32, [_i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp]),
     "ozk_residue_gemm": (_i32, [_i64, _i64, _i64, _vp, _vp, _i32, _i32, _vp, _i64, _i32, _vp]),
+    "ozk_residue_gemm_withheld": (_i32, [_i64, _i64, _i64, _vp, _vp, _i32, _vp, _i64, _i32, ctypes.c_uint32, _vp]),
     "ozk_crt_combine": (_i32, [_i64, _i64, _i32, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _i64, _vp]),
     "ozk_crt_lift": (_i32, [_i64, _i64, _i32, _vp, _i32, _i64, _i32, _vp, _vp]),
     "ozk_event_create": (_i32, [_vp]),
@@ -217,6 +218,12 @@ def ozk_quantize_b(K, N, B, ldb, t, n_moduli, b_slices, stream=None):
 def ozk_residue_gemm(M, N, K, a_slices, b_slices, n_moduli, out_kind, out, ldo, splits, stream=None):
     return _call("ozk_residue_gemm", M, N, K, _ptr(a_slices), _ptr(b_slices), n_moduli, out_kind, _ptr(out), ldo,
                  splits, _stream(stream))
+
+
+def ozk_residue_gemm_withheld(M, N, K, a_slices, b_slices, n_moduli, out, ldo, withhold_kb, timeout_us,
+                              stream=None):
+    return _call("ozk_residue_gemm_withheld", M, N, K, _ptr(a_slices), _ptr(b_slices), n_moduli, _ptr(out), ldo,
+                 withhold_kb, timeout_us, _stream(stream))
 
 
 def ozk_crt_combine(M, N, n_moduli, inp, in_kind, ldi, splits, s, t, C, ldc, stream=None):

@@ -269,6 +269,29 @@ int ozk_crt_lift(int64_t M, int64_t N, int n_moduli, const void* in, int in_kind
                  int64_t ldi, int splits, uint32_t* X, ozk_stream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* Test hook of the failure path.                                      */
+/* ------------------------------------------------------------------ */
+
+/* ozk_residue_gemm (out_kind 0, one split) on the single-CTA kernel with
+ * every pipeline wait limited to timeout_us microseconds (1..10^6) and the
+ * copy of k-block withhold_kb (0 .. kpad/64 - 1) of the first tile of CTA 0
+ * never issued.  The wait of that CTA's MMA issuer for the missing stage runs
+ * out: the kernel latches OZK_ERR_TIMEOUT, every role of the CTA stops, the
+ * copies and MMAs in flight drain, TMEM is freed and the kernel returns; the
+ * other CTAs finish their tiles.  Nothing faults or hangs, so the context
+ * stays usable.  Every pipeline wait of the library is bounded because a
+ * wrong mbarrier phase or arrive count leaves a wait hanging (the async
+ * Tensor Core article on yfxerp.com, section 6.1); this call is how a test
+ * reaches that bound.  Returns OZK_OK once launched (ozk_stream_status then reports
+ * OZK_ERR_TIMEOUT); OZK_ERR_INVALID_ARG for K with kpad >= 2048 (the CTA-pair
+ * kernel), a k-block or time limit out of range, or the arguments
+ * ozk_residue_gemm rejects.  The planes of the withheld CTA's tiles are not
+ * written. */
+int ozk_residue_gemm_withheld(int64_t M, int64_t N, int64_t K, const uint16_t* a_slices,
+                              const uint16_t* b_slices, int n_moduli, uint8_t* out, int64_t ldo,
+                              int withhold_kb, uint32_t timeout_us, ozk_stream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* Timing helpers (thin wrappers of the CUDA runtime).                 */
 /* ------------------------------------------------------------------ */
 int ozk_event_create(ozk_event_t* ev);

@@ -136,3 +136,11 @@ def test_argument_errors_come_back_before_any_cuda_call():
     assert L.ozk_dgemm_ws(2, 2, 2, a, 2, b, 2, c, 2, 1, None, 0, None) == ozk.OZK_ERR_UNSUPPORTED
     assert L.ozk_dgemm_bits(2, 2, 2, a, 2, b, 2, c, 2, 0, None) == ozk.OZK_ERR_INVALID_ARG   # target < 1
     assert L.ozk_dgemm_bits(2, 2, 2, a, 2, b, 2, c, 2, 200, None) == ozk.OZK_ERR_UNSUPPORTED
+    # the failure-path test hook: the single-CTA kernel only, a k-block that
+    # exists and a time limit of 1 us .. 1 s
+    w = L.ozk_residue_gemm_withheld
+    assert w(2, 2, 2048, a, b, 2, c, 16, 0, 1000, None) == ozk.OZK_ERR_INVALID_ARG
+    assert w(2, 2, 64, a, b, 2, c, 16, 1, 1000, None) == ozk.OZK_ERR_INVALID_ARG
+    assert w(2, 2, 64, a, b, 2, c, 16, 0, 0, None) == ozk.OZK_ERR_INVALID_ARG
+    assert w(2, 2, 64, a, b, 2, c, 16, 0, 2000000, None) == ozk.OZK_ERR_INVALID_ARG
+    assert w(2, 2, 64, a, b, 1, c, 16, 0, 1000, None) == ozk.OZK_ERR_UNSUPPORTED
