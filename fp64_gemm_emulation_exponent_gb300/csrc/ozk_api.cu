@@ -204,7 +204,7 @@ size_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
 }
 
 int validate(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
-             int64_t ldb, const double* C, int64_t ldc, int n) {
+             int64_t ldb, const double* C, int64_t ldc, int n, int rule = 0) {
   if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
   if (n < 2 || n > kMaxModuli) return OZK_ERR_UNSUPPORTED;
   if (K > OZK_MAX_K || M > kMaxDim || N > kMaxDim) return OZK_ERR_UNSUPPORTED;
@@ -212,7 +212,7 @@ int validate(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, cons
   if (!C || ldc < N) return OZK_ERR_INVALID_ARG;
   if (K == 0) return OZK_OK;
   if (!A || !B || lda < K || ldb < N) return OZK_ERR_INVALID_ARG;
-  if (beta_for(K, n) < 1) return OZK_ERR_UNSUPPORTED;
+  if ((rule ? gamma_for(K, n) : beta_for(K, n)) < 1) return OZK_ERR_UNSUPPORTED;
   const size_t cb = span_bytes(M, N, ldc);
   if (ranges_overlap(C, cb, A, span_bytes(M, K, lda)) || ranges_overlap(C, cb, B, span_bytes(K, N, ldb)))
     return OZK_ERR_INVALID_ARG;
@@ -247,8 +247,8 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   L.ldo = L.kind == 1 ? round_up(N, 4) : round_up(N, 16);
   L.planes = L.kind == 1 ? n * L.splits : (L.kind == 2 ? (n + 1) / 2 : n);
   size_t off = 0;
-  L.amax = off;
-  off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(M + N), 256);
+  L.amax = off;  // the maxima, then the norm sums of the norm rule
+  off = align_up(off + 2 * sizeof(uint64_t) * static_cast<size_t>(M + N), 256);
   L.s = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(M), 256);
   L.t = off;
@@ -329,10 +329,12 @@ bool fuse_rows(int64_t M, int64_t kpad) {
   return quantize_rows_fits(kpad) && M <= 0x7FFFFFFF && M * kpad >= (int64_t{1} << 22);
 }
 
+// rule 0: scales from each row's (column's) largest entry; rule 1: from the
+// computed 2-norm bound (OZK_SCALING_NORM).
 int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
               int64_t ldb, double* C, int64_t ldc, int n, void* ws, size_t ws_bytes,
-              cudaStream_t stream, ozk_event_t* ev) {
-  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n);
+              cudaStream_t stream, ozk_event_t* ev, int rule = 0) {
+  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n, rule);
   if (rc) return rc;
   if (M == 0 || N == 0) return OZK_OK;
   int sms = 0;
@@ -345,23 +347,24 @@ int run_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if (!ws || ws_bytes < L.total || reinterpret_cast<uintptr_t>(ws) % 256) return OZK_ERR_WORKSPACE;
   const auto [amax, s, t, as, bs, out, esize] = views_of(ws, L);
   (void)esize;
-  const int beta = beta_for(K, n);
+  const int budget = rule ? gamma_for(K, n) : beta_for(K, n);
+  uint64_t* nsum = rule ? amax + (M + N) : nullptr;  // the norm sums follow the maxima
 
   if ((rc = record(ev, 0, stream))) return rc;
   if (fuse_rows(M, L.kpad)) {
     // K up to 4096: each row of A is scanned inside its own quantisation
     // (read once); only B's columns need the separate scan, and B's
-    // quantisation derives t from the scanned maxima
-    OZK_CUDA(launch_scan(0, N, K, nullptr, 0, B, ldb, amax + M, stream));
+    // quantisation derives t from the scanned maxima (and norm sums)
+    OZK_CUDA(launch_scan(0, N, K, nullptr, 0, B, ldb, amax + M, nsum ? nsum + M : nullptr, stream));
     if ((rc = record(ev, 1, stream))) return rc;
-    OZK_CUDA(launch_quantize_rows(M, K, L.kpad, A, lda, n, beta, s, as, L.a_plane, stream));
-    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, B, ldb, nullptr, t, nullptr, amax + M, n, beta, nullptr,
-                             0, bs, L.b_plane, stream));
+    OZK_CUDA(launch_quantize_rows(M, K, L.kpad, A, lda, n, budget, rule != 0, s, as, L.a_plane, stream));
+    OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, B, ldb, nullptr, t, nullptr, amax + M, nullptr,
+                             nsum ? nsum + M : nullptr, n, budget, nullptr, 0, bs, L.b_plane, stream));
   } else {
-    OZK_CUDA(launch_scan(M, N, K, A, lda, B, ldb, amax, stream));
+    OZK_CUDA(launch_scan(M, N, K, A, lda, B, ldb, amax, nsum, stream));
     if ((rc = record(ev, 1, stream))) return rc;
-    OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, amax, amax + M, n, beta, as, L.a_plane, bs,
-                             L.b_plane, stream));
+    OZK_CUDA(launch_quantize(M, N, K, L.kpad, A, lda, B, ldb, s, t, amax, amax + M, nsum,
+                             nsum ? nsum + M : nullptr, n, budget, as, L.a_plane, bs, L.b_plane, stream));
   }
   if ((rc = record(ev, 2, stream))) return rc;
   OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n, L.kind, out, L.ldo, L.out_plane,
@@ -383,6 +386,18 @@ int beta_for(int64_t K, int n) {
   const int num = limbs_msb(P) - 1 - ceil_log2(K);
   const int beta = num >= 0 ? num / 2 : -((-num + 1) / 2);
   return beta >= 1 ? beta : -1;
+}
+
+int gamma_for(int64_t K, int n) {
+  if (n < 2 || n > kMaxModuli) return -1;
+  if (K < 1) K = 1;
+  Limbs P;
+  limbs_set(P, 1);
+  for (int k = 0; k < n; ++k) limbs_mul_small(P, modulus_at(k));
+  const int gamma = (limbs_msb(P) - 2) / 2;
+  // the rounding slack sqrt(K)/2 of the scaled norms must stay below 2^(gamma - 3)
+  if (gamma < 1 || ceil_log2(K) > 2 * gamma - 4) return -1;
+  return gamma;
 }
 
 int current_device_supported(int* sms) { return check_device(sms); }
@@ -444,6 +459,31 @@ size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli) {
   if (M <= 0 || N <= 0 || K <= 0 || K > OZK_MAX_K) return 0;
   if (M > kMaxDim || N > kMaxDim || beta_for(K, n_moduli) < 1) return 0;
   return layout_for(M, N, K, n_moduli).total;
+}
+
+int ozk_gamma(int64_t K, int n_moduli) {
+  const int g = gamma_for(K, n_moduli);
+  return g >= 1 ? g : -OZK_ERR_UNSUPPORTED;
+}
+
+int ozk_dgemm_norm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                      int64_t ldb, double* C, int64_t ldc, int n_moduli, void* workspace, size_t workspace_bytes,
+                      ozk_stream_t stream) {
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr, 1);
+}
+
+int ozk_dgemm_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                   int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
+  int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, 1);
+  if (rc) return rc;
+  if (M == 0 || N == 0) return OZK_OK;
+  if ((rc = check_device(nullptr))) return rc;
+  const size_t need = K > 0 ? layout_for(M, N, K, n_moduli).total : 0;
+  void* ws = nullptr;
+  if (need && (rc = cached_workspace(reinterpret_cast<cudaStream_t>(stream), need, &ws))) return rc;
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, ws, need, reinterpret_cast<cudaStream_t>(stream),
+                   nullptr, 1);
 }
 
 int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
@@ -558,14 +598,14 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
     OZK_CUDA(cudaEventRecord(h.ev_in[0], h.in));
     OZK_CUDA(cudaStreamWaitEvent(cs, h.ev_in[0], 0));
     if (fuse_rows(M, L.kpad)) {
-      OZK_CUDA(launch_scan(0, N, K, nullptr, 0, dB, N, amax + M, cs));
-      OZK_CUDA(launch_quantize_rows(M, K, L.kpad, dA, K, n_moduli, beta, s, as, L.a_plane, cs));
-      OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, nullptr, amax + M, n_moduli, beta,
-                               nullptr, 0, bs, L.b_plane, cs));
+      OZK_CUDA(launch_scan(0, N, K, nullptr, 0, dB, N, amax + M, nullptr, cs));
+      OZK_CUDA(launch_quantize_rows(M, K, L.kpad, dA, K, n_moduli, beta, false, s, as, L.a_plane, cs));
+      OZK_CUDA(launch_quantize(0, N, K, L.kpad, nullptr, 0, dB, N, nullptr, t, nullptr, amax + M, nullptr, nullptr,
+                               n_moduli, beta, nullptr, 0, bs, L.b_plane, cs));
     } else {
-      OZK_CUDA(launch_scan(M, N, K, dA, K, dB, N, amax, cs));
-      OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, amax, amax + M, n_moduli, beta, as, L.a_plane,
-                               bs, L.b_plane, cs));
+      OZK_CUDA(launch_scan(M, N, K, dA, K, dB, N, amax, nullptr, cs));
+      OZK_CUDA(launch_quantize(M, N, K, L.kpad, dA, K, dB, N, s, t, amax, amax + M, nullptr, nullptr, n_moduli, beta,
+                               as, L.a_plane, bs, L.b_plane, cs));
     }
     OZK_CUDA(launch_residue_gemm(M, N, L.kpad, as, L.a_plane, bs, L.b_plane, n_moduli, L.kind, out, L.ldo,
                                  L.out_plane, L.splits, sms, cs));
@@ -639,12 +679,12 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
         r0 = blk * rows;
         mr = std::min(rows, M - r0);
         if (fuse_rows(mr, L.kpad)) {
-          OZK_CUDA(launch_quantize_rows(mr, K, L.kpad, dA + r0 * K, K, n_moduli, beta, s + r0,
+          OZK_CUDA(launch_quantize_rows(mr, K, L.kpad, dA + r0 * K, K, n_moduli, beta, false, s + r0,
                                         as + r0 * L.kpad, L.a_plane, cs));
         } else {
-          OZK_CUDA(launch_scan(mr, 0, K, dA + r0 * K, K, nullptr, 0, amax + r0, cs));
+          OZK_CUDA(launch_scan(mr, 0, K, dA + r0 * K, K, nullptr, 0, amax + r0, nullptr, cs));
           OZK_CUDA(launch_quantize(mr, 0, K, L.kpad, dA + r0 * K, K, nullptr, 0, s + r0, nullptr, amax + r0, nullptr,
-                                   n_moduli, beta,
+                                   nullptr, nullptr, n_moduli, beta,
                                    as + r0 * L.kpad, L.a_plane, nullptr, 0, cs));
         }
         rows_in = r0 + mr;
@@ -653,9 +693,9 @@ static int host_enqueue(int64_t M, int64_t N, int64_t K, const double* A, int64_
       } else {
         c0 = blk * cols;
         nc = std::min(cols, N - c0);
-        OZK_CUDA(launch_scan(0, nc, K, nullptr, 0, dB + c0, N, amax + M + c0, cs));
+        OZK_CUDA(launch_scan(0, nc, K, nullptr, 0, dB + c0, N, amax + M + c0, nullptr, cs));
         OZK_CUDA(launch_quantize(0, nc, K, L.kpad, nullptr, 0, dB + c0, N, nullptr, t + c0, nullptr, amax + M + c0,
-                                 n_moduli, beta, nullptr,
+                                 nullptr, nullptr, n_moduli, beta, nullptr,
                                  0, bs + c0 * L.kpad, L.b_plane, cs));
         cols_in = c0 + nc;
         r0 = 0;
@@ -769,7 +809,22 @@ int ozk_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, con
   if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;
   int rc = check_device(nullptr);
   if (rc) return rc;
-  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, scratch,
+  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, scratch, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream)));
+  return OZK_OK;
+}
+
+int ozk_scale_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                   int64_t ldb, int n_moduli, int32_t* s, int32_t* t, uint64_t* scratch, ozk_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return OZK_ERR_INVALID_ARG;
+  const int gamma = gamma_for(K, n_moduli);
+  if (gamma < 1 || K > OZK_MAX_K || M > kMaxDim || N > kMaxDim) return OZK_ERR_UNSUPPORTED;
+  if (M + N == 0) return OZK_OK;
+  if (!scratch || (M && !s) || (N && !t)) return OZK_ERR_INVALID_ARG;
+  if (K > 0 && ((M && (!A || lda < K)) || (N && (!B || ldb < N)))) return OZK_ERR_INVALID_ARG;
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  OZK_CUDA(launch_scale(M, N, K, A, lda, B, ldb, gamma, s, t, scratch, scratch + (M + N),
                         reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
@@ -785,8 +840,10 @@ int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda, const int
   if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
+  // integers wide enough for the scales of either rule (|a'| <= 2^gamma, gamma >= beta)
+  const int width = std::max(beta, gamma_for(K, n_moduli));
   OZK_CUDA(launch_quantize(M, 0, K, ozk_kpad(K), A, lda, nullptr, 0, const_cast<int32_t*>(s), nullptr, nullptr,
-                           nullptr, n_moduli, beta,
+                           nullptr, nullptr, nullptr, n_moduli, width,
                            a_slices, M * ozk_kpad(K), nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }
@@ -802,8 +859,9 @@ int ozk_quantize_b(int64_t K, int64_t N, const double* B, int64_t ldb, const int
   if (beta < 1) return OZK_ERR_UNSUPPORTED;
   int rc = check_device(nullptr);
   if (rc) return rc;
+  const int width = std::max(beta, gamma_for(K, n_moduli));
   OZK_CUDA(launch_quantize(0, N, K, ozk_kpad(K), nullptr, 0, B, ldb, nullptr, const_cast<int32_t*>(t), nullptr,
-                           nullptr, n_moduli, beta,
+                           nullptr, nullptr, nullptr, n_moduli, width,
                            nullptr, 0, b_slices, N * ozk_kpad(K), reinterpret_cast<cudaStream_t>(stream)));
   return OZK_OK;
 }

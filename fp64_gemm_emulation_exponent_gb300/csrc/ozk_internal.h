@@ -107,21 +107,24 @@ struct CrtConst {
 };
 
 // Host-side method constants (ozk_api.cu).
-int beta_for(int64_t K, int n);  // -1 when unsupported
+int beta_for(int64_t K, int n);   // -1 when unsupported
+int gamma_for(int64_t K, int n);  // the norm rule's budget; -1 when unsupported
 // OZK_OK when the current device is an sm_103 GPU (its SM count in *sms when not null).
 int current_device_supported(int* sms);
 const CrtConst& crt_const(int n);
 
 // Launchers; each returns the first CUDA error it meets.
 // Exponent scan: the abs-bit maxima of the rows of A and the columns of B
-// into amax[0..M) and amax[M..M+N) (zeroed first), then the scales s, t.
+// into amax[0..M) and amax[M..M+N) (zeroed first); with nsum not null also
+// the norm sums of the norm rule, nsum[0..M+N); then the scales s, t
+// (budget: beta of the largest-entry rule, or gamma of the norm rule).
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
-                         const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
-                         uint64_t* amax, cudaStream_t stream);
-// The scan alone (the maxima, no scales): launch_quantize then derives the
-// scales from the maxima and stores them.
+                         const double* B, int64_t ldb, int budget, int32_t* s, int32_t* t,
+                         uint64_t* amax, uint64_t* nsum, cudaStream_t stream);
+// The scan alone (maxima and, with nsum, norm sums; no scales):
+// launch_quantize then derives the scales and stores them.
 cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
-                        int64_t ldb, uint64_t* amax, cudaStream_t stream);
+                        int64_t ldb, uint64_t* amax, uint64_t* nsum, cudaStream_t stream);
 // Per-modulus planes (residue slices, residue or partial-sum planes) sit
 // `plane` elements apart; the workspace spaces them an odd number of 256-byte
 // units apart so that the n streams of a kernel do not fall on the same DRAM
@@ -129,18 +132,21 @@ cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_
 //
 // Quantises A (when A is not null) and B (when B is not null) in one launch;
 // slices and plane strides must be 32-byte aligned.  With a_amax (b_amax) not
-// null the scales are derived from the scanned maxima and stored in s (t);
-// otherwise s (t) are read.
+// null the scales are derived from the scanned maxima (and, with a_nsum
+// (b_nsum), the norm sums: the norm rule) and stored in s (t); otherwise
+// s (t) are read.  budget is beta, or gamma for the norm rule; it also sets
+// the integer width (|a'| <= 2^budget).
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
                             int64_t lda, const double* B, int64_t ldb, int32_t* s, int32_t* t,
-                            const uint64_t* a_amax, const uint64_t* b_amax, int n, int beta, uint16_t* a_out,
-                            int64_t a_plane, uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
+                            const uint64_t* a_amax, const uint64_t* b_amax, const uint64_t* a_nsum,
+                            const uint64_t* b_nsum, int n, int budget, uint16_t* a_out, int64_t a_plane,
+                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream);
 // Rows of A scanned and quantised in one pass (one block per row): writes
 // s[0..M) and A's slices as launch_scale + launch_quantize would.  Only for
 // K up to 4096 (quantize_rows_fits(kpad)); cudaErrorInvalidValue beyond.
 bool quantize_rows_fits(int64_t kpad);
 cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const double* A, int64_t lda, int n,
-                                 int beta, int32_t* s, uint16_t* a_out, int64_t a_plane,
+                                 int budget, bool norm, int32_t* s, uint16_t* a_out, int64_t a_plane,
                                  cudaStream_t stream);
 cudaError_t launch_residue_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_slices,
                                 int64_t a_plane, const uint16_t* b_slices, int64_t b_plane, int n,

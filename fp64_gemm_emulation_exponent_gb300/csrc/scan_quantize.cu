@@ -49,7 +49,50 @@ __device__ __forceinline__ uint64_t load1_u64(const double* p) {
 // segment), the rest scan columns of B (32 threads of 1 or 4 columns each, 8
 // row groups over a row segment, reduced in shared memory); partial maxima
 // meet in amax through 64-bit atomicMax.
+//
+// The norm pass (NORM, the scaling from a computed 2-norm bound) runs the
+// same walk once the maxima are in: every nonzero entry adds
+// 2^max(h - H + W, 0) with h = floor(2 log2 |x|) and H that of the row's
+// (column's) largest entry, an exact integer sum (at most 2^30 per entry,
+// 2^52 per row), gathered with 64-bit atomicAdd into nsum.  Integers only, so
+// the sum, and the scale derived from it, do not depend on the order.
 // ---------------------------------------------------------------------------
+constexpr int kNormWindow = 30;  // half-octaves below the largest entry that are counted exactly
+constexpr uint64_t kFracMask = (1ull << 52) - 1;
+// 1 + f / 2^52 >= sqrt(2) exactly when the 52 fraction bits f reach this value:
+// (2^52 + f)^2 >= 2^105, and 2^105 is not a square
+constexpr uint64_t kHalfOctaveFrac = 0x6A09E667F3BCDull;
+static_assert((static_cast<unsigned __int128>(kHalfOctaveFrac + (1ull << 52)) * (kHalfOctaveFrac + (1ull << 52)) >
+               (static_cast<unsigned __int128>(1) << 105)) &&
+                  (static_cast<unsigned __int128>(kHalfOctaveFrac - 1 + (1ull << 52)) *
+                       (kHalfOctaveFrac - 1 + (1ull << 52)) <
+                   (static_cast<unsigned __int128>(1) << 105)),
+              "the half-octave threshold is the first significand at or above sqrt(2)");
+
+// floor(2 log2 |x|) for the bit pattern b of a finite nonzero |x|: with
+// |x| = 1.f 2^e, 2e plus one when 1.f >= sqrt(2) (subnormals normalised first).
+__device__ __forceinline__ int half_octave(uint64_t b) {
+  const int ex = static_cast<int>(b >> 52);
+  int e;
+  uint64_t frac;
+  if (ex) {
+    e = ex - 1023;
+    frac = b & kFracMask;
+  } else {
+    const int lz = __clzll(static_cast<long long>(b));
+    e = (63 - lz) - 1074;
+    frac = (b << (lz - 11)) & kFracMask;
+  }
+  return 2 * e + (frac >= kHalfOctaveFrac ? 1 : 0);
+}
+
+// An entry's part of the norm sum, given H of its row's (column's) maximum.
+__device__ __forceinline__ uint64_t norm_part(uint64_t b, int H) {
+  if (b == 0) return 0;
+  const int d = half_octave(b) - H + kNormWindow;  // at most kNormWindow for a finite row
+  return 1ull << (d > 0 ? (d < 62 ? d : 62) : 0);  // (a row with Inf/NaN ignores its sum)
+}
+
 struct ScanParams {
   const double* A;
   const double* B;
@@ -58,14 +101,39 @@ struct ScanParams {
   int64_t b_seg, b_segs, b_cols;    // columns per block = 32 * b_cols, rows per block = b_seg
   int a_vec, b_vec;                 // 32-byte loads possible
   uint64_t* amax;                   // [M + N]
+  uint64_t* nsum;                   // [M + N], the norm pass only
 };
 
+// max of abs bit patterns, or (NORM) the sum of the entries' norm parts
+template <bool NORM>
+__device__ __forceinline__ uint64_t fold(uint64_t acc, uint64_t bits, int H) {
+  return NORM ? acc + norm_part(bits & kAbsMask, H) : umax64(acc, bits & kAbsMask);
+}
+
+template <bool NORM>
+__device__ __forceinline__ uint64_t warp_fold(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = NORM ? v + w : umax64(v, w);
+  }
+  return v;
+}
+
+// H of a row or column from its scanned maximum (unused for an all-zero or
+// non-finite one: their scale does not depend on the sum)
+__device__ __forceinline__ int max_half_octave(uint64_t amax) {
+  return (amax == 0 || amax >= kInfBits) ? 0 : half_octave(amax);
+}
+
+template <bool NORM>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp) {
   const int64_t bid = blockIdx.x;
   if (bid < sp.a_blocks) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (bid / sp.a_segs) * 8 + warp;
     if (row >= sp.M) return;
+    const int H = NORM ? max_half_octave(sp.amax[row]) : 0;
     const int64_t k0 = (bid % sp.a_segs) * sp.a_seg;
     const int64_t k1 = min(sp.K, k0 + sp.a_seg);
     const double* a = sp.A + row * sp.lda;
@@ -76,15 +144,21 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
       for (int64_t g = (k0 >> 2) + lane; g < g1; g += 32) {
         uint64_t v[4];
         load4_u64(a + 4 * g, v);
-        m = umax64(m, umax64(umax64(v[0] & kAbsMask, v[1] & kAbsMask), umax64(v[2] & kAbsMask, v[3] & kAbsMask)));
+        m = fold<NORM>(fold<NORM>(m, v[0], H), v[1], H);
+        m = fold<NORM>(fold<NORM>(m, v[2], H), v[3], H);
       }
-      for (int64_t k = (g1 << 2) + lane; k < k1; k += 32) m = umax64(m, load1_u64(a + k) & kAbsMask);
+      for (int64_t k = (g1 << 2) + lane; k < k1; k += 32) m = fold<NORM>(m, load1_u64(a + k), H);
     } else {
 #pragma unroll 4
-      for (int64_t k = k0 + lane; k < k1; k += 32) m = umax64(m, load1_u64(a + k) & kAbsMask);
+      for (int64_t k = k0 + lane; k < k1; k += 32) m = fold<NORM>(m, load1_u64(a + k), H);
     }
-    m = warp_max_u64(m);
-    if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + row), m);
+    m = warp_fold<NORM>(m);
+    if (lane == 0 && m) {
+      if (NORM)
+        atomicAdd(reinterpret_cast<unsigned long long*>(sp.nsum + row), m);
+      else
+        atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + row), m);
+    }
   } else {
     // A block of B: 32 column threads (b_cols columns each) x 8 row groups
     // over a row segment; the row groups meet in shared memory, so each
@@ -98,6 +172,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
     constexpr int kRowGroups = kScanThreads / 32;
     const int64_t c = (cgrp * 32 + lane) * sp.b_cols;
     uint64_t m[4] = {0, 0, 0, 0};
+    int H[4] = {0, 0, 0, 0};
+    if (NORM) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < sp.b_cols && c + j < sp.N) H[j] = max_half_octave(sp.amax[sp.M + c + j]);
+    }
     if (c < sp.N) {
       if (sp.b_vec && c + 3 < sp.N) {
 #pragma unroll 4
@@ -105,13 +185,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
           uint64_t v[4];
           load4_u64(sp.B + k * sp.ldb + c, v);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) m[j] = umax64(m[j], v[j] & kAbsMask);
+          for (int j = 0; j < 4; ++j) m[j] = fold<NORM>(m[j], v[j], H[j]);
         }
       } else {
         for (int j = 0; j < 4 && j < sp.b_cols && c + j < sp.N; ++j) {
 #pragma unroll 4
           for (int64_t k = k0 + rg; k < k1; k += kRowGroups)
-            m[j] = umax64(m[j], load1_u64(sp.B + k * sp.ldb + c + j) & kAbsMask);
+            m[j] = fold<NORM>(m[j], load1_u64(sp.B + k * sp.ldb + c + j), H[j]);
         }
       }
     }
@@ -123,9 +203,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
       for (int j = 0; j < 4; ++j) {
         uint64_t v = red[0][lane * 4 + j];
 #pragma unroll
-        for (int g = 1; g < kRowGroups; ++g) v = umax64(v, red[g][lane * 4 + j]);
-        if (v && j < sp.b_cols && c + j < sp.N)
-          atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + sp.M + c + j), v);
+        for (int g = 1; g < kRowGroups; ++g) v = NORM ? v + red[g][lane * 4 + j] : umax64(v, red[g][lane * 4 + j]);
+        if (v && j < sp.b_cols && c + j < sp.N) {
+          if (NORM)
+            atomicAdd(reinterpret_cast<unsigned long long*>(sp.nsum + sp.M + c + j), v);
+          else
+            atomicMax(reinterpret_cast<unsigned long long*>(sp.amax + sp.M + c + j), v);
+        }
       }
     }
   }
@@ -141,12 +225,29 @@ __device__ __forceinline__ int32_t scale_of_max(uint64_t b, int beta) {
   return beta - E;
 }
 
-__global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, int64_t M, int64_t N,
-                                       int beta, int32_t* __restrict__ s,
+// The scale of the norm rule from the row's (column's) maximum and norm sum S:
+// ||x||^2 < S 2^(H + 1 - W), and s = floor((2 gamma - (H + 1 - W) - ceil(log2 S)) / 2)
+// keeps 2^(2s) S 2^(H + 1 - W) <= 2^(2 gamma).
+__device__ __forceinline__ int32_t scale_of_norm(uint64_t amax, uint64_t S, int gamma) {
+  if (amax >= kInfBits) return OZK_SCALE_NONFINITE;
+  if (amax == 0) return 0;
+  const int H = half_octave(amax);
+  const int c = S <= 1 ? 0 : 64 - __clzll(static_cast<long long>(S - 1));  // ceil(log2 S)
+  const int num = 2 * gamma - (H + 1 - kNormWindow) - c;
+  return num >= 0 ? num / 2 : -((-num + 1) / 2);
+}
+
+// budget is beta (largest-entry rule) or, with nsum, gamma (norm rule)
+__device__ __forceinline__ int32_t scale_of(const uint64_t* amax, const uint64_t* nsum, int64_t idx, int budget) {
+  return nsum ? scale_of_norm(amax[idx], nsum[idx], budget) : scale_of_max(amax[idx], budget);
+}
+
+__global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, const uint64_t* __restrict__ nsum,
+                                       int64_t M, int64_t N, int budget, int32_t* __restrict__ s,
                                        int32_t* __restrict__ t) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= M + N) return;
-  const int32_t r = scale_of_max(amax[idx], beta);
+  const int32_t r = scale_of(amax, nsum, idx, budget);
   if (idx < M)
     s[idx] = r;
   else
@@ -286,7 +387,9 @@ struct QuantParams {
   int32_t* t;  // scales of the columns of B: read, or written when b_amax is set
   const uint64_t* a_amax;  // scanned maxima of the rows of A (the scale is derived here), or null
   const uint64_t* b_amax;  // the same for the columns of B
-  int beta;
+  const uint64_t* a_nsum;  // norm sums of the rows of A (the norm rule), or null (largest-entry rule)
+  const uint64_t* b_nsum;  // the same for the columns of B
+  int budget;              // beta, or gamma for the norm rule
   uint16_t* a_out;  // modulus k, row i at a_out + k * a_plane + i * kpad
   uint16_t* b_out;  // modulus k, column j at b_out + k * b_plane + j * kpad
   int64_t a_plane, b_plane;
@@ -321,7 +424,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
     plane = qp.a_plane;
     out = qp.a_out;
     if (qp.a_amax) {  // the scale from the row's scanned maximum; the first thread of the row stores it
-      sc = scale_of_max(qp.a_amax[row], qp.beta);
+      sc = scale_of(qp.a_amax, qp.a_nsum, row, qp.budget);
       if (k0 == 0) qp.s[row] = sc;
     } else {
       sc = qp.s[row];
@@ -354,7 +457,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
     plane = qp.b_plane;
     out = qp.b_out;
     if (qp.b_amax) {
-      sc = scale_of_max(qp.b_amax[row], qp.beta);
+      sc = scale_of(qp.b_amax, qp.b_nsum, row, qp.budget);
       if (k0 == 0) qp.t[row] = sc;
     } else {
       sc = qp.t[row];
@@ -392,8 +495,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams q
 constexpr int kRowsMaxThreads = 256;
 static_assert(kRowsMaxThreads % 32 == 0 && kRowsMaxThreads <= 1024, "whole warps");
 
-template <int NL>
-__global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const QuantParams qp, int beta,
+template <int NL, bool NORM>
+__global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const QuantParams qp, int budget,
                                                                         int32_t* __restrict__ s_out) {
   __shared__ uint64_t wmax[kRowsMaxThreads / 32];
   const int64_t row = blockIdx.x;
@@ -424,7 +527,23 @@ __global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const Qu
   __syncthreads();
   m = 0;
   for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = umax64(m, wmax[w]);
-  const int32_t sc = scale_of_max(m, beta);
+  int32_t sc;
+  if constexpr (NORM) {  // the row's norm sum, reduced the same way
+    const int H = max_half_octave(m);
+    uint64_t part = 0;
+#pragma unroll
+    for (int e = 0; e < kQK; ++e) part += norm_part(v[e] & kAbsMask, H);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    __syncthreads();  // every thread has read the maxima
+    if (lane == 0) wmax[warp] = part;
+    __syncthreads();
+    uint64_t S = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) S += wmax[w];
+    sc = scale_of_norm(m, S, budget);
+  } else {
+    sc = scale_of_max(m, budget);
+  }
   if (threadIdx.x == 0) s_out[row] = sc;
   if (!active) return;
   if (sc == OZK_SCALE_NONFINITE) {
@@ -451,10 +570,12 @@ __global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const Qu
 }  // namespace
 
 cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
-                        int64_t ldb, uint64_t* amax, cudaStream_t stream) {
+                        int64_t ldb, uint64_t* amax, uint64_t* nsum, cudaStream_t stream) {
   if (M + N == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint64_t) * static_cast<size_t>(M + N), stream);
   if (e != cudaSuccess) return e;
+  if (nsum && (e = cudaMemsetAsync(nsum, 0, sizeof(uint64_t) * static_cast<size_t>(M + N), stream)) != cudaSuccess)
+    return e;
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -468,6 +589,7 @@ cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_
   sp.N = N;
   sp.K = K;
   sp.amax = amax;
+  sp.nsum = nsum;
   sp.a_vec = (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
   sp.b_vec = (reinterpret_cast<uintptr_t>(B) % 32 == 0) && (ldb % 4 == 0);
   sp.a_seg = sp.a_segs = sp.a_blocks = 0;
@@ -494,26 +616,32 @@ cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_
   }
   const int64_t blocks = sp.a_blocks + b_blocks;
   if (blocks > 0) {
-    scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
+    scan_kernel<false><<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (nsum) {  // the norm pass, once every maximum is in
+      scan_kernel<true><<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }
 
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
-                         const double* B, int64_t ldb, int beta, int32_t* s, int32_t* t,
-                         uint64_t* amax, cudaStream_t stream) {
+                         const double* B, int64_t ldb, int budget, int32_t* s, int32_t* t,
+                         uint64_t* amax, uint64_t* nsum, cudaStream_t stream) {
   if (M + N == 0) return cudaSuccess;
-  cudaError_t e = launch_scan(M, N, K, A, lda, B, ldb, amax, stream);
+  cudaError_t e = launch_scan(M, N, K, A, lda, B, ldb, amax, nsum, stream);
   if (e != cudaSuccess) return e;
-  finalize_scales_kernel<<<static_cast<unsigned>((M + N + 255) / 256), 256, 0, stream>>>(amax, M, N, beta, s, t);
+  finalize_scales_kernel<<<static_cast<unsigned>((M + N + 255) / 256), 256, 0, stream>>>(amax, nsum, M, N, budget,
+                                                                                          s, t);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
                             int64_t lda, const double* B, int64_t ldb, int32_t* s, int32_t* t,
-                            const uint64_t* a_amax, const uint64_t* b_amax, int n, int beta, uint16_t* a_out,
-                            int64_t a_plane, uint16_t* b_out, int64_t b_plane, cudaStream_t stream) {
+                            const uint64_t* a_amax, const uint64_t* b_amax, const uint64_t* a_nsum,
+                            const uint64_t* b_nsum, int n, int budget, uint16_t* a_out, int64_t a_plane,
+                            uint16_t* b_out, int64_t b_plane, cudaStream_t stream) {
   if (kpad == 0 || (M == 0 && N == 0)) return cudaSuccess;
   QuantParams qp;
   qp.A = A;
@@ -522,7 +650,9 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   qp.t = t;
   qp.a_amax = a_amax;
   qp.b_amax = b_amax;
-  qp.beta = beta;
+  qp.a_nsum = a_nsum;
+  qp.b_nsum = b_nsum;
+  qp.budget = budget;
   qp.a_out = a_out;
   qp.b_out = b_out;
   qp.a_plane = a_plane;
@@ -543,11 +673,11 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   const int64_t threads = qp.a_span + qp.b_threads;
   if (threads == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((threads + kQThreads - 1) / kQThreads);
-  // |a'| <= 2^beta: one 64-bit word for beta <= 62, three 22-bit limbs of
-  // two's complement for beta <= 64, four beyond
-  if (beta <= 62)
+  // |a'| <= 2^budget: one 64-bit word for a budget of at most 62, three
+  // 22-bit limbs of two's complement up to 64, four beyond
+  if (budget <= 62)
     quantize_kernel<2><<<blocks, kQThreads, 0, stream>>>(qp);
-  else if (beta <= 64)
+  else if (budget <= 64)
     quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
   else
     quantize_kernel<4><<<blocks, kQThreads, 0, stream>>>(qp);
@@ -557,7 +687,7 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
 bool quantize_rows_fits(int64_t kpad) { return kpad / kQK <= kRowsMaxThreads; }
 
 cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const double* A, int64_t lda, int n,
-                                 int beta, int32_t* s, uint16_t* a_out, int64_t a_plane,
+                                 int budget, bool norm, int32_t* s, uint16_t* a_out, int64_t a_plane,
                                  cudaStream_t stream) {
   if (M == 0 || kpad == 0) return cudaSuccess;
   if (!quantize_rows_fits(kpad) || M > 0x7FFFFFFF) return cudaErrorInvalidValue;
@@ -573,12 +703,20 @@ cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const doubl
   qp.a_vec = (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
   const unsigned threads = static_cast<unsigned>((kpad / kQK + 31) / 32 * 32);
   const unsigned blocks = static_cast<unsigned>(M);
-  if (beta <= 62)
-    quantize_rows_kernel<2><<<blocks, threads, 0, stream>>>(qp, beta, s);
-  else if (beta <= 64)
-    quantize_rows_kernel<3><<<blocks, threads, 0, stream>>>(qp, beta, s);
+#define OZK_ROWS_LAUNCH(NL)                                                    \
+  do {                                                                         \
+    if (norm)                                                                  \
+      quantize_rows_kernel<NL, true><<<blocks, threads, 0, stream>>>(qp, budget, s);  \
+    else                                                                       \
+      quantize_rows_kernel<NL, false><<<blocks, threads, 0, stream>>>(qp, budget, s); \
+  } while (0)
+  if (budget <= 62)
+    OZK_ROWS_LAUNCH(2);
+  else if (budget <= 64)
+    OZK_ROWS_LAUNCH(3);
   else
-    quantize_rows_kernel<4><<<blocks, threads, 0, stream>>>(qp, beta, s);
+    OZK_ROWS_LAUNCH(4);
+#undef OZK_ROWS_LAUNCH
   return cudaGetLastError();
 }
 
@@ -641,7 +779,7 @@ extern "C" int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* 
   if ((rc = noalloc_scratch(&amax))) return rc;
   // launch_scale zeroes the M + N maxima it uses before the scan, so the
   // contents left by an earlier call do not matter
-  if (launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, reinterpret_cast<cudaStream_t>(stream)) !=
+  if (launch_scale(M, N, K, A, lda, B, ldb, beta, s, t, amax, nullptr, reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return OZK_ERR_CUDA;
   return OZK_OK;

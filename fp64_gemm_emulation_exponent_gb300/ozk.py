@@ -35,6 +35,10 @@ SIGNATURES = {
     "ozk_moduli": (_i32, [_i32, _vp]),
     "ozk_beta": (_i32, [_i64, _i32]),
     "ozk_kpad": (_i64, [_i64]),
+    "ozk_gamma": (_i32, [_i64, _i32]),
+    "ozk_dgemm_norm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
+    "ozk_dgemm_norm_ws": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp]),
+    "ozk_scale_norm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
     "ozk_moduli_for_bits": (_i32, [_i64, _i32]),
     "ozk_dgemm_bits": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
@@ -177,9 +181,10 @@ def ozk_release_cached():
     return _call("ozk_release_cached")
 
 
-def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None):
+def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None, scaling="max"):
     """C = A @ B for float64 CUDA tensors through ozk_dgemm (or ozk_dgemm_bits
-    when target_bits is given: the moduli count then follows from K)."""
+    when target_bits is given: the moduli count then follows from K; or
+    ozk_dgemm_norm with scaling="norm": scales from the rows' 2-norms)."""
     import torch
 
     M, K = A.shape
@@ -188,7 +193,13 @@ def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None):
         raise ValueError("inner dimensions differ")
     if out is None:
         out = torch.empty((M, N), dtype=torch.float64, device=A.device)
-    if target_bits is None:
+    if scaling == "norm":
+        if target_bits is not None:
+            raise ValueError("target_bits picks the count of the largest-entry rule")
+        ozk_dgemm_norm(M, N, K, A, _ld(A), B, _ld(B), out, _ld(out), n_moduli, stream)
+    elif scaling != "max":
+        raise ValueError(f"unknown scaling {scaling!r}")
+    elif target_bits is None:
         ozk_dgemm(M, N, K, A, _ld(A), B, _ld(B), out, _ld(out), n_moduli, stream)
     else:
         _call("ozk_dgemm_bits", M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(out), _ld(out), target_bits,
@@ -199,6 +210,24 @@ def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None):
 # ---------------------------------------------------------------- stages
 def ozk_scale(M, N, K, A, lda, B, ldb, n_moduli, s, t, scratch, stream=None):
     return _call("ozk_scale", M, N, K, _ptr(A), lda, _ptr(B), ldb, n_moduli, _ptr(s), _ptr(t), _ptr(scratch),
+                 _stream(stream))
+
+
+def ozk_gamma(K: int, n_moduli: int) -> int:
+    return lib().ozk_gamma(K, n_moduli)
+
+
+def ozk_dgemm_norm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, stream=None):
+    return _call("ozk_dgemm_norm", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli, _stream(stream))
+
+
+def ozk_dgemm_norm_ws(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes, stream=None):
+    return _call("ozk_dgemm_norm_ws", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli, _ptr(workspace),
+                 workspace_bytes, _stream(stream))
+
+
+def ozk_scale_norm(M, N, K, A, lda, B, ldb, n_moduli, s, t, scratch, stream=None):
+    return _call("ozk_scale_norm", M, N, K, _ptr(A), lda, _ptr(B), ldb, n_moduli, _ptr(s), _ptr(t), _ptr(scratch),
                  _stream(stream))
 
 

@@ -81,6 +81,13 @@ int ozk_beta(int64_t K, int n_moduli);
  * target_bits < 1, or -OZK_ERR_UNSUPPORTED when 20 moduli do not reach it. */
 int ozk_moduli_for_bits(int64_t K, int target_bits);
 
+/* Norm budget gamma of the norm scaling rule (ozk_dgemm_norm):
+ * floor((floor(log2 P) - 2) / 2), so that two scaled vectors of 2-norm at
+ * most 2^gamma (plus the rounding slack sqrt(K)/2, required to stay below
+ * 2^(gamma - 3)) keep the symmetric CRT lift of their dot product exact.
+ * Returns gamma, or -OZK_ERR_UNSUPPORTED. */
+int ozk_gamma(int64_t K, int n_moduli);
+
 /* Row length of the residue slices: K rounded up to a multiple of 64. */
 int64_t ozk_kpad(int64_t K);
 
@@ -130,6 +137,29 @@ int ozk_dgemm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A,
                        int64_t ldc, int n_moduli, void* workspace,
                        size_t workspace_bytes, ozk_stream_t stream,
                        ozk_event_t* events);
+
+/* ozk_dgemm with the sharper scaling rule: the scale of row i of A is the
+ * largest s_i with 2^s_i ||a_i||_2 <= 2^gamma (ozk_gamma), from an exactly
+ * computed bound on the row's 2-norm (ozk_scale_norm), and likewise t_j for
+ * the columns of B.  By Cauchy-Schwarz, sum_k |a'_ik||b'_kj| <=
+ * ||a'_i|| ||b'_j|| then stays below P/2, so the method is as exact as with
+ * the largest-entry rule while each operand keeps more bits wherever a row's
+ * entries are not all near its largest (about 1.2 more bits per operand for
+ * Gaussian data at K = 4096); the same precision contract can then be met
+ * with fewer moduli.  The pages' precision-contract list (the "Day 12" page,
+ * section "先定義公平比較") sets moduli count against target bits; this rule
+ * is the library's reading of its "sharper scaling" step, not the pages'.
+ * Costs one more pass over the operands whose rows are scanned separately (B,
+ * and A when its rows are longer than 4096).  Same arguments, workspace and
+ * errors as ozk_dgemm / ozk_dgemm_ws; OZK_ERR_UNSUPPORTED when ozk_gamma
+ * rejects K. */
+int ozk_dgemm_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                   const double* B, int64_t ldb, double* C, int64_t ldc,
+                   int n_moduli, ozk_stream_t stream);
+int ozk_dgemm_norm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                      const double* B, int64_t ldb, double* C, int64_t ldc,
+                      int n_moduli, void* workspace, size_t workspace_bytes,
+                      ozk_stream_t stream);
 
 /* C = A * B for HOST matrices (pinned memory gives the fastest copies and
  * the overlap).  A goes to the device in row blocks and B in column blocks
@@ -210,6 +240,17 @@ int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* A, int64_t 
                       const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
                       ozk_stream_t stream);
 
+/* The scales of the norm rule: with H_i = max_k floor(2 log2 |a_ik|) and
+ * S_i = sum over the nonzero entries of 2^max(floor(2 log2 |a_ik|) - H_i + 30, 0)
+ * (an exact integer, the same for any summation order; ||a_i||_2^2 <
+ * S_i 2^(H_i - 29)), s_i = floor((2 gamma - (H_i - 29) - ceil(log2 S_i)) / 2);
+ * t_j likewise over the columns of B.  0 for an all-zero row/column,
+ * OZK_SCALE_NONFINITE when it holds an Inf or NaN.  scratch: 2 (M + N)
+ * uint64 of device scratch memory, overwritten. */
+int ozk_scale_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                   const double* B, int64_t ldb, int n_moduli, int32_t* s, int32_t* t,
+                   uint64_t* scratch, ozk_stream_t stream);
+
 /* Residue quantisation of A ("double load, exponent scaling, round, mod,
  * balanced int8 conversion").  For each modulus p and element:
  * a'_ik = a_ik 2^s_i rounded to the nearest integer (ties to even) and
@@ -217,7 +258,8 @@ int ozk_scale_noalloc(int64_t M, int64_t N, int64_t K, const double* A, int64_t 
  * stored as IEEE binary16 (fp16; exact for these integers) at
  * a_slices[(p * M + i) * kpad + k]; columns K..kpad-1 are zero.
  * kpad = ozk_kpad(K); a_slices must be 32-byte aligned.  Rows with
- * s_i = OZK_SCALE_NONFINITE are zero.  Returns OZK_ERR_UNSUPPORTED when
+ * s_i = OZK_SCALE_NONFINITE are zero.  The scales may come from ozk_scale or
+ * ozk_scale_norm.  Returns OZK_ERR_UNSUPPORTED when
  * ozk_beta(K, n_moduli) < 1. */
 int ozk_quantize_a(int64_t M, int64_t K, const double* A, int64_t lda,
                    const int32_t* s, int n_moduli, uint16_t* a_slices,

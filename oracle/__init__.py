@@ -40,6 +40,10 @@ def lib():
             "ozk_ref_dot2": [i64, i64, i64, vp, i64, vp, i64, vp],
             "ozk_ref_dot2_sample": [i64, vp, i64, vp, i64, i64, vp, vp, vp, vp],
             "ozk_ref_threads": [],
+            "ozk_ref_gamma": [i64, i32],
+            "ozk_ref_scale_norm": [i64, i64, i64, vp, i64, vp, i64, i32, vp, vp],
+            "ozk_ref_dgemm_norm": [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32],
+            "ozk_ref_sample_norm": [i64, i64, i64, vp, i64, vp, i64, i32, i64, vp, vp, vp, vp, vp, vp],
         }
         for name, args in sigs.items():
             f = getattr(L, name)
@@ -81,15 +85,23 @@ def beta(K, n):
     return _check(lib().ozk_ref_beta(K, n), "beta")
 
 
-def scale(A, B, n):
+def scale(A, B, n, rule="max"):
+    """Row and column scales: rule "max" (the largest entry, reading R2) or
+    "norm" (the computed 2-norm bound, reading R15)."""
     A, B = _f64(A), _f64(B)
     M, K = A.shape
     K2, N = B.shape
     assert K == K2
     s = np.zeros(M, dtype=np.int32)
     t = np.zeros(N, dtype=np.int32)
-    _check(lib().ozk_ref_scale(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, n, _p(s), _p(t)), "scale")
+    f = lib().ozk_ref_scale_norm if rule == "norm" else lib().ozk_ref_scale
+    _check(f(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, n, _p(s), _p(t)), "scale")
     return s, t
+
+
+def gamma(K, n):
+    """Norm budget per operand of the "norm" rule; raises OracleError when unsupported."""
+    return _check(lib().ozk_ref_gamma(K, n), "gamma")
 
 
 def integers(X, sc, by_row):
@@ -150,17 +162,18 @@ def round_scaled(X, S):
     return out
 
 
-def dgemm(A, B, n):
+def dgemm(A, B, n, rule="max"):
     """The whole method on the CPU.  Raises if the CRT check fails anywhere."""
     A, B = _f64(A), _f64(B)
     M, K = A.shape
     _, N = B.shape
     C = np.zeros((M, N), dtype=np.float64)
-    _check(lib().ozk_ref_dgemm(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, _p(C), N, n), "dgemm")
+    f = lib().ozk_ref_dgemm_norm if rule == "norm" else lib().ozk_ref_dgemm
+    _check(f(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, _p(C), N, n), "dgemm")
     return C
 
 
-def sample(A, B, n, ii, jj):
+def sample(A, B, n, ii, jj, rule="max"):
     """Method at chosen outputs: returns (C, raw n-per-pair, cmod n-per-pair, X limbs)."""
     A, B = _f64(A), _f64(B)
     M, K = A.shape
@@ -172,8 +185,9 @@ def sample(A, B, n, ii, jj):
     raw = np.zeros((q, n), dtype=np.int32)
     cmod = np.zeros((q, n), dtype=np.uint8)
     X = np.zeros((q, LIMBS), dtype=np.uint32)
-    _check(lib().ozk_ref_sample(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, n, q,
-                                _p(ii), _p(jj), _p(C), _p(raw), _p(cmod), _p(X)), "sample")
+    f = lib().ozk_ref_sample_norm if rule == "norm" else lib().ozk_ref_sample
+    _check(f(M, N, K, _p(A), A.strides[0] // 8, _p(B), B.strides[0] // 8, n, q,
+             _p(ii), _p(jj), _p(C), _p(raw), _p(cmod), _p(X)), "sample")
     return C, raw, cmod, X
 
 

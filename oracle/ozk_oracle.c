@@ -187,6 +187,80 @@ int ozk_ref_scale(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Step 1, sharper: scaling from a computed norm bound (reading R15).        */
+/* By Cauchy-Schwarz, sum_k |a'_ik||b'_kj| <= ||a'_i||_2 ||b'_j||_2, so it is */
+/* enough that every scaled row of A and column of B has 2-norm at most      */
+/* 2^gamma (plus the rounding slack), instead of every entry being below     */
+/* 2^beta with K entries at the bound.  The norm bound is computed exactly   */
+/* (integers only, so any summation order gives the same scales):           */
+/*   h(x) = floor(2 log2 |x|), so x^2 < 2^(h(x) + 1);                        */
+/*   H = max h over the row, W = OZK_REF_NORM_WINDOW;                        */
+/*   S = sum over the nonzero entries of 2^max(h - H + W, 0), an integer;    */
+/*   then ||x||^2 < S 2^(H + 1 - W), and                                     */
+/*   s = floor((2 gamma - (H + 1 - W) - ceil(log2 S)) / 2)                   */
+/* keeps 2^(2s) S 2^(H + 1 - W) <= 2^(2 gamma).                              */
+/* ------------------------------------------------------------------------- */
+
+/* gamma = floor((floor(log2 P) - 2) / 2), usable when sqrt(K) <= 2^(gamma - 2):
+ * then |a'_ik| <= 2^s |a_ik| + 1/2 gives ||a'_i|| <= 2^gamma + sqrt(K)/2
+ * <= 2^gamma (1 + 1/8), and 2 ||a'_i|| ||b'_j|| <= 2 (81/64) 2^(2 gamma)
+ * <= (81/128) 2^floor(log2 P) < P: the symmetric lift stays exact. */
+int ozk_ref_gamma(int64_t K, int n) {
+  if (n < 2 || n > OZK_REF_NMAX) return OZK_REF_EUNSUPPORTED;
+  if (K < 1) K = 1;
+  bigi P;
+  big_product_of_moduli(&P, n);
+  int gamma = (big_msb(&P) - 2) / 2;
+  if (gamma < 1 || ceil_log2_i64(K) > 2 * gamma - 4) return OZK_REF_EUNSUPPORTED;
+  return gamma;
+}
+
+/* floor(2 log2 |x|) for finite nonzero x: |x| = f 2^E with f in [0.5, 1), so
+ * 2 log2 |x| = 2 (E - 1) + 2 log2(2f), and 2 log2(2f) >= 1 exactly when
+ * (2f)^2 >= 2, i.e. m^2 >= 2^105 for the integer significand m = f 2^53. */
+static int half_octave(double x) {
+  int E;
+  double f = frexp(fabs(x), &E);
+  uint64_t m = (uint64_t)ldexp(f, 53);
+  unsigned __int128 mm = (unsigned __int128)m * m;
+  return 2 * (E - 1) + (mm >= ((unsigned __int128)1 << 105) ? 1 : 0);
+}
+
+static int32_t scale_norm_of(const double* x, int64_t len, int64_t stride, int gamma) {
+  int H = INT32_MIN;
+  for (int64_t k = 0; k < len; ++k) {
+    double v = x[k * stride];
+    if (!isfinite(v)) return OZK_REF_NONFINITE;
+    if (v != 0.0) {
+      int h = half_octave(v);
+      if (h > H) H = h;
+    }
+  }
+  if (H == INT32_MIN) return 0; /* an all-zero row or column */
+  uint64_t S = 0;
+  for (int64_t k = 0; k < len; ++k) {
+    double v = x[k * stride];
+    if (v == 0.0) continue;
+    int d = half_octave(v) - H + OZK_REF_NORM_WINDOW;
+    S += (uint64_t)1 << (d > 0 ? d : 0);
+  }
+  int c = 0; /* ceil(log2 S) */
+  while (((uint64_t)1 << c) < S) ++c;
+  int num = 2 * gamma - (H + 1 - OZK_REF_NORM_WINDOW) - c;
+  return num >= 0 ? num / 2 : -((-num + 1) / 2);
+}
+
+int ozk_ref_scale_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, int n, int32_t* s, int32_t* t) {
+  if (M < 0 || N < 0 || K < 0) return OZK_REF_EINVAL;
+  int gamma = ozk_ref_gamma(K, n);
+  if (gamma < 0) return gamma;
+  for (int64_t i = 0; i < M; ++i) s[i] = scale_norm_of(A + i * lda, K, 1, gamma);
+  for (int64_t j = 0; j < N; ++j) t[j] = scale_norm_of(B + j, K, ldb, gamma);
+  return OZK_REF_OK;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Step 2: exponent scaling and rounding to integers ("exponent scaling,     */
 /* round"; reading: to nearest, ties to even)                                */
 /* ------------------------------------------------------------------------- */
@@ -365,11 +439,13 @@ int ozk_ref_round(int64_t count, const uint32_t* X, const int32_t* S, double* ou
 /* ------------------------------------------------------------------------- */
 /* The whole method                                                          */
 /* ------------------------------------------------------------------------- */
-int ozk_ref_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
-                  const double* B, int64_t ldb, double* C, int64_t ldc, int n) {
+/* rule 0: the scales of reading R2 (ozk_ref_scale); rule 1: those of the
+ * computed norm bound, reading R15 (ozk_ref_scale_norm). */
+static int dgemm_rule(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                      const double* B, int64_t ldb, double* C, int64_t ldc, int n, int rule) {
   if (M < 0 || N < 0 || K < 0) return OZK_REF_EINVAL;
-  int beta = ozk_ref_beta(K, n);
-  if (beta < 0) return beta;
+  int budget = rule ? ozk_ref_gamma(K, n) : ozk_ref_beta(K, n);
+  if (budget < 0) return budget;
   if (M == 0 || N == 0) return OZK_REF_OK;
   int32_t* s = malloc(sizeof(int32_t) * (size_t)M);
   int32_t* t = malloc(sizeof(int32_t) * (size_t)N);
@@ -382,7 +458,10 @@ int ozk_ref_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
     err = OZK_REF_EINVAL;
     goto done;
   }
-  ozk_ref_scale(M, N, K, A, lda, B, ldb, n, s, t);
+  if (rule)
+    ozk_ref_scale_norm(M, N, K, A, lda, B, ldb, n, s, t);
+  else
+    ozk_ref_scale(M, N, K, A, lda, B, ldb, n, s, t);
   ozk_ref_integers(M, K, A, lda, s, 1, Ap);
   for (int64_t j = 0; j < N; ++j)
     for (int64_t q = 0; q < K; ++q) Bt[j * K + q] = round_scaled_int(B[q * ldb + j], t[j]);
@@ -429,13 +508,23 @@ done:
   return err;
 }
 
-int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
-                   const double* B, int64_t ldb, int n, int64_t npairs,
-                   const int64_t* ii, const int64_t* jj, double* C, int32_t* raw,
-                   uint8_t* cmod, uint32_t* X) {
+int ozk_ref_dgemm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                  const double* B, int64_t ldb, double* C, int64_t ldc, int n) {
+  return dgemm_rule(M, N, K, A, lda, B, ldb, C, ldc, n, 0);
+}
+
+int ozk_ref_dgemm_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, double* C, int64_t ldc, int n) {
+  return dgemm_rule(M, N, K, A, lda, B, ldb, C, ldc, n, 1);
+}
+
+static int sample_rule(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, int n, int64_t npairs,
+                       const int64_t* ii, const int64_t* jj, double* C, int32_t* raw,
+                       uint8_t* cmod, uint32_t* X, int rule) {
   if (M < 0 || N < 0 || K < 0 || npairs < 0) return OZK_REF_EINVAL;
-  int beta = ozk_ref_beta(K, n);
-  if (beta < 0) return beta;
+  int budget = rule ? ozk_ref_gamma(K, n) : ozk_ref_beta(K, n);
+  if (budget < 0) return budget;
   for (int64_t q = 0; q < npairs; ++q)
     if (ii[q] < 0 || ii[q] >= M || jj[q] < 0 || jj[q] >= N) return OZK_REF_EINVAL;
   int err = OZK_REF_OK;
@@ -443,8 +532,8 @@ int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
   for (int64_t q = 0; q < npairs; ++q) {
     const double* arow = A + ii[q] * lda;
     const double* bcol = B + jj[q];
-    int32_t si = scale_of(arow, K, 1, beta);
-    int32_t tj = scale_of(bcol, K, ldb, beta);
+    int32_t si = rule ? scale_norm_of(arow, K, 1, budget) : scale_of(arow, K, 1, budget);
+    int32_t tj = rule ? scale_norm_of(bcol, K, ldb, budget) : scale_of(bcol, K, ldb, budget);
     int64_t acc[OZK_REF_NMAX] = {0};
     bigi xd, prod, xc;
     big_set_u32(&xd, 0);
@@ -480,6 +569,20 @@ int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda
       C[q] = round_scaled(&xc, si + tj);
   }
   return err;
+}
+
+int ozk_ref_sample(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                   const double* B, int64_t ldb, int n, int64_t npairs,
+                   const int64_t* ii, const int64_t* jj, double* C, int32_t* raw,
+                   uint8_t* cmod, uint32_t* X) {
+  return sample_rule(M, N, K, A, lda, B, ldb, n, npairs, ii, jj, C, raw, cmod, X, 0);
+}
+
+int ozk_ref_sample_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                        const double* B, int64_t ldb, int n, int64_t npairs,
+                        const int64_t* ii, const int64_t* jj, double* C, int32_t* raw,
+                        uint8_t* cmod, uint32_t* X) {
+  return sample_rule(M, N, K, A, lda, B, ldb, n, npairs, ii, jj, C, raw, cmod, X, 1);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -104,6 +104,30 @@ int ozk_ref_dot2_sample(int64_t K, const double* A, int64_t lda, const double* B
                         int64_t ldb, int64_t npairs, const int64_t* ii,
                         const int64_t* jj, double* R, double* absAB);
 
+/* Sharper scaling from a computed norm bound (reading R15; the survey's
+ * "sharper scaling" next step).  gamma = floor((floor(log2 P) - 2) / 2), or
+ * OZK_REF_EUNSUPPORTED when sqrt(K) > 2^(gamma - 2). */
+#define OZK_REF_NORM_WINDOW 30 /* half-octaves below a row's largest entry counted exactly */
+int ozk_ref_gamma(int64_t K, int n);
+
+/* s[i] = floor((2 gamma - (H_i + 1 - W) - ceil(log2 S_i)) / 2) with
+ * H_i = max_k floor(2 log2 |a_ik|) over the nonzero entries of row i,
+ * S_i = sum over them of 2^max(floor(2 log2 |a_ik|) - H_i + W, 0) (an exact
+ * integer, W = OZK_REF_NORM_WINDOW), so that 2^s_i ||a_i||_2 < 2^gamma; t[j]
+ * likewise over the columns of B.  0 for an all-zero row/column, NONFINITE
+ * for one holding Inf/NaN. */
+int ozk_ref_scale_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, int n, int32_t* s, int32_t* t);
+
+/* ozk_ref_dgemm and ozk_ref_sample with the scales of ozk_ref_scale_norm;
+ * every other step is the same. */
+int ozk_ref_dgemm_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                       const double* B, int64_t ldb, double* C, int64_t ldc, int n);
+int ozk_ref_sample_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                        const double* B, int64_t ldb, int n, int64_t npairs,
+                        const int64_t* ii, const int64_t* jj, double* C, int32_t* raw,
+                        uint8_t* cmod, uint32_t* X);
+
 /* Threads OpenMP will use (for reporting). */
 int ozk_ref_threads(void);
 

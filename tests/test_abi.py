@@ -79,6 +79,16 @@ def test_moduli_for_bits_is_the_smallest_count_reaching_the_target():
     assert ozk.ozk_moduli_for_bits(4096, 0) == -ozk.OZK_ERR_INVALID_ARG
 
 
+def test_gamma_matches_the_oracle():
+    for n in range(2, 21):
+        for K in [1, 2, 63, 64, 1000, 4096, 65536, 131072, 10**6, 4194304]:
+            try:
+                want = oracle.gamma(K, n)
+            except oracle.OracleError:
+                want = -ozk.OZK_ERR_UNSUPPORTED
+            assert ozk.ozk_gamma(K, n) == want, (K, n)
+
+
 def test_kpad():
     assert [ozk.ozk_kpad(k) for k in [0, 1, 63, 64, 65, 128, 131071]] == [0, 64, 64, 64, 128, 128, 131072]
 

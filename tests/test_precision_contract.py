@@ -78,3 +78,47 @@ def test_precision_contract(name, n):
         verdict = "a-priori bound"
     print(f"\nPRECISION | {name} | {w.M}x{w.N}x{w.K} | {n} | {LABEL.get(n, '-')} | {beta} | {ii.size} | "
           f"{float(err.max()):.3e} | {max_rel:.3e} | {rms:.3e} | {eta:.3e} | {verdict} |")
+
+
+# The sharper scaling rule (scales from each row's and column's 2-norm bound,
+# ozk_dgemm_norm): the same contract with fewer moduli where the rows' entries
+# spread below their largest (Gaussian data), none lost where they do not
+# (uniform).  13 moduli meet eta <= 1e-14 at 4096^3 with it.
+NORM_CASES = [("square1024_wide", 13), ("square1024_wide", 14), ("square4096_normal", 13),
+              ("square4096_normal", 14), ("square8192_uniform", 13), ("wide8192_k512", 13),
+              ("tall512_k65536", 13)]
+
+
+@pytest.mark.parametrize("name,n", NORM_CASES)
+def test_precision_contract_norm_rule(name, n):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.workload_operands(w)
+    dA, dB = dev(A), dev(B)
+    C = ozk.dgemm(dA, dB, n, scaling="norm")
+    torch.cuda.synchronize()
+    assert ozk.ozk_stream_status() == 0
+    ii, jj = outputs(w, 2048 if w.K <= 8192 else 512, seed=17 * n)
+    Cg = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().numpy()
+    del dA, dB, C
+    torch.cuda.empty_cache()
+    R, absAB = oracle.dot2_sample(A, B, ii, jj)
+    err = np.abs(Cg - R)
+    eta = float(np.max(err / absAB))
+    nz = R != 0
+    max_rel = float(np.max(err[nz] / np.abs(R[nz])))
+    rms = float(np.sqrt(np.mean(err**2)))
+    gamma = ozk.ozk_gamma(w.K, n)
+    if name == "square1024_wide" and n == 13:
+        # the wide-range rows keep too few bits for 1e-14 at 13 moduli: the
+        # a-priori bound of rounding the operands, with the norm rule's scales
+        s, t = oracle.scale(A, B, n, rule="norm")
+        s, t = s[ii].astype(np.int64), t[jj].astype(np.int64)
+        bound = (np.abs(A).sum(1)[ii] * np.ldexp(1.0, -t - 1) + np.ldexp(1.0, -s - 1) * np.abs(B).sum(0)[jj]
+                 + w.K * np.ldexp(1.0, -(s + t + 2)))
+        assert np.all(err <= bound * (1 + 1e-12) + np.spacing(np.abs(Cg)))
+        verdict = "a-priori bound"
+    else:
+        assert eta <= 1e-14
+        verdict = "eta <= 1e-14"
+    print(f"\nPRECISION-NORM | {name} | {w.M}x{w.N}x{w.K} | {n} | gamma {gamma} | {ii.size} | "
+          f"{float(err.max()):.3e} | {max_rel:.3e} | {rms:.3e} | {eta:.3e} | {verdict} |")
