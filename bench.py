@@ -358,6 +358,40 @@ def run_gpu(args, ranks: Ranks):
     if ozk.ozk_stream_status(stream) != 0:
         raise RuntimeError("device status after the end-to-end runs")
 
+    # the same workload with the sharper (norm) scaling rule at the moduli count
+    # it needs for the same contract: at 4096^3 N(0,1), 13 moduli keep
+    # eta <= 1e-14 (tests/test_precision_contract.py asserts it)
+    norm_rule = None
+    if not args.no_norm_rule and ozk.ozk_gamma(K, args.norm_moduli) > 0:
+        nn = args.norm_moduli
+        need_n = ozk.ozk_workspace_size(M, N, K, nn)
+        ws_n = torch.empty(need_n, dtype=torch.uint8, device="cuda")
+
+        def step_norm(ev=None):
+            ozk.ozk_dgemm_norm_ws_timed(M, N, K, dA, K, dB, N, dC, N, nn, ws_n, need_n, ev, stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step_norm()
+        torch.cuda.synchronize()
+        ev_n = [[ozk.Event() for _ in range(5)] for _ in range(args.steps)]
+        n0, n1 = ozk.Event(), ozk.Event()
+        ranks.barrier()
+        torch.cuda.synchronize()
+        n0.record(stream)
+        for k in range(args.steps):
+            step_norm(ev_n[k])
+        n1.record(stream)
+        torch.cuda.synchronize()
+        if ozk.ozk_stream_status() != 0:
+            raise RuntimeError("device status in the norm-rule run")
+        nms = n0.elapsed_ms(n1) / args.steps
+        nst = {st: sum(e[i].elapsed_ms(e[i + 1]) for e in ev_n) / args.steps for i, st in enumerate(STAGES)}
+        norm_rule = {"n_moduli": nn, "scaling": "norm (2-norm bound per row/column)",
+                     "gamma": ozk.ozk_gamma(K, nn), "ms_per_step": nms,
+                     "value": ranks.world * flops / (ranks.max(nms / 1e3)) / 1e12, "unit": "TFLOP/s",
+                     "stages_ms": nst, "contract": "eta <= 1e-14 asserted by the precision-contract tests"}
+        del ws_n
+
     pk = peaks()
     gemm_s = stage_ms["residue_gemm"] / 1e3
     algo_flops = 2.0 * M * N * K * n  # one M x N x K residue GEMM per modulus
@@ -404,6 +438,7 @@ def run_gpu(args, ranks: Ranks):
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 8 * (M * K + K * N),
                     "d2h_bytes_per_step": 8 * M * N, "steps": e2e_steps, "matches_device_result": ok_e2e,
                     "mode": "ozk_dgemm_host, one synchronous call per step"},
+            "norm_rule": norm_rule,
             "e2e_pipelined": {"value": pipe_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 8 * (M * K + K * N),
                               "d2h_bytes_per_step": 8 * M * N, "steps": e2e_steps, "matches_device_result": ok_pipe,
                               "mode": "ozk_dgemm_host_async, calls back to back on one stream, one final sync"},
@@ -425,6 +460,9 @@ def main():
                     help="GEMM shape to time (the headline line uses the default)")
     ap.add_argument("--moduli", type=int, default=N_MODULI)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--norm-moduli", type=int, default=13,
+                    help="moduli count of the extra norm-rule measurement")
+    ap.add_argument("--no-norm-rule", action="store_true", help="skip the norm-rule measurement")
     ap.add_argument("--clock-log", default=tempfile.gettempdir(),
                     help="folder for the nvidia-smi clock samples taken during the timed region")
     args = ap.parse_args()

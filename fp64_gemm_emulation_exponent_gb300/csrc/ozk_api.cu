@@ -473,6 +473,13 @@ int ozk_dgemm_norm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t 
                    reinterpret_cast<cudaStream_t>(stream), nullptr, 1);
 }
 
+int ozk_dgemm_norm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
+                            int64_t ldb, double* C, int64_t ldc, int n_moduli, void* workspace,
+                            size_t workspace_bytes, ozk_stream_t stream, ozk_event_t* events) {
+  return run_dgemm(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), events, 1);
+}
+
 int ozk_dgemm_norm(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda, const double* B,
                    int64_t ldb, double* C, int64_t ldc, int n_moduli, ozk_stream_t stream) {
   int rc = validate(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, 1);

@@ -38,6 +38,7 @@ SIGNATURES = {
     "ozk_gamma": (_i32, [_i64, _i32]),
     "ozk_dgemm_norm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_dgemm_norm_ws": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp]),
+    "ozk_dgemm_norm_ws_timed": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp, _vp]),
     "ozk_scale_norm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _vp, _vp]),
     "ozk_moduli_for_bits": (_i32, [_i64, _i32]),
     "ozk_dgemm_bits": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
@@ -159,6 +160,13 @@ def ozk_dgemm_ws_timed(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, wor
                        stream=None):
     ev = (ctypes.c_void_p * 5)(*[e.value for e in events]) if events is not None else None
     return _call("ozk_dgemm_ws_timed", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli,
+                 _ptr(workspace), workspace_bytes, _stream(stream), ctypes.cast(ev, _vp) if ev else None)
+
+
+def ozk_dgemm_norm_ws_timed(M, N, K, A, lda, B, ldb, C, ldc, n_moduli, workspace, workspace_bytes, events,
+                            stream=None):
+    ev = (ctypes.c_void_p * 5)(*[e.value for e in events]) if events is not None else None
+    return _call("ozk_dgemm_norm_ws_timed", M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, n_moduli,
                  _ptr(workspace), workspace_bytes, _stream(stream), ctypes.cast(ev, _vp) if ev else None)
 
 

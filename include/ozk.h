@@ -160,6 +160,11 @@ int ozk_dgemm_norm_ws(int64_t M, int64_t N, int64_t K, const double* A, int64_t 
                       const double* B, int64_t ldb, double* C, int64_t ldc,
                       int n_moduli, void* workspace, size_t workspace_bytes,
                       ozk_stream_t stream);
+/* ozk_dgemm_norm_ws with the stage events of ozk_dgemm_ws_timed. */
+int ozk_dgemm_norm_ws_timed(int64_t M, int64_t N, int64_t K, const double* A, int64_t lda,
+                            const double* B, int64_t ldb, double* C, int64_t ldc,
+                            int n_moduli, void* workspace, size_t workspace_bytes,
+                            ozk_stream_t stream, ozk_event_t* events);
 
 /* C = A * B for HOST matrices (pinned memory gives the fastest copies and
  * the overlap).  A goes to the device in row blocks and B in column blocks
