@@ -461,6 +461,30 @@ size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli) {
   return layout_for(M, N, K, n_moduli).total;
 }
 
+int ozk_workspace_layout(int64_t M, int64_t N, int64_t K, int n_moduli, ozk_workspace_info* info) {
+  if (!info) return OZK_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return OZK_ERR_INVALID_ARG;
+  if (K > OZK_MAX_K || M > kMaxDim || N > kMaxDim || n_moduli < 2 || n_moduli > kMaxModuli ||
+      beta_for(K, n_moduli) < 1)
+    return OZK_ERR_UNSUPPORTED;
+  const Layout L = layout_for(M, N, K, n_moduli);
+  info->total_bytes = L.total;
+  info->maxima_offset = L.amax;
+  info->s_offset = L.s;
+  info->t_offset = L.t;
+  info->a_slices_offset = L.a;
+  info->b_slices_offset = L.b;
+  info->planes_offset = L.out;
+  info->kpad = L.kpad;
+  info->a_plane = L.a_plane;
+  info->b_plane = L.b_plane;
+  info->planes_kind = L.kind;
+  info->planes_ld = L.ldo;
+  info->planes_plane = L.out_plane;
+  info->splits = L.splits;
+  return OZK_OK;
+}
+
 int ozk_gamma(int64_t K, int n_moduli) {
   const int g = gamma_for(K, n_moduli);
   return g >= 1 ? g : -OZK_ERR_UNSUPPORTED;

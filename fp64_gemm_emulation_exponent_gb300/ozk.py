@@ -43,6 +43,7 @@ SIGNATURES = {
     "ozk_moduli_for_bits": (_i32, [_i64, _i32]),
     "ozk_dgemm_bits": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
+    "ozk_workspace_layout": (_i32, [_i64, _i64, _i64, _i32, _vp]),
     "ozk_dgemm": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "ozk_dgemm_ws": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp]),
     "ozk_dgemm_ws_timed": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _vp, _sz, _vp, _vp]),
@@ -64,6 +65,16 @@ SIGNATURES = {
     "ozk_event_elapsed": (_i32, [_vp, _vp, _vp]),
     "ozk_device_sm_count": (_i32, []),
 }
+
+class WorkspaceInfo(ctypes.Structure):
+    """ozk_workspace_info of include/ozk.h."""
+    _fields_ = [("total_bytes", ctypes.c_size_t), ("maxima_offset", ctypes.c_size_t),
+                ("s_offset", ctypes.c_size_t), ("t_offset", ctypes.c_size_t),
+                ("a_slices_offset", ctypes.c_size_t), ("b_slices_offset", ctypes.c_size_t),
+                ("planes_offset", ctypes.c_size_t), ("kpad", ctypes.c_int64), ("a_plane", ctypes.c_int64),
+                ("b_plane", ctypes.c_int64), ("planes_kind", ctypes.c_int), ("planes_ld", ctypes.c_int64),
+                ("planes_plane", ctypes.c_int64), ("splits", ctypes.c_int)]
+
 
 _lib = None
 
@@ -219,6 +230,12 @@ def dgemm(A, B, n_moduli: int = 14, out=None, stream=None, target_bits=None, sca
 def ozk_scale(M, N, K, A, lda, B, ldb, n_moduli, s, t, scratch, stream=None):
     return _call("ozk_scale", M, N, K, _ptr(A), lda, _ptr(B), ldb, n_moduli, _ptr(s), _ptr(t), _ptr(scratch),
                  _stream(stream))
+
+
+def ozk_workspace_layout(M: int, N: int, K: int, n_moduli: int) -> WorkspaceInfo:
+    info = WorkspaceInfo()
+    _call("ozk_workspace_layout", M, N, K, n_moduli, ctypes.cast(ctypes.pointer(info), _vp))
+    return info
 
 
 def ozk_gamma(K: int, n_moduli: int) -> int:

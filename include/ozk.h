@@ -96,6 +96,33 @@ int64_t ozk_kpad(int64_t K);
  * ozk_dgemm_ws then reports. */
 size_t ozk_workspace_size(int64_t M, int64_t N, int64_t K, int n_moduli);
 
+/* Where one ozk_dgemm_ws call keeps each stage's results in its workspace,
+ * for reading them back after the call (the intermediate buffers of a real
+ * call in its own launch configuration: scales, residue slices, residue
+ * planes).  Offsets are in bytes from the workspace start; plane strides
+ * in elements of the region's type.  The layout is an implementation
+ * detail of this library version: use it for inspection, not storage. */
+typedef struct {
+  size_t total_bytes;       /* = ozk_workspace_size */
+  size_t maxima_offset;     /* uint64 abs-bit maxima: rows of A, then columns of B */
+  size_t s_offset;          /* int32 s[M] */
+  size_t t_offset;          /* int32 t[N] */
+  size_t a_slices_offset;   /* fp16 [n][M][kpad], modulus planes a_plane elements apart */
+  size_t b_slices_offset;   /* fp16 [n][N][kpad] (B transposed), b_plane elements apart */
+  size_t planes_offset;     /* the residue GEMM's output, in the layout of planes_kind */
+  int64_t kpad;
+  int64_t a_plane, b_plane;
+  int planes_kind;          /* 0: uint8 residues, 1: int32 split-K sums, 2: uint16 pair residues
+                               (the out_kind of ozk_residue_gemm) */
+  int64_t planes_ld;        /* row stride of a plane, elements */
+  int64_t planes_plane;     /* elements between consecutive planes */
+  int splits;               /* K splits (planes_kind 1) */
+} ozk_workspace_info;
+
+/* Fills *info for ozk_dgemm_ws(M, N, K, ..., n_moduli).  OZK_ERR_INVALID_ARG
+ * for a null info or an empty product, OZK_ERR_UNSUPPORTED as ozk_dgemm. */
+int ozk_workspace_layout(int64_t M, int64_t N, int64_t K, int n_moduli, ozk_workspace_info* info);
+
 /* ------------------------------------------------------------------ */
 /* The GEMM.                                                           */
 /* ------------------------------------------------------------------ */

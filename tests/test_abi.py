@@ -89,6 +89,27 @@ def test_gamma_matches_the_oracle():
             assert ozk.ozk_gamma(K, n) == want, (K, n)
 
 
+def test_workspace_layout_regions_fit_and_do_not_overlap():
+    for (M, N, K, n) in [(1, 1, 1, 2), (300, 257, 700, 14), (2048, 1024, 2100, 14), (300, 257, 9000, 13),
+                         (96, 80, 140000, 14), (8192, 8192, 512, 20)]:
+        info = ozk.ozk_workspace_layout(M, N, K, n)
+        assert info.total_bytes == ozk.ozk_workspace_size(M, N, K, n)
+        assert info.kpad == ozk.ozk_kpad(K)
+        esize = {0: 1, 1: 4, 2: 2}[info.planes_kind]
+        planes = {0: n, 1: n * info.splits, 2: (n + 1) // 2}[info.planes_kind]
+        regions = [(info.maxima_offset, 2 * 8 * (M + N)), (info.s_offset, 4 * M), (info.t_offset, 4 * N),
+                   (info.a_slices_offset, 2 * ((n - 1) * info.a_plane + M * info.kpad)),
+                   (info.b_slices_offset, 2 * ((n - 1) * info.b_plane + N * info.kpad)),
+                   (info.planes_offset, esize * ((planes - 1) * info.planes_plane + M * info.planes_ld))]
+        end = 0
+        for off, size in regions:
+            assert off >= end and off % 256 == 0
+            end = off + size
+        assert end <= info.total_bytes
+        assert info.a_plane >= M * info.kpad and info.b_plane >= N * info.kpad
+        assert info.planes_ld >= N and info.planes_plane >= M * info.planes_ld
+
+
 def test_kpad():
     assert [ozk.ozk_kpad(k) for k in [0, 1, 63, 64, 65, 128, 131071]] == [0, 64, 64, 64, 128, 128, 131072]
 
