@@ -63,7 +63,7 @@ def test_stage_buffers_of_one_call(M, N, K, n, kind):
         assert np.array_equal(f16_to_int(gb[:, :K]), rb[p].T.astype(np.int64))
         assert np.all(ga[:, K:] == 0) and np.all(gb[:, K:] == 0)
     # 3. the residue GEMM's planes at sampled outputs, and C
-    ii = np.concatenate([rng.integers(0, M, 200), [0, M - 1, 255, 256 % M]])
+    ii = np.concatenate([rng.integers(0, M, 200), [0, M - 1, 255 % M, 256 % M]])
     jj = np.concatenate([rng.integers(0, N, 200), [N - 1, 0, 255 % N, 256 % N]])
     Co, _, cmod, _ = oracle.sample(A, B, n, ii, jj)
     ld, pl = info.planes_ld, info.planes_plane
