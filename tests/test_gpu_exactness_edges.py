@@ -25,6 +25,12 @@
    (runtime moduli count for narrow outputs, compile-time count for wide
    ones), against the oracle's Garner CRT and correctly rounded unscale.
 
+3. The combine's quotient estimate q = round(S/P) may be off by one within
+   P 2^-19 of the lift boundary +-P/2, where an exact lift decides; random
+   residues land there about once in 2^18 outputs.  These tests put every
+   output there (X = P/2 - 1 - d or -P/2 + d, from d = 0 up to the edge of
+   that window), through all input kinds, both kernels and the limb output.
+
 Method: Ozaki scheme II on the "Day 12" page (ithelp.ithome.com.tw), sections
 "Profile 不能只看 Tensor Core" (the integer GEMM per modulus, mod reduction,
 CRT reconstruction, undo scaling) and "先定義公平比較" (the precision
@@ -241,4 +247,85 @@ def test_crt_round_to_even_ties(n, M, N):
     # the lifted integers themselves
     X8 = run_lift(dev(planes8), 0, ld8, 1, M, N, n).cpu().numpy().view(np.uint32)
     assert np.array_equal(X8, Xo)
+    assert ozk.ozk_stream_status() == 0
+
+
+# --------------------------------------------------------------------------
+# 3. the symmetric lift at its boundary
+# --------------------------------------------------------------------------
+def lift_boundary_problem(n, M, N, seed):
+    """X within P 2^-19 of the lift boundary, X in [-P/2, P/2): P/2 - 1 - d or
+    -P/2 + d.  There the combine's quotient estimate q = round(S/P) may be
+    off by one and the exact lift decides.  Per row a size for d: zero (the
+    two boundary values themselves), small, about P 2^-21, and about P 2^-19
+    (the edge of the window the kernels check).  Returns byte residues,
+    pair residues, s, t and a dict of spot-checked X."""
+    rng = np.random.default_rng(seed)
+    ps = [int(p) for p in oracle.moduli(n)]
+    P = 1
+    for p in ps:
+        P *= p
+    half = P // 2  # P is even (256 is a modulus): -P/2 <= X < P/2
+    bits_p = P.bit_length()
+    limbs = (bits_p + 31) // 32
+    dbits = np.select([np.arange(M) % 4 == 0, np.arange(M) % 4 == 1, np.arange(M) % 4 == 2],
+                      [0, 12, bits_p - 21], bits_p - 19)
+    d = rng.integers(0, 2**32, (M, N, limbs), dtype=np.uint64)
+    keep = np.clip(dbits[:, None] - 32 * np.arange(limbs)[None, :], 0, 32)  # bits of limb l kept in row i
+    d &= ((np.uint64(1) << keep.astype(np.uint64)) - np.uint64(1))[:, None, :]
+    neg = rng.integers(0, 2, (M, N)).astype(bool)
+
+    def residues_mod(m):
+        pw = np.array([pow(2, 32 * l, m) for l in range(limbs)], dtype=np.uint64)
+        dm = (d % np.uint64(m) * pw).sum(axis=2).astype(np.int64) % m
+        return np.where(neg, (dm - half % m) % m, ((half - 1) % m - dm) % m)
+
+    cmod = np.stack([residues_mod(p) for p in ps]).astype(np.uint8)
+    pair = np.stack([residues_mod(ps[2 * j] * ps[2 * j + 1]) if 2 * j + 1 < n else residues_mod(ps[2 * j])
+                     for j in range((n + 1) // 2)]).astype(np.uint16)
+    s = rng.integers(-800, 900, M).astype(np.int32)
+    spot = [(int(i), int(j)) for i, j in zip(rng.integers(0, M, 60), rng.integers(0, N, 60))]
+    spot += [(0, 0), (0, N - 1), (M - 1, 0)]
+
+    def xval(i, j):
+        dv = sum(int(d[i, j, l]) << (32 * l) for l in range(limbs))
+        return -half + dv if neg[i, j] else half - 1 - dv
+
+    return cmod, pair, s, np.zeros(N, dtype=np.int32), {(i, j): xval(i, j) for i, j in spot}
+
+
+@pytest.mark.parametrize("n", [8, 14, 20])
+@pytest.mark.parametrize("M,N", [(96, 200), (1024, 1248)])
+def test_crt_lift_at_the_boundary(n, M, N):
+    """Every output within P 2^-19 of +-P/2 (the two boundary values
+    included): the lifted integers (from byte and pair residues) and C (byte,
+    pair and split int32 inputs; the runtime-count kernel at 96 x 200, the
+    compile-time-count kernel at 1024 x 1248) against the oracle."""
+    cmod, pair, s, t, Xspot = lift_boundary_problem(n, M, N, seed=7000 + 100 * n + M)
+    Xo = oracle.crt(cmod, n)
+    for (i, j), x in Xspot.items():  # the oracle lifts to the constructed X
+        assert oracle.limbs_to_int(Xo[i, j]) == x
+    S = np.broadcast_to(s[:, None].astype(np.int64) + t[None, :], (M, N)).astype(np.int32)
+    want = oracle.round_scaled(Xo.reshape(-1, oracle.LIMBS), S.ravel().copy()).reshape(M, N)
+    ds, dt = dev(s), dev(t)
+    ld8 = (N + 15) // 16 * 16
+    planes8 = np.zeros((n, M, ld8), dtype=np.uint8)
+    planes8[:, :, :N] = cmod
+    assert np.array_equal(run_lift(dev(planes8), 0, ld8, 1, M, N, n).cpu().numpy().view(np.uint32), Xo)
+    assert same_bits(run_combine(dev(planes8), 0, ld8, 1, ds, dt, M, N, n).cpu().numpy(), want)
+    ld16 = (N + 7) // 8 * 8
+    planes16 = np.zeros((pair.shape[0], M, ld16), dtype=np.uint16)
+    planes16[:, :, :N] = pair
+    p16 = dev(planes16.view(np.int16))
+    assert np.array_equal(run_lift(p16, 2, ld16, 1, M, N, n).cpu().numpy().view(np.uint32), Xo)
+    assert same_bits(run_combine(p16, 2, ld16, 1, ds, dt, M, N, n).cpu().numpy(), want)
+    rng = np.random.default_rng(n * 31 + M)
+    ps = oracle.moduli(n).astype(np.int64)[:, None, None]
+    ld32 = (N + 3) // 4 * 4
+    part0 = rng.integers(-(2**29), 2**29, (n, M, N))
+    part1 = (cmod.astype(np.int64) - part0) % ps + ps * rng.integers(-(2**20), 2**20, (n, M, N))
+    planes32 = np.zeros((2, n, M, ld32), dtype=np.int32)
+    planes32[0, :, :, :N] = part0
+    planes32[1, :, :, :N] = part1
+    assert same_bits(run_combine(dev(planes32), 1, ld32, 2, ds, dt, M, N, n).cpu().numpy(), want)
     assert ozk.ozk_stream_status() == 0

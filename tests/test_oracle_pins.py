@@ -303,6 +303,25 @@ def test_crt_satisfies_the_defining_congruences(n):
     assert X[0] == 0
 
 
+@pytest.mark.parametrize("n", [2, 8, 14, 20])
+def test_crt_lift_boundary_convention(n):
+    """The symmetric lift keeps X in [-P/2, P/2): P/2 - 1 is positive, the
+    class of P/2 lifts to -P/2, and values a little inside either end stay
+    where they are (P is even: 256 is a modulus)."""
+    ps = MODULI_ALL[:n]
+    P = prod(ps)
+    assert P % 2 == 0
+    half = P // 2
+    xs = [half - 1, -half, half - 2, -half + 1, half - 1 - 12345, -half + 12345, 0, -1, 1,
+          half - 1 - (P >> 20), -half + (P >> 20)]
+    cm = np.array([[x % p for x in xs] for p in ps], dtype=np.uint8)
+    X = oracle.limbs_to_int(oracle.crt(cm, n))
+    assert X == xs
+    # the class of +P/2 itself
+    cm_half = np.array([[half % p] for p in ps], dtype=np.uint8)
+    assert oracle.limbs_to_int(oracle.crt(cm_half, n)) == [-half]
+
+
 def test_crt_recovers_extreme_products():
     # values right at the edge of what beta allows: +-K 2^(2 beta)
     for n in (8, 14, 20):
