@@ -31,6 +31,11 @@
    output there (X = P/2 - 1 - d or -P/2 + d, from d = 0 up to the edge of
    that window), through all input kinds, both kernels and the limb output.
 
+4. The quantiser rounds a 2^s to the nearest integer, ties to even; data
+   rarely scale to exact halves.  These tests build rows and columns whose
+   entries mostly do, at every integer width of the quantiser and through
+   the fused row scan of ozk_dgemm.
+
 Method: Ozaki scheme II on the "Day 12" page (ithelp.ithome.com.tw), sections
 "Profile 不能只看 Tensor Core" (the integer GEMM per modulus, mod reduction,
 CRT reconstruction, undo scaling) and "先定義公平比較" (the precision
@@ -44,7 +49,7 @@ import torch
 
 import oracle
 from fp64_gemm_emulation_exponent_gb300 import ozk
-from gpu_helpers import dev, run_combine, run_gemm, run_lift, same_bits
+from gpu_helpers import dev, f16_to_int, run_combine, run_gemm, run_lift, run_quantize, run_scale, same_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -329,3 +334,70 @@ def test_crt_lift_at_the_boundary(n, M, N):
     planes32[1, :, :, :N] = part1
     assert same_bits(run_combine(dev(planes32), 1, ld32, 2, ds, dt, M, N, n).cpu().numpy(), want)
     assert ozk.ozk_stream_status() == 0
+
+
+# --------------------------------------------------------------------------
+# 4. round-to-nearest-even ties in the quantiser
+# --------------------------------------------------------------------------
+def quantize_tie_operands(M, N, K, n, seed):
+    """A and B whose scaled entries are mostly exact halves.  With the
+    largest-entry rule a row (column) whose largest entry is 0.75 2^E (frexp
+    exponent E) gets the scale beta - E, so an entry (2k+1) 2^(E - beta - 1)
+    scales to (2k+1)/2: a tie, which rounds to the even neighbour.  About
+    three entries in four are ties of either sign, the rest random below the
+    largest; E varies from row to row."""
+    rng = np.random.default_rng(seed)
+    beta = oracle.beta(K, n)
+    top = min(beta, 52)  # |2k+1| < 2^top stays exact in a double
+
+    def lines(count, length):
+        E = rng.integers(-60, 60, count)
+        odd = (rng.integers(0, 2**(top - 1), (count, length)) * 2 + 1) * rng.choice([-1, 1], (count, length))
+        x = np.ldexp(odd.astype(np.float64), (E - beta - 1)[:, None])
+        plain = rng.random((count, length)) < 0.25
+        x = np.where(plain, np.ldexp(rng.uniform(-0.7, 0.7, (count, length)), E[:, None]), x)
+        x[np.arange(count), rng.integers(0, length, count)] = np.ldexp(0.75, E)  # the largest entry
+        return x
+
+    return lines(M, K), np.ascontiguousarray(lines(N, K).T)
+
+
+@pytest.mark.parametrize("n,K", [(8, 300), (14, 1000), (17, 100), (17, 16), (18, 1000), (20, 700)])
+def test_quantize_round_half_to_even(n, K):
+    """Scales and every residue slice bit-exact against the oracle when most
+    scaled entries are exact halves: beta 26, 49 and 62 (the one-word
+    integer path of the quantiser), 63 and 64 (three limbs), 72 (four)."""
+    M, N = 70, 90
+    A, B = quantize_tie_operands(M, N, K, n, seed=n * 100 + K)
+    s, t = run_scale(dev(A), dev(B), n)
+    so, to = oracle.scale(A, B, n)
+    assert np.array_equal(s.cpu().numpy(), so) and np.array_equal(t.cpu().numpy(), to)
+    beta = oracle.beta(K, n)
+    assert np.all(so == beta - np.frexp(np.abs(A).max(axis=1))[1])  # the construction's scale
+    Ap = oracle.integers(A, so, True)
+    ties = np.abs(np.ldexp(A, so[:, None]) - np.trunc(np.ldexp(A, so[:, None]))) == 0.5
+    assert ties.mean() > 0.6 and np.all(Ap[ties] % 2 == 0)  # ties went to the even neighbour
+    a_sl, b_sl = run_quantize(dev(A), dev(B), s, t, n)
+    Bp = oracle.integers(B, to, False)
+    ga = a_sl.cpu().numpy().view(np.uint16)
+    gb = b_sl.cpu().numpy().view(np.uint16)
+    assert np.array_equal(f16_to_int(ga[:, :, :K]), oracle.residues(Ap, n).astype(np.int64))
+    assert np.array_equal(f16_to_int(gb[:, :, :K]), oracle.residues(Bp, n).transpose(0, 2, 1).astype(np.int64))
+    assert ozk.ozk_stream_status() == 0
+
+
+@pytest.mark.parametrize("n", [14, 20])
+def test_dgemm_round_half_to_even_fused_row_scan(n):
+    """The same ties through ozk_dgemm where the rows of A are scanned and
+    quantised in one block each (M kpad >= 2^22, K <= 4096): sampled outputs
+    bit-exact against the oracle."""
+    M, N, K = 1100, 200, 4000
+    A, B = quantize_tie_operands(M, N, K, n, seed=n)
+    C = ozk.dgemm(dev(A), dev(B), n)
+    torch.cuda.synchronize()
+    assert ozk.ozk_stream_status() == 0
+    rng = np.random.default_rng(n)
+    ii = np.concatenate([rng.integers(0, M, 300), [0, M - 1]])
+    jj = np.concatenate([rng.integers(0, N, 300), [N - 1, 0]])
+    Cg = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().numpy()
+    assert same_bits(Cg, oracle.sample(A, B, n, ii, jj)[0])
