@@ -3,7 +3,8 @@ and a C program that takes the address of every entry point the header
 declares links against libozk.so and, with no GPU, gets the same answers
 from the host-only helpers and the argument checks as the Python binding
 does.  (A declaration that does not match an exported symbol fails the
-link.)"""
+link.)  On a GPU, a C program with device buffers from the CUDA runtime
+gets C bit-exact from ozk_dgemm and ozk_dgemm_host."""
 import os
 import re
 import shutil
@@ -99,3 +100,75 @@ int main(void) {{
     assert out[7] == ozk.status_string(ozk.OZK_ERR_TIMEOUT)
     assert [int(x) for x in out[8:12]] == [ozk.OZK_ERR_INVALID_ARG, ozk.OZK_ERR_UNSUPPORTED,
                                            ozk.OZK_ERR_INVALID_ARG, ozk.OZK_OK]
+
+
+@pytest.mark.gpu
+def test_c_program_multiplies_on_the_gpu(tmp_path):
+    """A plain C caller (CUDA runtime for device memory, no Python in the
+    loop): ozk_dgemm on device buffers and ozk_dgemm_host on host buffers,
+    both bit-exact against the oracle."""
+    import numpy as np
+
+    lib = ozk_build.build()
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    M, N, K, n = 67, 45, 130, 14
+    rng = np.random.default_rng(5)
+    A = rng.standard_normal((M, K))
+    B = rng.standard_normal((K, N))
+    A.tofile(tmp_path / "a.bin")
+    B.tofile(tmp_path / "b.bin")
+    src = tmp_path / "gpu_caller.c"
+    src.write_text(f"""#include <stdio.h>
+#include <stdlib.h>
+#include <cuda_runtime_api.h>
+#include "ozk.h"
+
+static int load(const char* path, double* x, size_t count) {{
+  FILE* f = fopen(path, "rb");
+  size_t got;
+  if (!f) return 1;
+  got = fread(x, sizeof(double), count, f);
+  fclose(f);
+  return got != count;
+}}
+
+int main(int argc, char** argv) {{
+  const int64_t M = {M}, N = {N}, K = {K};
+  double *A = malloc(sizeof(double) * M * K), *B = malloc(sizeof(double) * K * N);
+  double *C1 = malloc(sizeof(double) * M * N), *C2 = malloc(sizeof(double) * M * N);
+  double *dA, *dB, *dC;
+  int rc, i;
+  if (argc < 3 || load(argv[1], A, M * K) || load(argv[2], B, K * N)) return 10;
+  if (cudaMalloc((void**)&dA, sizeof(double) * M * K) || cudaMalloc((void**)&dB, sizeof(double) * K * N) ||
+      cudaMalloc((void**)&dC, sizeof(double) * M * N))
+    return 11;
+  cudaMemcpy(dA, A, sizeof(double) * M * K, cudaMemcpyHostToDevice);
+  cudaMemcpy(dB, B, sizeof(double) * K * N, cudaMemcpyHostToDevice);
+  rc = ozk_dgemm(M, N, K, dA, K, dB, N, dC, N, {n}, NULL);
+  if (rc != OZK_OK) return 20 + rc;
+  if (ozk_stream_status(NULL) != OZK_OK) return 14;  /* waits for the call */
+  if (cudaMemcpy(C1, dC, sizeof(double) * M * N, cudaMemcpyDeviceToHost)) return 12;
+  rc = ozk_dgemm_host(M, N, K, A, K, B, N, C2, N, {n}, NULL);
+  if (rc != OZK_OK) return 30 + rc;
+  if (ozk_stream_status(NULL) != OZK_OK) return 13;
+  for (i = 0; i < M * N; ++i) printf("%a %a\\n", C1[i], C2[i]);
+  cudaFree(dA);
+  cudaFree(dB);
+  cudaFree(dC);
+  free(A); free(B); free(C1); free(C2);
+  return 0;
+}}
+""")
+    exe = tmp_path / "gpu_caller"
+    libdir = os.path.dirname(lib)
+    compile_ok(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, "-I", os.path.join(cuda, "include"),
+                str(src), "-L", libdir, "-lozk", f"-Wl,-rpath,{libdir}", "-L", os.path.join(cuda, "lib64"),
+                "-lcudart", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}", "-o", str(exe)])
+    r = subprocess.run([str(exe), str(tmp_path / "a.bin"), str(tmp_path / "b.bin")], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    got = np.array([[float.fromhex(v) for v in line.split()] for line in r.stdout.splitlines()])
+    want = oracle.dgemm(A, B, n).ravel()
+    assert got.shape == (M * N, 2)
+    assert np.array_equal(got[:, 0].view(np.uint64), want.view(np.uint64))
+    assert np.array_equal(got[:, 1].view(np.uint64), want.view(np.uint64))
