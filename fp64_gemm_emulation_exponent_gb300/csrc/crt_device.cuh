@@ -160,8 +160,9 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&X)[NL], i
 
 // Fast path of round_scaled_bits for |X| >= 2^(32(NL-2)) with a normal
 // result: a 64-bit window from the top two nonzero-headed limbs, 53 bits
-// kept, round to nearest even with the bits below as sticky.  Returns false
-// (and leaves *out alone) when the slow path must decide.
+// kept, round to nearest even with the bits below as sticky.  Branch-free:
+// always writes *out, and returns false when that value is not the answer
+// (the slow path must decide).
 template <int NL>
 __device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S, uint64_t* out) {
   const uint32_t sgn = X[NL - 1] >> 31;
@@ -201,13 +202,11 @@ __device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S
     t0 = top ? m[0] : 0u;
     st = 0u;
   }
-  if (t2 == 0u) return false;
-  const int lz = __clz(t2);
+  const int lz = __clz(t2);  // 32 when t2 = 0: then the result is discarded
   const uint32_t hi = __funnelshift_l(t1, t2, lz);
   const uint32_t mid = __funnelshift_l(t0, t1, lz);
-  const uint32_t lo = t0 << lz;
+  const uint32_t lo = t0 << (lz & 31);
   const int e = (top ? 32 * (NL - 1) : 32 * (NL - 2)) + 31 - lz - S;  // |X| 2^-S in [2^e, 2^(e+1))
-  if (e < -1022 || e > 1023) return false;
   const uint32_t sig_lo = __funnelshift_r(mid, hi, 11);
   const uint32_t sig_hi = hi >> 11;
   const uint32_t rb = (mid >> 10) & 1u;
@@ -218,7 +217,7 @@ __device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S
   const uint64_t bits = (static_cast<uint64_t>(e + 1022) << 52) +
                         ((static_cast<uint64_t>(sig_hi) << 32) | sig_lo) + inc;
   *out = bits | (static_cast<uint64_t>(sgn) << 63);
-  return true;
+  return t2 != 0u && e >= -1022 && e <= 1023;
 }
 
 __device__ __forceinline__ void store4_f64(double* dst, const uint64_t (&b)[4]) {
@@ -408,10 +407,11 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
           }
         }
       });
-#pragma unroll
-      for (int o = 0; o < kPassCols; ++o) {
-        const int oc = pass * kPassCols + o;  // output column j0 + oc
-        // q = round(S / P) from qh 2^16 + ql (32.32 fixed point) plus one half
+      // q = round(S / P) from qh 2^16 + ql (32.32 fixed point) plus one
+      // half, then X = S + q (2^(32 NL) - P) mod 2^(32 NL) from the 16-bit
+      // columns (limb l = c_2l + c_2l+1 2^16 + the carry of limb l - 1);
+      // returns the fraction of S / P + 1/2 (0.32 fixed point)
+      auto assemble = [&](int o, uint32_t (&X)[NL]) -> uint32_t {
         uint32_t q, frac;
         asm("{\n\t.reg .u32 t;\n\t"
             "shl.b32 t, %2, 16;\n\t"
@@ -422,9 +422,6 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
             : "=r"(q), "=r"(frac)
             : "r"(qh[o]), "r"(ql[o]));
         q += qh[o] >> 16;
-        // X = S + q (2^(32 NL) - P) mod 2^(32 NL), from the 16-bit columns:
-        // limb l = c_2l + c_2l+1 2^16 + the carry of limb l - 1
-        uint32_t X[NL];
         uint32_t carry = 0;
 #pragma unroll
         for (int l = 0; l < NL; ++l) {
@@ -443,19 +440,54 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
           X[l] = x;
           carry = nc;
         }
-        if (frac < kLiftMargin || frac > ~kLiftMargin) exact_lift<NL>(X, K);
+        return frac;
+      };
+      // With four outputs per pass the common case takes no branch: the fast
+      // unscale of every output; outputs that need the exact lift, have a
+      // non-finite scale or fall outside the fast unscale are marked and
+      // redone after the pass.  (Wider X, two outputs per pass: each output
+      // takes its own branches, which measured faster there.)
+      constexpr bool kDeferRare = kPassCols == 4;
+      uint32_t rare = 0;
+#pragma unroll
+      for (int o = 0; o < kPassCols; ++o) {
+        const int oc = pass * kPassCols + o;  // output column j0 + oc
+        uint32_t X[NL];
+        const uint32_t frac = assemble(o, X);
+        const bool lift = frac < kLiftMargin || frac > ~kLiftMargin;
         if constexpr (LIMBS) {
+          if (lift) exact_lift<NL>(X, K);
           if (j0 + oc < N) {
             uint32_t* dst = Xout + (i * N + j0 + oc) * OZK_LIMBS;
             const uint32_t ext = is_negative<NL>(X) ? 0xFFFFFFFFu : 0u;
 #pragma unroll
             for (int l = 0; l < OZK_LIMBS; ++l) dst[l] = l < NL ? X[l] : ext;
           }
+        } else if constexpr (kDeferRare) {
+          const bool ok = round_scaled_fast<NL>(X, si + tj[oc], &outbits[oc]);
+          rare |= (lift || !ok || si == OZK_SCALE_NONFINITE || tj[oc] == OZK_SCALE_NONFINITE) ? 1u << o : 0u;
         } else {
+          if (lift) exact_lift<NL>(X, K);
           if (si == OZK_SCALE_NONFINITE || tj[oc] == OZK_SCALE_NONFINITE)
             outbits[oc] = kQuietNaN;
           else if (!round_scaled_fast<NL>(X, si + tj[oc], &outbits[oc]))
             outbits[oc] = round_scaled_bits<NL>(X, si + tj[oc]);
+        }
+      }
+      if constexpr (!LIMBS && kDeferRare) {
+        if (rare) {
+#pragma unroll
+          for (int o = 0; o < kPassCols; ++o) {
+            if (!((rare >> o) & 1u)) continue;
+            const int oc = pass * kPassCols + o;
+            uint32_t X[NL];
+            const uint32_t frac = assemble(o, X);
+            if (frac < kLiftMargin || frac > ~kLiftMargin) exact_lift<NL>(X, K);
+            if (si == OZK_SCALE_NONFINITE || tj[oc] == OZK_SCALE_NONFINITE)
+              outbits[oc] = kQuietNaN;
+            else if (!round_scaled_fast<NL>(X, si + tj[oc], &outbits[oc]))
+              outbits[oc] = round_scaled_bits<NL>(X, si + tj[oc]);
+          }
         }
       }
     }
