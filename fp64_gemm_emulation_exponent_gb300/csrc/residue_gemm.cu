@@ -8,9 +8,11 @@
 // [-128, 127]) are fed to the fp16 tensor cores, where they are exact: every
 // product is an integer of magnitude at most 2^14, so every fp32 partial sum
 // of a 1024-term chunk is an integer of magnitude at most 2^24 and the fp32
-// accumulator in TMEM holds the chunk's exact integer sum.  The epilogue
-// warps read each chunk out of TMEM, convert it exactly (cvt.rni) and add it
-// into int32 registers (exact for K < 2^17), then reduce mod p once per tile.
+// accumulator in TMEM holds the chunk's exact integer sum.  Where a K split
+// spans several chunks the epilogue warps read each chunk out of TMEM,
+// convert it exactly (cvt.rni) and add it into int32 registers (exact for
+// K < 2^17), then reduce mod p once per tile; where the split is one chunk
+// (K <= 1024) they reduce the fp32 sums mod p directly, on the FP32 pipes.
 // Outputs: the residues mod p as uint8 planes (out_kind 0); the exact int32
 // sums of a K split (1); or, with the two moduli of a pair run back to back
 // on one tile, the uint16 residue of the pair modulus p_2j p_2j+1 (2, the
@@ -22,10 +24,11 @@
 //    rows of A and half of the B tile, so a stage is 32 KB per SM, the ring is
 //    6 deep and the shared-memory traffic per MMA is a third lower than with
 //    one CTA per tile.  Both CTAs drain their own 128 accumulator rows.
-//  * K < 2048: one CTA per 128 x 256 tile, 4-stage ring; 1024-term chunks
-//    from K = 1024, below that 256-term chunks (sums at most 2^22) converted
-//    with one fp32 add of 1.5 * 2^23, cheaper per chunk when the drain cannot
-//    be spread over a long K.
+//  * K < 2048: one CTA per 128 x 256 tile, 4-stage ring.  Up to K = 1024
+//    the tile's sums are one chunk: the epilogue loads all of its 128
+//    columns, hands the accumulator back to the MMA issuer at once and
+//    reduces in fp32 while the next tile accumulates (at short K the
+//    epilogue, not the tensor core, set the pace of the int32 form).
 //
 // Structure of both: persistent CTAs (one per SM), warp-specialised.
 //   warp 0      TMA producer: A and B slice tiles into the smem ring (128-byte
@@ -58,12 +61,8 @@ constexpr int kStages = 4;   // smem ring depth
 static_assert(kKBlock % BK == 0, "slices are padded to whole stages");
 constexpr int kSwizzleBytes = BK * 2;                  // 128-byte or 64-byte swizzle
 constexpr uint64_t kLayoutType = kSwizzleBytes == 128 ? 2 : 4;  // descriptor swizzle code
-// k-blocks per exact chunk: 1024 terms (|sum| <= 2^24, converted with
-// cvt.rni) or 256 terms (|sum| <= 2^22, converted with the 1.5 * 2^23 add)
-template <bool LONG>
-constexpr int chunk_kb() {
-  return (LONG ? 1024 : 256) / BK;
-}
+// k-blocks per exact chunk: 1024 terms, every partial sum |x| <= 2^24
+constexpr int kChunkKB = 1024 / BK;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warpgroup 0: control, 1-2: epilogue
 // Register split between the warpgroups (setmaxnreg).  The kernel launches
@@ -107,10 +106,9 @@ static_assert(kSmemBytes + kStashBytes <= 232448 && kPairSmemBytes + kStashBytes
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // limit of every pipeline wait in normal runs
 constexpr uint64_t kDrainNs = 50000000ull;
 
-// fp32 bits of 1.5 * 2^23: x + 1.5*2^23 for an integer |x| <= 2^22 has the
-// integer x in its low mantissa bits, exactly.
+// 1.5 * 2^23: y + 1.5 * 2^23 for |y| <= 2^22 is rounded to an integer (ulp
+// 1), and for an integer y holds y in its low mantissa bits, exactly.
 constexpr float kMagic = 12582912.0f;
-constexpr uint32_t kMagicBits = 0x4B400000u;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B fp16 (bits 7-9 and 10-12 = 0), both K-major (bits 15, 16 = 0),
@@ -128,6 +126,7 @@ constexpr uint32_t kPairIdesc = (1u << 4) |  // M of the whole pair
 // t < 2^25 is divided exactly as umulhi(t, ceil(2^42 / m)) >> 10.
 struct ModTable {
   uint32_t p[kMaxModuli], magic[kMaxModuli], bias[kMaxModuli];
+  float inv[kMaxModuli];  // 1/p rounded to nearest fp32
   uint32_t pu0[kMaxModuli / 2], pu1[kMaxModuli / 2], pm[kMaxModuli / 2], pmagic[kMaxModuli / 2];
 };
 
@@ -143,6 +142,7 @@ __host__ __device__ constexpr ModTable make_mod_table() {
     t.p[k] = modulus_at(k);
     t.magic[k] = magic_of(t.p[k]);
     t.bias[k] = bias_of(t.p[k]);
+    t.inv[k] = 1.0f / static_cast<float>(t.p[k]);
   }
   for (int j = 0; j < kMaxModuli / 2; ++j) {
     const uint32_t pa = modulus_at(2 * j), pb = modulus_at(2 * j + 1);
@@ -461,39 +461,35 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
 }
 
 // acc[base .. base+31] += the 32 exact chunk sums held as fp32 in v.
-template <bool LONG>
 __device__ __forceinline__ void add_chunk(int32_t (&acc)[kCols], int base, const uint32_t (&v)[32]) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    if constexpr (LONG)
-      acc[base + e] += __float2int_rn(__uint_as_float(v[e]));
-    else
-      acc[base + e] += __float_as_int(__uint_as_float(v[e]) + kMagic);
+  for (int e = 0; e < 32; ++e) acc[base + e] += __float2int_rn(__uint_as_float(v[e]));
+}
+
+// Adds this thread's kCols chunk sums from TMEM into acc, one block of 32
+// columns per tcgen05.ld, loaded after the previous block is added up (the
+// registers go to the conversions).
+template <int Q>
+__device__ __forceinline__ void drain_chunk(int32_t (&acc)[kCols], uint32_t taddr, uint32_t (&cur)[32]) {
+  add_chunk(acc, 32 * Q, cur);
+  if constexpr (Q + 1 < kCols / 32) {
+    tmem_ld32(taddr + 32 * (Q + 1), cur);
+    tmem_wait_ld(cur);
+    drain_chunk<Q + 1>(acc, taddr, cur);
   }
 }
 
-// Adds this thread's kCols chunk sums from TMEM into acc, 32 columns per
-// tcgen05.ld.  Short chunks double-buffer the loads (load Q+1 in flight while
-// load Q is added up); long chunks, drained a quarter as often, load one
-// block at a time and keep the registers for the conversions.
-template <bool LONG, int Q>
-__device__ __forceinline__ void drain_chunk(int32_t (&acc)[kCols], uint32_t taddr, uint32_t (&cur)[32],
-                                            uint32_t (&nxt)[32]) {
-  if constexpr (LONG) {
-    add_chunk<LONG>(acc, 32 * Q, cur);
-    if constexpr (Q + 1 < kCols / 32) {
-      tmem_ld32(taddr + 32 * (Q + 1), cur);
-      tmem_wait_ld(cur);
-      drain_chunk<LONG, Q + 1>(acc, taddr, cur, nxt);
-    }
-  } else {
-    if constexpr (Q + 1 < kCols / 32) tmem_ld32(taddr + 32 * (Q + 1), nxt);
-    add_chunk<LONG>(acc, 32 * Q, cur);
-    if constexpr (Q + 1 < kCols / 32) {
-      tmem_wait_ld(nxt);
-      drain_chunk<LONG, Q + 1>(acc, taddr, nxt, cur);
-    }
-  }
+// (x mod p) for an fp32 sum x of one chunk (an integer, |x| <= 2^24), as
+// the low byte of the returned fp32 bits.  q = rint(x * (1/p)) by one fma
+// with the 1.5 * 2^23 add: x * (1/p) is within |x| p^-1 2^-24 < 2^-7 of
+// x / p, so q is x / p rounded up or down and |x - q p| < p; the fma gives
+// r = x - q p exactly, and r + p if r < 0 is the residue in [0, p), whose
+// sum with 1.5 * 2^23 carries it in the low mantissa bits.
+__device__ __forceinline__ uint32_t residue_bits(uint32_t xbits, float pf, float inv, float pmagic) {
+  const float x = __uint_as_float(xbits);
+  const float q = __fsub_rn(__fmaf_rn(x, inv, kMagic), kMagic);
+  const float r = __fmaf_rn(-q, pf, x);
+  return __float_as_uint(__fadd_rn(r, r < 0.0f ? pmagic : kMagic));
 }
 
 // x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
@@ -582,6 +578,32 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
   }
 }
 
+// out_kind 0 from the fp32 sums of a one-chunk split: (x mod p) as uint8 in
+// plane p for this thread's kCols columns gj0.. of row gi, 16 per store.
+__device__ __forceinline__ void store_residues_f32(const uint32_t (&x)[kCols / 32][32], int p, int64_t gi,
+                                                   int64_t gj0, const GemmParams& prm) {
+  if (gi >= prm.M) return;
+  const float pf = static_cast<float>(c_mod.p[p]), inv = c_mod.inv[p], pmagic = kMagic + pf;
+  uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(p) * prm.out_plane + gi * prm.ldo + gj0;
+#pragma unroll
+  for (int v = 0; v < kCols / 16; ++v) {
+    if (gj0 + 16 * v < prm.ldo) {
+      uint32_t word[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int e = 16 * v + 4 * b;
+        const uint32_t* xs = &x[e / 32][e % 32];
+        const uint32_t lo = __byte_perm(residue_bits(xs[0], pf, inv, pmagic), residue_bits(xs[1], pf, inv, pmagic),
+                                        0x0040);
+        const uint32_t hi = __byte_perm(residue_bits(xs[2], pf, inv, pmagic), residue_bits(xs[3], pf, inv, pmagic),
+                                        0x0040);
+        word[b] = __byte_perm(lo, hi, 0x5410);
+      }
+      *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+    }
+  }
+}
+
 template <bool LONG, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -601,7 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accf0 = empty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
-  constexpr int kChunkKB = chunk_kb<LONG>();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -736,32 +757,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
       for (int ps = 0; ps < w.passes && ok; ++ps) {
-        int32_t acc[kCols];
+        if constexpr (LONG) {
+          int32_t acc[kCols];
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = 0;
-        for (int c = 0; c < nchunks; ++c) {
-          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
-            ok = false;
-            break;
+          for (int e = 0; e < kCols; ++e) acc[e] = 0;
+          for (int c = 0; c < nchunks; ++c) {
+            if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(ab * BN + half * kCols);
+            uint32_t va[32];
+            tmem_ld32(taddr, va);
+            tmem_wait_ld(va);
+            drain_chunk<0>(acc, taddr, va);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * ab);
+            ab ^= 1;
+            if (ab == 0) aphase ^= 1u;
           }
-          tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                 static_cast<uint32_t>(ab * BN + half * kCols);
-          uint32_t va[32], vb[32];
-          tmem_ld32(taddr, va);
-          tmem_wait_ld(va);
-          drain_chunk<LONG, 0>(acc, taddr, va, vb);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acce0 + 8 * ab);
-          ab ^= 1;
-          if (ab == 0) aphase ^= 1u;
-        }
-        if (!ok) break;
-        const uint32_t offset = LONG ? 0u : static_cast<uint32_t>(nchunks) * kMagicBits;  // the 1.5 * 2^23 adds
+          if (!ok) break;
+          store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
+        } else {
+          // One chunk (none for an empty split): all kCols sums are loaded at
+          // once and the accumulator goes back to the MMA issuer before the
+          // reduction.
+          uint32_t x[kCols / 32][32];
+          if (nchunks > 0) {
+            if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(ab * BN + half * kCols);
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = static_cast<int32_t>(static_cast<uint32_t>(acc[e]) - offset);
-        store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
+            for (int q = 0; q < kCols / 32; ++q) tmem_ld32(taddr + 32 * q, x[q]);
+#pragma unroll
+            for (int q = 0; q < kCols / 32; ++q) tmem_wait_ld(x[q]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * ab);
+            ab ^= 1;
+            if (ab == 0) aphase ^= 1u;
+          } else {
+#pragma unroll
+            for (int q = 0; q < kCols / 32; ++q)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) x[q][e] = 0u;
+          }
+          if (!PAIRS && prm.out_kind == 0) {
+            store_residues_f32(x, w.p + ps, gi, gj0, prm);
+          } else {
+            int32_t acc[kCols];
+#pragma unroll
+            for (int e = 0; e < kCols; ++e) acc[e] = __float2int_rn(__uint_as_float(x[e / 32][e % 32]));
+            store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
+          }
+        }
       }
     }
   }
@@ -775,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kPairChunkKB = chunk_kb<true>();
+constexpr int kPairChunkKB = kChunkKB;
 
 // The CTA-pair kernel: tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
 // even CTA of a cluster of two; long (1024-term) chunks only.
@@ -944,10 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                  static_cast<uint32_t>(ab * BN + half * kCols);
-          uint32_t va[32], vb[32];
+          uint32_t va[32];
           tmem_ld32(taddr, va);
           tmem_wait_ld(va);
-          drain_chunk<true, 0>(acc, taddr, va, vb);
+          drain_chunk<0>(acc, taddr, va);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(cluster_addr(acce0 + 8 * ab, 0));
@@ -1120,7 +1176,7 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   prm.out_plane = out_plane;
   prm.out = out;
   // CTA pairs with long chunks once every split holds kPairMinK terms;
-  // single CTAs with short chunks otherwise
+  // single CTAs otherwise
   const bool pairs = static_cast<int64_t>(prm.kb_per_split) * BK >= kPairMinK;
   prm.tiles_m = static_cast<int>(pairs ? (M + kPairM - 1) / kPairM : (M + BM - 1) / BM);
   CUtensorMap tmA, tmB;
@@ -1128,7 +1184,8 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
       !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, pairs ? kBHalf : BN))
     return cudaErrorInvalidValue;
   const int64_t units = static_cast<int64_t>(prm.mod_units) * splits * prm.tiles_m * prm.tiles_n;
-  const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK >= 1024;
+  // several 1024-term chunks per split (int32 sums), or one (fp32 epilogue)
+  const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK > 1024;
   // PAIRS: the pair-residue output (out_kind 2) is compiled in only where used
   const bool po = out_kind == 2;
   auto kernel = pairs ? (po ? residue_gemm_pair_kernel<true> : residue_gemm_pair_kernel<false>)

@@ -1,18 +1,22 @@
 """GPU parity at the edges the kernels' exactness rests on, against the oracle.
 
 1. The residue GEMM runs on fp16 tensor cores with fp32 accumulators in TMEM.
-   It is exact only because every fp32 partial sum of a chunk is an integer
-   that fp32 holds exactly: at most 1024 * 2^14 = 2^24 in magnitude on the
-   1024-term chunks (converted with cvt.rni), at most 256 * 2^14 = 2^22 on
-   the 256-term chunks (converted by adding 1.5 * 2^23).  Residues drawn from
-   data keep chunk sums near 2^17, so these tests feed crafted slices that
-   drive every chunk to the bound (all products (-128)(-128) = 2^14: a chunk
-   sum of exactly 2^24, or 2^22), one odd small term short of it (1023
-   products of 2^14 and one of +-1, +-3, 127, ...), and the negative side
-   (products of -16256).  The int32 sums (out_kind 1) and the residues mod p
-   (out_kind 0) must equal the oracle's exact int64 sums bit for bit, on the
-   single-CTA kernel (K < 2048: 256-term chunks below K = 1024, 1024-term
-   from there) and on the CTA-pair kernel (K >= 2048).
+   It is exact only because every fp32 partial sum of a 1024-term chunk is
+   an integer that fp32 holds exactly (at most 1024 * 2^14 = 2^24 in
+   magnitude).  A K split of several chunks converts each with cvt.rni and
+   adds them in int32; a split of at most 1024 terms is one chunk, reduced
+   mod p in fp32 (q = round(x/p) estimated by an fma, r = x - q p exact).
+   Residues drawn from data keep chunk sums near 2^17, so these tests feed
+   crafted slices that drive every chunk to the bound (all products
+   (-128)(-128) = 2^14: a chunk sum of exactly K 2^14, up to 2^24), one odd
+   small term short of it (products of 2^14 and one of +-1, +-3, 127, ...),
+   and the negative side (products of -16256), plus one-chunk sums spread
+   over the whole range and every residue class, where the fp32 estimate of
+   round(x/p) can go either way.  The int32 sums (out_kind 1), the residues
+   mod p (out_kind 0) and the pair residues (out_kind 2) must equal the
+   oracle's exact sums bit for bit, on the single-CTA kernel (K < 2048: one
+   chunk up to K = 1024, several from there) and on the CTA-pair kernel
+   (K >= 2048).
 
 2. The combine's unscale rounds X 2^-(s+t) to nearest, ties to even, from
    integer bits (a funnel-shift path for normal results, a general one for
@@ -97,9 +101,9 @@ def crafted_operands(M, N, K, seed):
 
 @pytest.mark.parametrize("K", [1024, 1088, 2048, 3072, 4096])
 def test_gemm_chunk_sums_at_two_to_the_24(K):
-    """1024-term chunks (single CTA at K = 1024 and 1088, CTA pairs from 2048):
-    chunk sums of exactly 2^24, 2^24 - 2^14 + small odd terms, and their
-    negative counterparts, bit-exact."""
+    """1024-term chunks (single CTA at K = 1024, one chunk, and 1088, two;
+    CTA pairs from 2048): chunk sums of exactly 2^24, 2^24 - 2^14 + small
+    odd terms, and their negative counterparts, bit-exact."""
     M, N, n = 300, 260, 2
     ra, rb = crafted_operands(M, N, K, seed=K)
     raw, cmod = oracle.gemm_mod(ra, rb, n)
@@ -116,13 +120,13 @@ def test_gemm_chunk_sums_at_two_to_the_24(K):
 
 
 @pytest.mark.parametrize("K", [255, 256, 512, 768, 960])
-def test_gemm_chunk_sums_at_two_to_the_22(K):
-    """K below 1024: 256-term chunks converted by the 1.5 * 2^23 add; chunk
-    sums of exactly 2^22 (the add lands on 2^24) and just below, bit-exact."""
+def test_gemm_one_chunk_sums_at_the_bound(K):
+    """K below 1024, one chunk reduced in fp32: sums of exactly K 2^14 and
+    just below, and their negative counterparts, bit-exact."""
     M, N, n = 300, 260, 2
     ra, rb = crafted_operands(M, N, K, seed=K)
     raw, cmod = oracle.gemm_mod(ra, rb, n)
-    assert int(raw[0].max()) == K * 2**14  # every 256-term chunk of a full row/column is 2^22
+    assert int(raw[0].max()) == K * 2**14  # a full row/column of (-128)(-128)
     kpad = ozk.ozk_kpad(K)
     a_sl = f16_slices(ra, kpad)
     b_sl = f16_slices(rb.transpose(0, 2, 1), kpad)
@@ -130,6 +134,53 @@ def test_gemm_chunk_sums_at_two_to_the_22(K):
     assert np.array_equal(out32.cpu().numpy()[0, :, :, :N], raw)
     out8, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
     assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    assert ozk.ozk_stream_status() == 0
+
+
+def wide_sum_operands(n, M, N, K, seed):
+    """Residues whose sums spread over the whole exact range: each row of A
+    and column of B of one sign, magnitudes 88 to 128 (sums near +-K 2^13.5,
+    about +-2^23.5 at K = 1024), every seventh row of A small (|r| <= 3,
+    sums near zero, either sign) and one row of zeros."""
+    rng = np.random.default_rng(seed)
+    sa = rng.choice([-1, 1], size=(n, M, 1))
+    sb = rng.choice([-1, 1], size=(n, 1, N))
+    ra = np.where(sa > 0, 127 - rng.integers(0, 40, (n, M, K)), -128 + rng.integers(0, 40, (n, M, K)))
+    rb = np.where(sb > 0, 127 - rng.integers(0, 40, (n, K, N)), -128 + rng.integers(0, 40, (n, K, N)))
+    ra[:, ::7] = rng.integers(-3, 4, ra[:, ::7].shape)
+    ra[:, 3] = 0
+    return ra.astype(np.int8), rb.astype(np.int8)
+
+
+@pytest.mark.parametrize("K", [1024, 333, 64])
+def test_gemm_one_chunk_residues_over_the_whole_range(K):
+    """One-chunk sums over [-2^24, 2^24] and every residue class of all 20
+    moduli, among them sums within 2^-7 p of a half-integer multiple of p
+    (x/p = j + 1/2 +- 1/(2p)), where at K = 1024 the fp32 estimate of
+    round(x/p) is off by one for several hundred: residues (out_kind 0), int32 sums (1) and pair residues
+    (2) bit-exact against the oracle."""
+    M, N, n = 300, 260, 20
+    ra, rb = wide_sum_operands(n, M, N, K, seed=K + 11)
+    raw, cmod = oracle.gemm_mod(ra, rb, n)
+    ps = [int(p) for p in oracle.moduli(n)]
+    x = raw.astype(np.int64)
+    assert np.abs(x).max() > K * 2**13
+    near_half = [np.count_nonzero(np.isin(x[k] % p, [(p - 1) // 2, (p + 1) // 2, p // 2]) & (np.abs(x[k]) > K * 2**13))
+                 for k, p in enumerate(ps)]
+    assert min(near_half) > 20
+    kpad = ozk.ozk_kpad(K)
+    a_sl = f16_slices(ra, kpad)
+    b_sl = f16_slices(rb.transpose(0, 2, 1), kpad)
+    out8, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=0)
+    assert np.array_equal(out8.cpu().numpy()[:, :, :N], cmod)
+    out32, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=1)
+    assert np.array_equal(out32.cpu().numpy()[0, :, :, :N], raw)
+    out16, _ = run_gemm(a_sl, b_sl, M, N, K, n, out_kind=2)
+    g16 = out16.cpu().numpy()[:, :, :N].view(np.uint16).astype(np.int64)
+    for j in range(n // 2):
+        assert np.all(g16[j] < ps[2 * j] * ps[2 * j + 1])
+        assert np.array_equal(g16[j] % ps[2 * j], cmod[2 * j].astype(np.int64))
+        assert np.array_equal(g16[j] % ps[2 * j + 1], cmod[2 * j + 1].astype(np.int64))
     assert ozk.ozk_stream_status() == 0
 
 
