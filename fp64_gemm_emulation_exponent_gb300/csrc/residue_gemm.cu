@@ -44,6 +44,8 @@
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
+#include <cstdint>
+#include <cstring>
 #include <map>
 #include <mutex>
 
@@ -83,7 +85,7 @@ static_assert(2 * BN <= static_cast<int>(kTmemCols), "two accumulators fit the a
 // mbarriers after the ring: full and empty per stage, two accumulator-full,
 // two accumulator-empty, one drain; then the TMEM address and the abort flag
 constexpr int kNumBars = 2 * kStages + 5;
-constexpr size_t kBarBytes = 256;
+constexpr size_t kBarBytes = 1024;  // keeps the stash after it 1024-byte aligned (128-byte swizzle)
 static_assert(8 * kNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 // CTA-pair kernel: each CTA holds 128 rows of A and half of the B tile per
@@ -98,9 +100,14 @@ constexpr int kPairNumBars = 2 * kPairStages + 5;
 static_assert(8 * kPairNumBars + 8 <= static_cast<int>(kBarBytes), "barrier block overflows");
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kBarBytes;
 // out_kind 2: each epilogue thread parks the residues of the first modulus of
-// a pair (kCols bytes) in shared memory until the second modulus is done
+// a pair (kCols bytes) in shared memory until the second modulus is done.
+// out_kind 0 from one chunk: the same bytes stage each warp's 32 x kCols
+// residue block for one TMA store (rows of kCols = 128 bytes, 128-byte
+// swizzle).
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr size_t kStashBytes = static_cast<size_t>(kEpiThreads) * kCols;
+static_assert(kCols == 128, "a staged residue row is one 128-byte swizzle row");
+constexpr uint32_t kStageOutBytes = 32 * kCols;  // one warp's block
 static_assert(kSmemBytes + kStashBytes <= 232448 && kPairSmemBytes + kStashBytes <= 232448,
               "ring, barriers and stash exceed the shared memory of a CTA");
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // limit of every pipeline wait in normal runs
@@ -253,6 +260,35 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// TMA store of a box from shared memory (bulk-group completion), and the
+// waits on this thread's bulk groups: until their shared-memory source has
+// been read, or until their writes are done.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory visible to the
+// async proxy (a following TMA store).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -578,36 +614,42 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
   }
 }
 
-// out_kind 0 from the fp32 sums of a one-chunk split: (x mod p) as uint8 in
-// plane p for this thread's kCols columns gj0.. of row gi, 16 per store.
-__device__ __forceinline__ void store_residues_f32(const uint32_t (&x)[kCols / 32][32], int p, int64_t gi,
-                                                   int64_t gj0, const GemmParams& prm) {
-  if (gi >= prm.M) return;
+// out_kind 0 from one chunk through a TMA store: the warp's 32 rows x kCols
+// residues go into its staging block (16-byte chunk c of row r at chunk
+// c ^ (r & 7), the 128-byte swizzle), then lane 0 stores the block as one
+// 128 x 32 box at (gj0, row0, p); the map clips rows >= M and columns >= ldo.
+// The staging block is rewritten only after the previous store has read it.
+__device__ __forceinline__ void store_residues_tma(const uint32_t (&x)[kCols / 32][32], int p, int64_t row0,
+                                                   int64_t gj0, uint32_t stage, const CUtensorMap* tmO,
+                                                   int lane) {
   const float pf = static_cast<float>(c_mod.p[p]), inv = c_mod.inv[p], pmagic = kMagic + pf;
-  uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(p) * prm.out_plane + gi * prm.ldo + gj0;
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * kCols;
 #pragma unroll
   for (int v = 0; v < kCols / 16; ++v) {
-    if (gj0 + 16 * v < prm.ldo) {
-      uint32_t word[4];
+    uint32_t word[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int e = 16 * v + 4 * b;
-        const uint32_t* xs = &x[e / 32][e % 32];
-        const uint32_t lo = __byte_perm(residue_bits(xs[0], pf, inv, pmagic), residue_bits(xs[1], pf, inv, pmagic),
-                                        0x0040);
-        const uint32_t hi = __byte_perm(residue_bits(xs[2], pf, inv, pmagic), residue_bits(xs[3], pf, inv, pmagic),
-                                        0x0040);
-        word[b] = __byte_perm(lo, hi, 0x5410);
-      }
-      *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+    for (int b = 0; b < 4; ++b) {
+      const int e = 16 * v + 4 * b;
+      const uint32_t* xs = &x[e / 32][e % 32];
+      const uint32_t lo = __byte_perm(residue_bits(xs[0], pf, inv, pmagic), residue_bits(xs[1], pf, inv, pmagic),
+                                      0x0040);
+      const uint32_t hi = __byte_perm(residue_bits(xs[2], pf, inv, pmagic), residue_bits(xs[3], pf, inv, pmagic),
+                                      0x0040);
+      word[b] = __byte_perm(lo, hi, 0x5410);
     }
+    st_shared_v4(row + static_cast<uint32_t>((v ^ (lane & 7)) * 16), word[0], word[1], word[2], word[3]);
   }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) tma_store_3d(tmO, stage, static_cast<int>(gj0), static_cast<int>(row0), p);
 }
 
 template <bool LONG, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
-    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
+    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
@@ -751,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aphase = 0;
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kStages * kStageBytes + kBarBytes) + (threadIdx.x - 128);
+    const uint32_t out_stage = smem_u32(smem + kStages * kStageBytes + kBarBytes) + static_cast<uint32_t>(ew) * kStageOutBytes;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit w = decode_unit<PAIRS>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
@@ -810,7 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 32; ++e) x[q][e] = 0u;
           }
           if (!PAIRS && prm.out_kind == 0) {
-            store_residues_f32(x, w.p + ps, gi, gj0, prm);
+            if (gj0 < prm.ldo && gi - lane < prm.M)  // boxes wholly outside the planes are not stored
+              store_residues_tma(x, w.p + ps, gi - lane, gj0, out_stage, &tmO, lane);
           } else {
             int32_t acc[kCols];
 #pragma unroll
@@ -820,6 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // the residue stores in flight finish before the CTA's shared memory goes
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -837,8 +883,8 @@ constexpr int kPairChunkKB = kChunkKB;
 // even CTA of a cluster of two; long (1024-term) chunks only.
 template <bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
-    residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams prm) {
+    residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
@@ -1064,6 +1110,21 @@ bool make_slice_map(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of the uint8 residue planes (row stride ldo, plane stride
+// out_plane bytes) for TMA stores of one warp's 128 x 32 block.
+bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t ldo, int64_t out_plane, int n) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(ldo), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(n)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldo), static_cast<cuuint64_t>(out_plane)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kCols), 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
@@ -1186,6 +1247,12 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   const int64_t units = static_cast<int64_t>(prm.mod_units) * splits * prm.tiles_m * prm.tiles_n;
   // several 1024-term chunks per split (int32 sums), or one (fp32 epilogue)
   const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK > 1024;
+  // the one-chunk epilogue writes residue planes by TMA stores (the callers
+  // give a 16-byte aligned base, ldo and plane stride)
+  CUtensorMap tmO;
+  memset(&tmO, 0, sizeof(tmO));
+  if (out_kind == 0 && !pairs && !long_chunks && !make_out_map(&tmO, out, M, ldo, out_plane, n))
+    return cudaErrorInvalidValue;
   // PAIRS: the pair-residue output (out_kind 2) is compiled in only where used
   const bool po = out_kind == 2;
   auto kernel = pairs ? (po ? residue_gemm_pair_kernel<true> : residue_gemm_pair_kernel<false>)
@@ -1198,7 +1265,7 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   if (e != cudaSuccess) return e;
   if (!pairs) {
     const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
-    kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, prm);
+    kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, tmO, prm);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1209,7 +1276,7 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   if (resident < npairs) npairs = resident;
   if (units < npairs) npairs = units;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);  // clusters of two CTAs
-  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, prm);
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmO, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

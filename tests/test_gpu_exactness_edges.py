@@ -184,6 +184,33 @@ def test_gemm_one_chunk_residues_over_the_whole_range(K):
     assert ozk.ozk_stream_status() == 0
 
 
+def test_gemm_one_chunk_residue_planes_by_tma_store():
+    """The one-chunk epilogue writes the residue planes by TMA stores of
+    128 x 32 boxes, clipped at M and ldo: bit-exact against the oracle with
+    ragged M and N, at two base offsets, and nothing written outside the
+    planes; a base off the 16-byte grid is refused before any launch."""
+    M, N, K, n = 333, 200, 500, 14
+    ra, rb = wide_sum_operands(n, M, N, K, seed=3)
+    _, cmod = oracle.gemm_mod(ra, rb, n)
+    kpad = ozk.ozk_kpad(K)
+    a_sl = f16_slices(ra, kpad)
+    b_sl = f16_slices(rb.transpose(0, 2, 1), kpad)
+    ldo = (N + 15) // 16 * 16
+    for offset in (0, 16):
+        buf = torch.full((offset + n * M * ldo + 64,), 0xEE, dtype=torch.uint8, device="cuda")
+        out = buf[offset:offset + n * M * ldo].view(n, M, ldo)
+        ozk.ozk_residue_gemm(M, N, K, a_sl, b_sl, n, 0, out, ldo, 1)
+        got = buf.cpu().numpy()
+        assert np.all(got[:offset] == 0xEE) and np.all(got[offset + n * M * ldo:] == 0xEE)
+        assert np.array_equal(out.cpu().numpy()[:, :, :N], cmod)
+    buf = torch.full((8 + n * M * ldo,), 0xEE, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ozk.OzkError) as e:
+        ozk.ozk_residue_gemm(M, N, K, a_sl, b_sl, n, 0, buf[8:].view(n, M, ldo), ldo, 1)
+    assert e.value.status == ozk.OZK_ERR_INVALID_ARG
+    assert np.all(buf.cpu().numpy() == 0xEE)
+    assert ozk.ozk_stream_status() == 0
+
+
 def test_gemm_chunk_bound_split_k():
     """Split-K shares of the CTA-pair kernel, each share's chunks at 2^24."""
     M, N, n, K, splits = 260, 300, 2, 6144, 3
