@@ -515,17 +515,53 @@ __device__ __forceinline__ void drain_chunk(int32_t (&acc)[kCols], uint32_t tadd
   }
 }
 
-// (x mod p) for an fp32 sum x of one chunk (an integer, |x| <= 2^24), as
-// the low byte of the returned fp32 bits.  q = rint(x * (1/p)) by one fma
-// with the 1.5 * 2^23 add: x * (1/p) is within |x| p^-1 2^-24 < 2^-7 of
-// x / p, so q is x / p rounded up or down and |x - q p| < p; the fma gives
-// r = x - q p exactly, and r + p if r < 0 is the residue in [0, p), whose
-// sum with 1.5 * 2^23 carries it in the low mantissa bits.
-__device__ __forceinline__ uint32_t residue_bits(uint32_t xbits, float pf, float inv, float pmagic) {
-  const float x = __uint_as_float(xbits);
-  const float q = __fsub_rn(__fmaf_rn(x, inv, kMagic), kMagic);
-  const float r = __fmaf_rn(-q, pf, x);
-  return __float_as_uint(__fadd_rn(r, r < 0.0f ? pmagic : kMagic));
+// Packed fp32 pairs (f32x2: one instruction for two lanes of data).
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack2f(float v) {
+  return pack2(__float_as_uint(v), __float_as_uint(v));
+}
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2_rm(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Per-modulus constants of residues2, each in both halves of a pair.
+struct ResidueConsts {
+  uint64_t inv, magic, neg_magic, neg_p;
+};
+__device__ __forceinline__ ResidueConsts residue_consts(int p) {
+  return {pack2f(c_mod.inv[p]), pack2f(kMagic), pack2f(-kMagic), pack2f(-static_cast<float>(c_mod.p[p]))};
+}
+
+// (x mod p) of two fp32 sums of one chunk (integers, |x| <= 2^24), each as
+// the low byte of its half of the result, every step exact:
+//   q = rint(x * (1/p)) by one fma with the 1.5 * 2^23 add (ulp 1 there):
+//     x * (1/p) is within |x| p^-1 2^-24 < 2^-7 of x / p, so q is x / p
+//     rounded up or down and r = x - q p, formed exactly by an fma, lies in
+//     (-p, p);
+//   k = floor(r * (1/p)) in {-1, 0} by an fma with the same add rounding
+//     toward minus infinity, and r - k p, exact, is the residue in [0, p);
+//   adding 1.5 * 2^23 puts it in the low mantissa bits.
+__device__ __forceinline__ uint64_t residues2(uint64_t x, const ResidueConsts& c) {
+  const uint64_t q = add2_rn(fma2_rn(x, c.inv, c.magic), c.neg_magic);
+  const uint64_t r = fma2_rn(q, c.neg_p, x);
+  const uint64_t k = add2_rn(fma2_rm(r, c.inv, c.magic), c.neg_magic);
+  return add2_rn(fma2_rn(k, c.neg_p, r), c.magic);
 }
 
 // x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
@@ -622,7 +658,7 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
 __device__ __forceinline__ void store_residues_tma(const uint32_t (&x)[kCols / 32][32], int p, int64_t row0,
                                                    int64_t gj0, uint32_t stage, const CUtensorMap* tmO,
                                                    int lane) {
-  const float pf = static_cast<float>(c_mod.p[p]), inv = c_mod.inv[p], pmagic = kMagic + pf;
+  const ResidueConsts rc = residue_consts(p);
   if (lane == 0) bulk_wait_read();
   __syncwarp();
   const uint32_t row = stage + static_cast<uint32_t>(lane) * kCols;
@@ -633,10 +669,9 @@ __device__ __forceinline__ void store_residues_tma(const uint32_t (&x)[kCols / 3
     for (int b = 0; b < 4; ++b) {
       const int e = 16 * v + 4 * b;
       const uint32_t* xs = &x[e / 32][e % 32];
-      const uint32_t lo = __byte_perm(residue_bits(xs[0], pf, inv, pmagic), residue_bits(xs[1], pf, inv, pmagic),
-                                      0x0040);
-      const uint32_t hi = __byte_perm(residue_bits(xs[2], pf, inv, pmagic), residue_bits(xs[3], pf, inv, pmagic),
-                                      0x0040);
+      const uint64_t r01 = residues2(pack2(xs[0], xs[1]), rc), r23 = residues2(pack2(xs[2], xs[3]), rc);
+      const uint32_t lo = __byte_perm(static_cast<uint32_t>(r01), static_cast<uint32_t>(r01 >> 32), 0x0040);
+      const uint32_t hi = __byte_perm(static_cast<uint32_t>(r23), static_cast<uint32_t>(r23 >> 32), 0x0040);
       word[b] = __byte_perm(lo, hi, 0x5410);
     }
     st_shared_v4(row + static_cast<uint32_t>((v ^ (lane & 7)) * 16), word[0], word[1], word[2], word[3]);
