@@ -127,15 +127,26 @@ constexpr uint32_t kPairIdesc = (1u << 4) |  // M of the whole pair
                                 (static_cast<uint32_t>(BN >> 3) << 17) |
                                 (static_cast<uint32_t>(kPairM >> 4) << 24);
 
-// Per modulus: p, and the constants of mod_p.  Per pair of moduli (2j, 2j+1)
+// Per modulus: p, 1/p rounded up to fp32, and the constants of mod_p.  Per
+// pair of moduli (2j, 2j+1)
 // with m = p_2j p_2j+1: u0 = 1 mod p_2j and 0 mod p_2j+1, u1 the other way
 // round, so (c_2j u0 + c_2j+1 u1) mod m is the residue of the pair modulus;
 // t < 2^25 is divided exactly as umulhi(t, ceil(2^42 / m)) >> 10.
 struct ModTable {
   uint32_t p[kMaxModuli], magic[kMaxModuli], bias[kMaxModuli];
-  float inv[kMaxModuli];  // 1/p rounded to nearest fp32
+  float inv_up[kMaxModuli];
   uint32_t pu0[kMaxModuli / 2], pu1[kMaxModuli / 2], pm[kMaxModuli / 2], pmagic[kMaxModuli / 2];
 };
+
+// 1/p rounded up to fp32 (p <= 256): the nearest value, raised by one ulp
+// when it lies below 1/p.
+__host__ __device__ constexpr float inverse_up(uint32_t p) {
+  const float inv = 1.0f / static_cast<float>(p);
+  if (static_cast<double>(inv) * p >= 1.0) return inv;
+  float ulp = 1.0f;
+  while (ulp > inv) ulp *= 0.5f;  // the power of two at or below inv
+  return inv + ulp * (1.0f / 8388608.0f);
+}
 
 __host__ __device__ constexpr uint32_t inverse_mod(uint32_t a, uint32_t p) {
   for (uint32_t x = 1; x < p; ++x)
@@ -149,7 +160,7 @@ __host__ __device__ constexpr ModTable make_mod_table() {
     t.p[k] = modulus_at(k);
     t.magic[k] = magic_of(t.p[k]);
     t.bias[k] = bias_of(t.p[k]);
-    t.inv[k] = 1.0f / static_cast<float>(t.p[k]);
+    t.inv_up[k] = inverse_up(t.p[k]);
   }
   for (int j = 0; j < kMaxModuli / 2; ++j) {
     const uint32_t pa = modulus_at(2 * j), pb = modulus_at(2 * j + 1);
@@ -540,28 +551,94 @@ __device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Per-modulus constants of residues2, each in both halves of a pair.
+// Per-modulus constants of the residue steps, each in both halves of a
+// pair: 1/p rounded up, 1.5 * 2^23 and its negation, -p.
 struct ResidueConsts {
   uint64_t inv, magic, neg_magic, neg_p;
 };
 __device__ __forceinline__ ResidueConsts residue_consts(int p) {
-  return {pack2f(c_mod.inv[p]), pack2f(kMagic), pack2f(-kMagic), pack2f(-static_cast<float>(c_mod.p[p]))};
+  return {pack2f(c_mod.inv_up[p]), pack2f(kMagic), pack2f(-kMagic), pack2f(-static_cast<float>(c_mod.p[p]))};
 }
 
-// (x mod p) of two fp32 sums of one chunk (integers, |x| <= 2^24), each as
-// the low byte of its half of the result, every step exact:
-//   q = rint(x * (1/p)) by one fma with the 1.5 * 2^23 add (ulp 1 there):
-//     x * (1/p) is within |x| p^-1 2^-24 < 2^-7 of x / p, so q is x / p
-//     rounded up or down and r = x - q p, formed exactly by an fma, lies in
-//     (-p, p);
-//   k = floor(r * (1/p)) in {-1, 0} by an fma with the same add rounding
-//     toward minus infinity, and r - k p, exact, is the residue in [0, p);
-//   adding 1.5 * 2^23 puts it in the low mantissa bits.
-__device__ __forceinline__ uint64_t residues2(uint64_t x, const ResidueConsts& c) {
-  const uint64_t q = add2_rn(fma2_rn(x, c.inv, c.magic), c.neg_magic);
-  const uint64_t r = fma2_rn(q, c.neg_p, x);
-  const uint64_t k = add2_rn(fma2_rm(r, c.inv, c.magic), c.neg_magic);
-  return add2_rn(fma2_rn(k, c.neg_p, r), c.magic);
+// Cuts two fp32 chunk sums (integers, |x| <= 2^24) to r = x - q p with
+// q = rint(x * (1/p)), from one fma with the 1.5 * 2^23 add (ulp 1 there):
+// x * (1/p) lies within |x| p^-1 2^-23 < 0.012 of x / p, so q is x / p
+// rounded up or down, |r| < 0.512 p, and the fma forms r exactly.  q_shift
+// is -(1.5 * 2^23 + s): r comes out s p higher.
+__device__ __forceinline__ uint64_t cut2(uint64_t x, const ResidueConsts& c, uint64_t q_shift) {
+  return fma2_rn(add2_rn(fma2_rn(x, c.inv, c.magic), q_shift), c.neg_p, x);
+}
+
+// The residues mod p of two integers 0 <= R < 2^22, each as the low byte of
+// its half of the result: k = floor(R * (1/p)) by an fma with the
+// 1.5 * 2^23 add rounding toward minus infinity.  With 1/p rounded up,
+// R * (1/p) is at least R / p and exceeds it by less than R 2^-23 / p, which
+// stays below the distance 1/p from R / p to the next integer while
+// R < 2^23; so k = floor(R / p), R - k p (exact, by an fma) is the residue,
+// and adding 1.5 * 2^23 puts it in the low mantissa bits.  For -p < R < 0
+// the same steps give k = -1 and again the residue.
+__device__ __forceinline__ uint64_t floor_residues2(uint64_t R, const ResidueConsts& c) {
+  const uint64_t k = add2_rn(fma2_rm(R, c.inv, c.magic), c.neg_magic);
+  return add2_rn(fma2_rn(k, c.neg_p, R), c.magic);
+}
+
+// Low bytes of the four fp32 words in a and b, in order.
+__device__ __forceinline__ uint32_t low_bytes4(uint64_t a, uint64_t b) {
+  const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(a >> 32), 0x0040);
+  const uint32_t hi = __byte_perm(static_cast<uint32_t>(b), static_cast<uint32_t>(b >> 32), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+// Residue words (bytes of columns 4i .. 4i+3 in words[i]) of one chunk:
+// r from cut2 lies in (-p, p), where floor_residues2 applies.
+__device__ __forceinline__ void one_chunk_words(const uint32_t (&x)[kCols / 32][32], uint32_t (&words)[kCols / 4],
+                                                const ResidueConsts& c) {
+#pragma unroll
+  for (int i = 0; i < kCols / 4; ++i) {
+    const uint32_t* xs = &x[(4 * i) / 32][(4 * i) % 32];
+    words[i] = low_bytes4(floor_residues2(cut2(pack2(xs[0], xs[1]), c, c.neg_magic), c),
+                          floor_residues2(cut2(pack2(xs[2], xs[3]), c, c.neg_magic), c));
+  }
+}
+
+// Several chunks: each chunk's sums are cut (cut2) and the cut values added
+// up in fp32 pairs R.  The first chunk's quotient is lowered by the number of
+// chunks nc, which adds nc p to R, so R ends in (0.48 nc p, 1.52 nc p): a
+// positive integer below 2^22 (nc <= 128, K < 2^17), exact in fp32, and
+// floor_residues2 reduces it.  This adds the 32 columns of block Q (loaded
+// in cur) and loads and adds the blocks after it.
+template <bool FIRST, int Q>
+__device__ __forceinline__ void cut_chunk(uint64_t (&R)[kCols / 2], uint32_t taddr, uint32_t (&cur)[32],
+                                          const ResidueConsts& c, uint64_t first_shift) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint64_t r = cut2(pack2(cur[2 * e], cur[2 * e + 1]), c, FIRST ? first_shift : c.neg_magic);
+    R[16 * Q + e] = FIRST ? r : add2_rn(R[16 * Q + e], r);
+  }
+  if constexpr (Q + 1 < kCols / 32) {
+    tmem_ld32(taddr + 32 * (Q + 1), cur);
+    tmem_wait_ld(cur);
+    cut_chunk<FIRST, Q + 1>(R, taddr, cur, c, first_shift);
+  }
+}
+
+__device__ __forceinline__ void chunk_words(const uint64_t (&R)[kCols / 2], uint32_t (&words)[kCols / 4],
+                                            const ResidueConsts& c) {
+#pragma unroll
+  for (int i = 0; i < kCols / 4; ++i) words[i] = low_bytes4(floor_residues2(R[2 * i], c), floor_residues2(R[2 * i + 1], c));
+}
+
+// out_kind 1: the exact int32 sums of this thread's kCols columns gj0.. of
+// row gi, in plane (sk, p).
+__device__ __forceinline__ void store_sums(const int32_t (&acc)[kCols], const Unit& w, int ps, int64_t gi,
+                                           int64_t gj0, const GemmParams& prm) {
+  if (gi >= prm.M) return;
+  int32_t* dst = static_cast<int32_t*>(prm.out) +
+                 (static_cast<int64_t>(w.sk) * prm.n + w.p + ps) * prm.out_plane + gi * prm.ldo + gj0;
+#pragma unroll
+  for (int v = 0; v < kCols / 4; ++v)
+    if (gj0 + 4 * v < prm.ldo)
+      *reinterpret_cast<int4*>(dst + 4 * v) = make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
 }
 
 // x mod p in [0, p) for an exact int32 dot product (|x| < 2^31 - 2^14).
@@ -573,55 +650,98 @@ __device__ __forceinline__ uint32_t mod_p(int32_t x, uint32_t p, uint32_t magic,
   return static_cast<uint32_t>(r);
 }
 
-// Writes pass ps of unit w for this thread's kCols columns gj0.. of row gi,
-// acc holding the exact int32 sums.  out_kind 0: (x mod p) as uint8 in plane p;
-// 1: x as int32 in plane (sk, p); 2: pass 0 of a pair parks (x mod p) in the
-// thread's stash slots (stash[v * kEpiThreads]), pass 1 combines it with its
-// own residue into the pair residue, written as uint16 in plane q (an odd
-// last modulus writes its own residue there).
-template <bool PAIRS>
-__device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Unit& w, int ps, int64_t gi,
-                                           int64_t gj0, const GemmParams& prm, uint4* stash) {
+// Combines the residues of the moduli of pair q into the pair residue:
+// (c_2j u0 + c_2j+1 u1) mod p_2j p_2j+1 (< 2^25 before the reduction).
+__device__ __forceinline__ uint32_t pair_residue(uint32_t c0, uint32_t c1, uint32_t u0, uint32_t u1, uint32_t m,
+                                                 uint32_t pmg) {
+  const uint32_t t = c0 * u0 + c1 * u1;
+  return t - (__umulhi(t, pmg) >> 10) * m;
+}
+
+// out_kind 2 from exact int32 sums (several chunks: the int32 drain is the
+// cheaper one per chunk once a split holds about six or more): pass 0 of a
+// pair parks the residues mod p in the thread's stash slots
+// (stash[v * kEpiThreads]); pass 1 combines them with its own into the pair
+// residue, written as uint16 in plane q (an odd last modulus writes its own
+// residue there).
+__device__ __forceinline__ void store_pair_sums(const int32_t (&acc)[kCols], const Unit& w, int ps, int64_t gi,
+                                                int64_t gj0, const GemmParams& prm, uint4* stash) {
   const int p = w.p + ps;
   const uint32_t pp = c_mod.p[p], mg = c_mod.magic[p], bs = c_mod.bias[p];
-  if (PAIRS && ps == 0 && w.passes == 2) {
+  if (ps == 0 && w.passes == 2) {
 #pragma unroll
     for (int v = 0; v < kCols / 16; ++v) {
       uint32_t word[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        word[b] = mod_p(acc[16 * v + 4 * b], pp, mg, bs) | (mod_p(acc[16 * v + 4 * b + 1], pp, mg, bs) << 8) |
-                  (mod_p(acc[16 * v + 4 * b + 2], pp, mg, bs) << 16) |
-                  (mod_p(acc[16 * v + 4 * b + 3], pp, mg, bs) << 24);
+        const int e = 16 * v + 4 * b;
+        word[b] = mod_p(acc[e], pp, mg, bs) | (mod_p(acc[e + 1], pp, mg, bs) << 8) |
+                  (mod_p(acc[e + 2], pp, mg, bs) << 16) | (mod_p(acc[e + 3], pp, mg, bs) << 24);
       }
       stash[v * kEpiThreads] = make_uint4(word[0], word[1], word[2], word[3]);
     }
     return;
   }
   if (gi >= prm.M) return;
-  if (!PAIRS && prm.out_kind == 0) {
-    uint8_t* dst = static_cast<uint8_t*>(prm.out) + static_cast<int64_t>(p) * prm.out_plane + gi * prm.ldo + gj0;
+  uint16_t* dst = static_cast<uint16_t*>(prm.out) + static_cast<int64_t>(w.q) * prm.out_plane + gi * prm.ldo + gj0;
+  const bool pair = w.passes == 2;
+  const uint32_t u0 = c_mod.pu0[w.q], u1 = c_mod.pu1[w.q], m = c_mod.pm[w.q], pmg = c_mod.pmagic[w.q];
 #pragma unroll
-    for (int v = 0; v < kCols / 16; ++v) {
-      if (gj0 + 16 * v < prm.ldo) {
-        uint32_t word[4];
+  for (int v = 0; v < kCols / 16; ++v) {
+    const uint4 first = pair ? stash[v * kEpiThreads] : make_uint4(0, 0, 0, 0);
+    const uint32_t fw[4] = {first.x, first.y, first.z, first.w};
+    uint32_t r[16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          word[b] = mod_p(acc[16 * v + 4 * b], pp, mg, bs) | (mod_p(acc[16 * v + 4 * b + 1], pp, mg, bs) << 8) |
-                    (mod_p(acc[16 * v + 4 * b + 2], pp, mg, bs) << 16) |
-                    (mod_p(acc[16 * v + 4 * b + 3], pp, mg, bs) << 24);
-        }
-        *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
-      }
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t c = mod_p(acc[16 * v + e], pp, mg, bs);
+      r[e] = pair ? pair_residue((fw[e >> 2] >> (8 * (e & 3))) & 0xFFu, c, u0, u1, m, pmg) : c;
     }
-  } else if (!PAIRS) {  // out_kind 1
-    int32_t* dst = static_cast<int32_t*>(prm.out) + (static_cast<int64_t>(w.sk) * prm.n + p) * prm.out_plane +
-                   gi * prm.ldo + gj0;
 #pragma unroll
-    for (int v = 0; v < kCols / 4; ++v)
-      if (gj0 + 4 * v < prm.ldo)
-        *reinterpret_cast<int4*>(dst + 4 * v) = make_int4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+    for (int h = 0; h < 2; ++h)
+      if (gj0 + 16 * v + 8 * h < prm.ldo)
+        *reinterpret_cast<uint4*>(dst + 16 * v + 8 * h) =
+            make_uint4(r[8 * h] | (r[8 * h + 1] << 16), r[8 * h + 2] | (r[8 * h + 3] << 16),
+                       r[8 * h + 4] | (r[8 * h + 5] << 16), r[8 * h + 6] | (r[8 * h + 7] << 16));
+  }
+}
+
+// Writes the residue words of pass ps of unit w, for this thread's kCols
+// columns gj0.. of row row0 + lane (row0: the warp's first row).
+//  out_kind 0 (!PAIRS): a TMA store.  The warp's 32 x kCols bytes go into its
+//    staging block (16-byte chunk v of row r at chunk v ^ (r & 7), the
+//    128-byte swizzle; rewritten only after the previous store has read it),
+//    then lane 0 stores the block as one 128 x 32 box at (gj0, row0, p); the
+//    map clips rows >= M and columns >= ldo, and a box wholly outside is
+//    not stored.
+//  out_kind 2 (PAIRS): pass 0 of a pair parks the residues in the thread's
+//    stash slots (stash[v * kEpiThreads]); pass 1 combines them with its own
+//    into the pair residue, written as uint16 in plane q (an odd last modulus
+//    writes its own residue there).
+template <bool PAIRS>
+__device__ __forceinline__ void store_words(const uint32_t (&words)[kCols / 4], const Unit& w, int ps, int64_t row0,
+                                            int lane, int64_t gj0, const GemmParams& prm, uint4* stash,
+                                            uint32_t stage, const CUtensorMap* tmO) {
+  if constexpr (!PAIRS) {
+    if (gj0 >= prm.ldo || row0 >= prm.M) return;  // the same for the whole warp
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+    const uint32_t row = stage + static_cast<uint32_t>(lane) * kCols;
+#pragma unroll
+    for (int v = 0; v < kCols / 16; ++v)
+      st_shared_v4(row + static_cast<uint32_t>((v ^ (lane & 7)) * 16), words[4 * v], words[4 * v + 1],
+                   words[4 * v + 2], words[4 * v + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_3d(tmO, stage, static_cast<int>(gj0), static_cast<int>(row0), w.p + ps);
   } else {
+    if (ps == 0 && w.passes == 2) {
+#pragma unroll
+      for (int v = 0; v < kCols / 16; ++v)
+        stash[v * kEpiThreads] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
+      return;
+    }
+    const int64_t gi = row0 + lane;
+    if (gi >= prm.M) return;
     uint16_t* dst = static_cast<uint16_t*>(prm.out) + static_cast<int64_t>(w.q) * prm.out_plane + gi * prm.ldo + gj0;
     const bool pair = w.passes == 2;
     const uint32_t u0 = c_mod.pu0[w.q], u1 = c_mod.pu1[w.q], m = c_mod.pm[w.q], pmg = c_mod.pmagic[w.q];
@@ -632,13 +752,8 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
       uint32_t r[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const uint32_t c = mod_p(acc[16 * v + e], pp, mg, bs);
-        if (pair) {
-          const uint32_t t = ((fw[e >> 2] >> (8 * (e & 3))) & 0xFFu) * u0 + c * u1;  // < 2^25
-          r[e] = t - (__umulhi(t, pmg) >> 10) * m;
-        } else {
-          r[e] = c;
-        }
+        const uint32_t c = (words[4 * v + (e >> 2)] >> (8 * (e & 3))) & 0xFFu;
+        r[e] = pair ? pair_residue((fw[e >> 2] >> (8 * (e & 3))) & 0xFFu, c, u0, u1, m, pmg) : c;
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -650,38 +765,107 @@ __device__ __forceinline__ void store_tile(const int32_t (&acc)[kCols], const Un
   }
 }
 
-// out_kind 0 from one chunk through a TMA store: the warp's 32 rows x kCols
-// residues go into its staging block (16-byte chunk c of row r at chunk
-// c ^ (r & 7), the 128-byte swizzle), then lane 0 stores the block as one
-// 128 x 32 box at (gj0, row0, p); the map clips rows >= M and columns >= ldo.
-// The staging block is rewritten only after the previous store has read it.
-__device__ __forceinline__ void store_residues_tma(const uint32_t (&x)[kCols / 32][32], int p, int64_t row0,
-                                                   int64_t gj0, uint32_t stage, const CUtensorMap* tmO,
-                                                   int lane) {
-  const ResidueConsts rc = residue_consts(p);
-  if (lane == 0) bulk_wait_read();
-  __syncwarp();
-  const uint32_t row = stage + static_cast<uint32_t>(lane) * kCols;
+// One pass of one unit in an epilogue warp: takes the pass's nchunks
+// accumulators from TMEM (tbase: this warp's lanes and columns of buffer 0),
+// waiting on the accumulator-full barrier and handing each buffer back
+// through release(ab), and writes the pass's output.  Returns false if a wait
+// ran out.
+//  out_kind 1, and 2 over several chunks: exact int32 sums (cvt.rni and
+//    int32 adds per chunk).
+//  out_kind 0, and 2 from one chunk: residues in fp32 throughout (one chunk:
+//    one_chunk_words; several: cut_chunk and chunk_words).
+template <bool LONG, int KIND, typename Release>
+__device__ __forceinline__ bool epilogue_pass(const Unit& w, int ps, int nchunks, int64_t row0, int lane,
+                                              int64_t gj0, const GemmParams& prm, uint4* stash, uint32_t out_stage,
+                                              const CUtensorMap* tmO, uint32_t tbase, uint32_t accf0,
+                                              volatile int* abort_flag, int& ab, uint32_t& aphase,
+                                              Release release) {
+  auto acquire = [&]() -> bool {
+    if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) return false;
+    tc_fence_after();
+    return true;
+  };
+  auto handback = [&]() {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release(ab);
+    ab ^= 1;
+    if (ab == 0) aphase ^= 1u;
+  };
+  // one chunk: all kCols sums at once, the buffer handed back before the
+  // arithmetic (zeros for an empty split)
+  auto load_all = [&](uint32_t (&x)[kCols / 32][32]) -> bool {
+    if (nchunks == 0) {
 #pragma unroll
-  for (int v = 0; v < kCols / 16; ++v) {
-    uint32_t word[4];
+      for (int q = 0; q < kCols / 32; ++q)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int e = 16 * v + 4 * b;
-      const uint32_t* xs = &x[e / 32][e % 32];
-      const uint64_t r01 = residues2(pack2(xs[0], xs[1]), rc), r23 = residues2(pack2(xs[2], xs[3]), rc);
-      const uint32_t lo = __byte_perm(static_cast<uint32_t>(r01), static_cast<uint32_t>(r01 >> 32), 0x0040);
-      const uint32_t hi = __byte_perm(static_cast<uint32_t>(r23), static_cast<uint32_t>(r23 >> 32), 0x0040);
-      word[b] = __byte_perm(lo, hi, 0x5410);
+        for (int e = 0; e < 32; ++e) x[q][e] = 0u;
+      return true;
     }
-    st_shared_v4(row + static_cast<uint32_t>((v ^ (lane & 7)) * 16), word[0], word[1], word[2], word[3]);
+    if (!acquire()) return false;
+    const uint32_t taddr = tbase + static_cast<uint32_t>(ab * BN);
+#pragma unroll
+    for (int q = 0; q < kCols / 32; ++q) tmem_ld32(taddr + 32 * q, x[q]);
+#pragma unroll
+    for (int q = 0; q < kCols / 32; ++q) tmem_wait_ld(x[q]);
+    handback();
+    return true;
+  };
+  if constexpr (KIND == 1 || (KIND == 2 && LONG)) {
+    int32_t acc[kCols];
+    if constexpr (LONG) {
+#pragma unroll
+      for (int e = 0; e < kCols; ++e) acc[e] = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!acquire()) return false;
+        const uint32_t taddr = tbase + static_cast<uint32_t>(ab * BN);
+        uint32_t va[32];
+        tmem_ld32(taddr, va);
+        tmem_wait_ld(va);
+        drain_chunk<0>(acc, taddr, va);
+        handback();
+      }
+    } else {
+      uint32_t x[kCols / 32][32];
+      if (!load_all(x)) return false;
+#pragma unroll
+      for (int e = 0; e < kCols; ++e) acc[e] = __float2int_rn(__uint_as_float(x[e / 32][e % 32]));
+    }
+    if constexpr (KIND == 1)
+      store_sums(acc, w, ps, row0 + lane, gj0, prm);
+    else
+      store_pair_sums(acc, w, ps, row0 + lane, gj0, prm, stash);
+    return true;
+  } else {
+    const ResidueConsts rc = residue_consts(w.p + ps);
+    uint32_t words[kCols / 4];
+    if constexpr (LONG) {
+      uint64_t R[kCols / 2];
+      const uint64_t first_shift = pack2f(-(kMagic + static_cast<float>(nchunks)));
+      for (int c = 0; c < nchunks; ++c) {
+        if (!acquire()) return false;
+        const uint32_t taddr = tbase + static_cast<uint32_t>(ab * BN);
+        uint32_t va[32];
+        tmem_ld32(taddr, va);
+        tmem_wait_ld(va);
+        if (c == 0)
+          cut_chunk<true, 0>(R, taddr, va, rc, first_shift);
+        else
+          cut_chunk<false, 0>(R, taddr, va, rc, first_shift);
+        handback();
+      }
+      chunk_words(R, words, rc);
+    } else {
+      uint32_t x[kCols / 32][32];
+      if (!load_all(x)) return false;
+      one_chunk_words(x, words, rc);
+    }
+    store_words<KIND == 2>(words, w, ps, row0, lane, gj0, prm, stash, out_stage, tmO);
+    return true;
   }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) tma_store_3d(tmO, stage, static_cast<int>(gj0), static_cast<int>(row0), p);
 }
 
-template <bool LONG, bool PAIRS>
+template <bool LONG, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
@@ -737,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<PAIRS>(u, prm);
+        const Unit w = decode_unit<KIND == 2>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
@@ -780,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<PAIRS>(u, prm);
+        const Unit w = decode_unit<KIND == 2>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
           const int c1 = min(w.kb1, c0 + kChunkKB);
@@ -823,81 +1007,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 4;
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
     const int half = ew >> 2;   // which kCols of the BN tile columns
-    const int row_in_tile = quad * 32 + lane;
     int ab = 0;
     uint32_t aphase = 0;
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kStages * kStageBytes + kBarBytes) + (threadIdx.x - 128);
     const uint32_t out_stage = smem_u32(smem + kStages * kStageBytes + kBarBytes) + static_cast<uint32_t>(ew) * kStageOutBytes;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(half * kCols);
+    auto release = [&](int b) { mbar_arrive(acce0 + 8 * b); };
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<PAIRS>(u, prm);
+      const Unit w = decode_unit<KIND == 2>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
-      const int64_t gi = static_cast<int64_t>(w.mt) * BM + row_in_tile;
+      const int64_t row0 = static_cast<int64_t>(w.mt) * BM + quad * 32;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
-      for (int ps = 0; ps < w.passes && ok; ++ps) {
-        if constexpr (LONG) {
-          int32_t acc[kCols];
-#pragma unroll
-          for (int e = 0; e < kCols; ++e) acc[e] = 0;
-          for (int c = 0; c < nchunks; ++c) {
-            if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                   static_cast<uint32_t>(ab * BN + half * kCols);
-            uint32_t va[32];
-            tmem_ld32(taddr, va);
-            tmem_wait_ld(va);
-            drain_chunk<0>(acc, taddr, va);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * ab);
-            ab ^= 1;
-            if (ab == 0) aphase ^= 1u;
-          }
-          if (!ok) break;
-          store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
-        } else {
-          // One chunk (none for an empty split): all kCols sums are loaded at
-          // once and the accumulator goes back to the MMA issuer before the
-          // reduction.
-          uint32_t x[kCols / 32][32];
-          if (nchunks > 0) {
-            if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                   static_cast<uint32_t>(ab * BN + half * kCols);
-#pragma unroll
-            for (int q = 0; q < kCols / 32; ++q) tmem_ld32(taddr + 32 * q, x[q]);
-#pragma unroll
-            for (int q = 0; q < kCols / 32; ++q) tmem_wait_ld(x[q]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * ab);
-            ab ^= 1;
-            if (ab == 0) aphase ^= 1u;
-          } else {
-#pragma unroll
-            for (int q = 0; q < kCols / 32; ++q)
-#pragma unroll
-              for (int e = 0; e < 32; ++e) x[q][e] = 0u;
-          }
-          if (!PAIRS && prm.out_kind == 0) {
-            if (gj0 < prm.ldo && gi - lane < prm.M)  // boxes wholly outside the planes are not stored
-              store_residues_tma(x, w.p + ps, gi - lane, gj0, out_stage, &tmO, lane);
-          } else {
-            int32_t acc[kCols];
-#pragma unroll
-            for (int e = 0; e < kCols; ++e) acc[e] = __float2int_rn(__uint_as_float(x[e / 32][e % 32]));
-            store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
-          }
-        }
-      }
+      for (int ps = 0; ps < w.passes && ok; ++ps)
+        ok = epilogue_pass<LONG, KIND>(w, ps, nchunks, row0, lane, gj0, prm, stash, out_stage, &tmO, tbase, accf0,
+                                        abort_flag, ab, aphase, release);
     }
     // the residue stores in flight finish before the CTA's shared memory goes
     if (lane == 0) bulk_wait_all();
@@ -916,7 +1040,7 @@ constexpr int kPairChunkKB = kChunkKB;
 
 // The CTA-pair kernel: tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
 // even CTA of a cluster of two; long (1024-term) chunks only.
-template <bool PAIRS>
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
@@ -979,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kPairStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit<PAIRS>(u, prm);
+        const Unit w = decode_unit<KIND == 2>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
@@ -1016,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit<PAIRS>(u, prm);
+        const Unit w = decode_unit<KIND == 2>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
           const int c1 = min(w.kb1, c0 + kPairChunkKB);
@@ -1059,42 +1183,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 4;
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. 32*quad+31
     const int half = ew >> 2;   // which kCols of the BN tile columns
-    const int row_in_tile = quad * 32 + lane;
     int ab = 0;
     uint32_t aphase = 0;
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kPairStages * kPairStageBytes + kBarBytes) + (threadIdx.x - 128);
+    const uint32_t out_stage =
+        smem_u32(smem + kPairStages * kPairStageBytes + kBarBytes) + static_cast<uint32_t>(ew) * kStageOutBytes;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(half * kCols);
+    auto release = [&](int b) { mbar_arrive_cluster(cluster_addr(acce0 + 8 * b, 0)); };
     for (int u = pair; u < units && ok; u += npairs) {
-      const Unit w = decode_unit<PAIRS>(u, prm);
+      const Unit w = decode_unit<KIND == 2>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kPairChunkKB - 1) / kPairChunkKB;
-      const int64_t gi = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + row_in_tile;
+      const int64_t row0 = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + quad * 32;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
-      for (int ps = 0; ps < w.passes && ok; ++ps) {
-        int32_t acc[kCols];
-#pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = 0;
-        for (int c = 0; c < nchunks; ++c) {
-          if (!warp_wait(accf0 + 8 * ab, aphase, abort_flag, prm.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                 static_cast<uint32_t>(ab * BN + half * kCols);
-          uint32_t va[32];
-          tmem_ld32(taddr, va);
-          tmem_wait_ld(va);
-          drain_chunk<0>(acc, taddr, va);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(cluster_addr(acce0 + 8 * ab, 0));
-          ab ^= 1;
-          if (ab == 0) aphase ^= 1u;
-        }
-        if (!ok) break;
-        store_tile<PAIRS>(acc, w, ps, gi, gj0, prm, stash);
-      }
+      for (int ps = 0; ps < w.passes && ok; ++ps)
+        ok = epilogue_pass<true, KIND>(w, ps, nchunks, row0, lane, gj0, prm, stash, out_stage, &tmO, tbase, accf0,
+                                        abort_flag, ab, aphase, release);
     }
+    // the residue stores in flight finish before the CTA's shared memory goes
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -1282,17 +1389,17 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   const int64_t units = static_cast<int64_t>(prm.mod_units) * splits * prm.tiles_m * prm.tiles_n;
   // several 1024-term chunks per split (int32 sums), or one (fp32 epilogue)
   const bool long_chunks = static_cast<int64_t>(prm.kb_per_split) * BK > 1024;
-  // the one-chunk epilogue writes residue planes by TMA stores (the callers
-  // give a 16-byte aligned base, ldo and plane stride)
+  // residue planes are written by TMA stores (the callers give a 16-byte
+  // aligned base, ldo and plane stride)
   CUtensorMap tmO;
   memset(&tmO, 0, sizeof(tmO));
-  if (out_kind == 0 && !pairs && !long_chunks && !make_out_map(&tmO, out, M, ldo, out_plane, n))
-    return cudaErrorInvalidValue;
-  // PAIRS: the pair-residue output (out_kind 2) is compiled in only where used
-  const bool po = out_kind == 2;
-  auto kernel = pairs ? (po ? residue_gemm_pair_kernel<true> : residue_gemm_pair_kernel<false>)
-                      : (long_chunks ? (po ? residue_gemm_kernel<true, true> : residue_gemm_kernel<true, false>)
-                                     : (po ? residue_gemm_kernel<false, true> : residue_gemm_kernel<false, false>));
+  if (out_kind == 0 && !make_out_map(&tmO, out, M, ldo, out_plane, n)) return cudaErrorInvalidValue;
+  // one instantiation per output kind: each holds only its own epilogue
+  auto pick = [out_kind](auto k0, auto k1, auto k2) { return out_kind == 0 ? k0 : (out_kind == 1 ? k1 : k2); };
+  auto kernel = pairs ? pick(residue_gemm_pair_kernel<0>, residue_gemm_pair_kernel<1>, residue_gemm_pair_kernel<2>)
+                : long_chunks
+                    ? pick(residue_gemm_kernel<true, 0>, residue_gemm_kernel<true, 1>, residue_gemm_kernel<true, 2>)
+                    : pick(residue_gemm_kernel<false, 0>, residue_gemm_kernel<false, 1>, residue_gemm_kernel<false, 2>);
   const size_t smem = (pairs ? kPairSmemBytes : kSmemBytes) + kStashBytes;
   if (withhold_kb >= 0 && (pairs || withhold_kb >= prm.kb_per_split)) return cudaErrorInvalidValue;
   int resident = 0;
