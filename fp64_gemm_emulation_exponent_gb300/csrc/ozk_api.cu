@@ -16,7 +16,10 @@ namespace ozk {
 namespace {
 
 constexpr int kSplitSms = 152;  // SM count the split-K choice plans for (GB300)
-constexpr int64_t kPairOutMinK = 8192;  // K from which the GEMM writes pair residues
+// K from which the GEMM writes pair residues: below it the byte planes,
+// reduced in fp32 per chunk and stored by TMA, cost less overall (measured
+// from K = 8192 to 16384; at 32768 the pair output is ahead)
+constexpr int64_t kPairOutMinK = 32768;
 constexpr int64_t kMaxDim = INT32_MAX / 2;  // rows/columns the kernels index with int
 
 // ---- small unsigned multi-limb integers for the host-side constants -------

@@ -91,7 +91,7 @@ def test_gamma_matches_the_oracle():
 
 def test_workspace_layout_regions_fit_and_do_not_overlap():
     for (M, N, K, n) in [(1, 1, 1, 2), (300, 257, 700, 14), (2048, 1024, 2100, 14), (300, 257, 9000, 13),
-                         (96, 80, 140000, 14), (8192, 8192, 512, 20)]:
+                         (300, 257, 33000, 13), (96, 80, 140000, 14), (8192, 8192, 512, 20)]:
         info = ozk.ozk_workspace_layout(M, N, K, n)
         assert info.total_bytes == ozk.ozk_workspace_size(M, N, K, n)
         assert info.kpad == ozk.ozk_kpad(K)

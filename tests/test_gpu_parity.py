@@ -174,10 +174,11 @@ def test_dgemm_bit_exact(M, N, K, n):
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
 
-@pytest.mark.parametrize("M,N,K,n", [(65, 300, 8200, 13), (130, 90, 8192, 14)])
+@pytest.mark.parametrize("M,N,K,n", [(65, 300, 32800, 13), (130, 90, 32768, 14), (65, 300, 8200, 13)])
 def test_dgemm_bit_exact_pair_residue_path(M, N, K, n):
-    """K of 8192 or more: the GEMM's epilogue writes uint16 residues of moduli
-    pairs (an odd last modulus alone) and the combine starts from them."""
+    """K of 32768 or more: the GEMM's epilogue writes uint16 residues of
+    moduli pairs (an odd last modulus alone) and the combine starts from
+    them.  K = 8200: byte planes reduced over nine chunks."""
     A, B = inputs(M, N, K, seed=M + N + K + n)
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
@@ -418,14 +419,14 @@ def test_caller_workspace_and_host_buffers_agree():
     assert ozk.ozk_stream_status() == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(2100, 300, 700), (2100, 2300, 700), (3000, 2048, 300), (2048, 72, 8200)])
+@pytest.mark.parametrize("M,N,K", [(2100, 300, 700), (2100, 2300, 700), (3000, 2048, 300), (2048, 72, 32800)])
 def test_host_buffers_in_blocks(M, N, K):
     """ozk_dgemm_host on row and column blocks (a dimension >= 2048 goes in
     four blocks of whole 256-row or 256-column tiles, copies overlapping the
     stages; ragged last blocks here) with padded host leading dimensions:
     equal to the device path bit for bit, and to the oracle on sampled
     outputs, block edges included (byte residues at K <= 700, pair residues
-    at K = 8200)."""
+    at K = 32800)."""
     A, B = inputs(M, N, K, seed=M + N + K)
     hA = torch.zeros((M, K + 3), dtype=torch.float64).pin_memory()
     hB = torch.zeros((K, N + 5), dtype=torch.float64).pin_memory()
@@ -469,10 +470,10 @@ def test_host_async_calls_in_flight():
 
 def test_host_async_pair_residue_and_split_k_outputs():
     """Back-to-back ozk_dgemm_host_async calls whose later ones find an earlier
-    call still computing (the whole-product schedule), with K >= 8192 (the
+    call still computing (the whole-product schedule), with K >= 32768 (the
     GEMM writes uint16 pair residues) and K >= 2^17 (int32 split-K partials):
     every C equals the device path bit for bit."""
-    shapes = [(1024, 1024, 8200), (1024, 520, 8200), (96, 40, 140000), (96, 40, 140000)]
+    shapes = [(768, 768, 32800), (768, 392, 32800), (96, 40, 140000), (96, 40, 140000)]
     st = torch.cuda.Stream()
     calls = []
     for idx, (M, N, K) in enumerate(shapes):

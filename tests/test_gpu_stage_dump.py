@@ -1,7 +1,7 @@
 """The intermediate buffers of one real ozk_dgemm_ws call, read back from its
 workspace (ozk_workspace_layout) and compared with the oracle: the scales,
 sampled rows of A's residue slices and columns of B's, the residue GEMM's
-planes at sampled outputs (byte residues, pair residues for K >= 8192, or
+planes at sampled outputs (byte residues, pair residues for K >= 32768, or
 int32 split-K sums for K >= 2^17) and C.  The stage entry points run each
 kernel alone; this checks every stage in the launch configuration of the
 whole call (fused row scan, CTA-pair GEMM, split-K, the combine kernel
@@ -27,7 +27,8 @@ def region(ws, offset, count, dtype):
     return ws[offset: offset + nbytes].cpu().numpy().view(dtype)
 
 
-@pytest.mark.parametrize("M,N,K,n,kind", [(2048, 1024, 2100, 14, 0), (600, 520, 9000, 13, 2),
+@pytest.mark.parametrize("M,N,K,n,kind", [(2048, 1024, 2100, 14, 0), (600, 520, 9000, 13, 0),
+                                          (600, 520, 33000, 13, 2),
                                           (96, 80, 140000, 14, 1), (513, 300, 700, 20, 0)])
 def test_stage_buffers_of_one_call(M, N, K, n, kind):
     rng = np.random.default_rng(M + K)
