@@ -428,8 +428,8 @@ def run_gpu(args, ranks: Ranks):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config(w, n),
             "tensor_path": "residues in [-128,127] as fp16 on tcgen05 kind::f16 (sm_103a has no kind::i8); "
-                           "fp32 TMEM sums exact per 1024-term chunk (256 below K = 1024); CTA-pair "
-                           "tcgen05.mma.cta_group::2 for K >= 2048",
+                           "fp32 TMEM sums exact per 1024-term chunk, reduced mod p on the packed fp32 "
+                           "pipe and stored by TMA; CTA-pair tcgen05.mma.cta_group::2 for K >= 2048",
             "fp16_tensor_tflops_issued": 2.0 * M * N * ozk.ozk_kpad(K) * n / gemm_s / 1e12,
             "int8_tensor_peak": "none on sm_103a: ptxas rejects tcgen05.mma kind::i8 for sm_103a, so the "
                                 "residue GEMMs run on the fp16 tensor path (same dense rate as bf16)",
