@@ -8,11 +8,13 @@
 // [-128, 127]) are fed to the fp16 tensor cores, where they are exact: every
 // product is an integer of magnitude at most 2^14, so every fp32 partial sum
 // of a 1024-term chunk is an integer of magnitude at most 2^24 and the fp32
-// accumulator in TMEM holds the chunk's exact integer sum.  Where a K split
-// spans several chunks the epilogue warps read each chunk out of TMEM,
-// convert it exactly (cvt.rni) and add it into int32 registers (exact for
-// K < 2^17), then reduce mod p once per tile; where the split is one chunk
-// (K <= 1024) they reduce the fp32 sums mod p directly, on the FP32 pipes.
+// accumulator in TMEM holds the chunk's exact integer sum.  For residues
+// the epilogue warps stay in fp32, two outputs per packed instruction: one
+// chunk is reduced mod p directly; several are each cut to a small remainder
+// and added up, then reduced once.  For exact sums (split-K shares, and pair
+// residues over eight or more chunks, where that is cheaper per chunk) they
+// convert each chunk exactly (cvt.rni) and add it into int32 registers
+// (exact for K < 2^17).
 // Outputs: the residues mod p as uint8 planes (out_kind 0); the exact int32
 // sums of a K split (1); or, with the two moduli of a pair run back to back
 // on one tile, the uint16 residue of the pair modulus p_2j p_2j+1 (2, the
@@ -38,7 +40,8 @@
 //               one lane waits and issues the MMAs (the even CTA of a pair).
 //   warps 2, 3  idle (they complete warpgroup 0, which hands its registers
 //               to the epilogue through setmaxnreg).
-//   warps 4..11 epilogue: TMEM -> registers -> int32 sums -> mod p -> HBM.
+//   warps 4..11 epilogue: TMEM -> registers -> residues mod p in fp32 (or
+//               exact int32 sums) -> HBM, residue planes by TMA stores.
 // Every mbarrier wait is bounded (2 s); a wait that runs out latches
 // OZK_ERR_TIMEOUT on the device, makes all roles of the CTA stop, drains
 // in-flight copies and MMAs, frees TMEM and returns.

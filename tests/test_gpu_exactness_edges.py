@@ -99,11 +99,12 @@ def crafted_operands(M, N, K, seed):
     return ra, rb
 
 
-@pytest.mark.parametrize("K", [1024, 1088, 2048, 3072, 4096])
+@pytest.mark.parametrize("K", [1024, 1088, 2048, 3072, 4096, 9000, 20000])
 def test_gemm_chunk_sums_at_two_to_the_24(K):
     """1024-term chunks (single CTA at K = 1024, one chunk, and 1088, two;
-    CTA pairs from 2048): chunk sums of exactly 2^24, 2^24 - 2^14 + small
-    odd terms, and their negative counterparts, bit-exact."""
+    CTA pairs from 2048, up to 20 chunks, whose fp32 cuts add up before the
+    one reduction): chunk sums of exactly 2^24, 2^24 - 2^14 + small odd
+    terms, and their negative counterparts, bit-exact."""
     M, N, n = 300, 260, 2
     ra, rb = crafted_operands(M, N, K, seed=K)
     raw, cmod = oracle.gemm_mod(ra, rb, n)
