@@ -214,9 +214,18 @@ __device__ __forceinline__ bool round_scaled_fast(const uint32_t (&X)[NL], int S
   const uint32_t inc = rb & (sticky | (sig_lo & 1u));
   // the significand carries the leading one at bit 52: exponent field e + 1022
   // plus one; a rounding carry into bit 53 bumps it once more (to Inf at the top)
-  const uint64_t bits = (static_cast<uint64_t>(e + 1022) << 52) +
-                        ((static_cast<uint64_t>(sig_hi) << 32) | sig_lo) + inc;
-  *out = bits | (static_cast<uint64_t>(sgn) << 63);
+  if constexpr (NL >= 4) {
+    // exponent field and sign into the high word by funnel shifts (the ALU's
+    // shifter, off the multiply pipe the combine is bound by from four limbs
+    // up); a rounding carry out of the low word by the 64-bit add
+    const uint32_t hi_word = __funnelshift_l(0u, static_cast<uint32_t>(e + 1022), 20) + sig_hi;
+    const uint64_t bits = ((static_cast<uint64_t>(hi_word) << 32) | sig_lo) + inc;
+    *out = bits | (static_cast<uint64_t>(__funnelshift_l(0u, sgn, 31)) << 32);
+  } else {
+    const uint64_t bits = (static_cast<uint64_t>(e + 1022) << 52) +
+                          ((static_cast<uint64_t>(sig_hi) << 32) | sig_lo) + inc;
+    *out = bits | (static_cast<uint64_t>(sgn) << 63);
+  }
   return t2 != 0u && e >= -1022 && e <= 1023;
 }
 
@@ -314,7 +323,14 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(
     const uint8_t* base = static_cast<const uint8_t*>(in) + i * ldi + jt;
     static_for<0, kMaxModuli>([&](auto kc) {
       constexpr int k = decltype(kc)::value;
-      if (k < n) load_words<G>(base + k * plane, cw[k]);
+      if (k < n) {
+        if constexpr (NL >= 4) {  // plane by plane with adds, off the multiply pipe (see assemble)
+          load_words<G>(base, cw[k]);
+          base += plane;
+        } else {
+          load_words<G>(base + k * plane, cw[k]);
+        }
+      }
     });
   } else {
     static_for<0, kMaxModuli>([&](auto kc) {
