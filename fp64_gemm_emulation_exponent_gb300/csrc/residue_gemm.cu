@@ -628,7 +628,8 @@ __device__ __forceinline__ void cut_chunk(uint64_t (&R)[kCols / 2], uint32_t tad
 __device__ __forceinline__ void chunk_words(const uint64_t (&R)[kCols / 2], uint32_t (&words)[kCols / 4],
                                             const ResidueConsts& c) {
 #pragma unroll
-  for (int i = 0; i < kCols / 4; ++i) words[i] = low_bytes4(floor_residues2(R[2 * i], c), floor_residues2(R[2 * i + 1], c));
+  for (int i = 0; i < kCols / 4; ++i)
+    words[i] = low_bytes4(floor_residues2(R[2 * i], c), floor_residues2(R[2 * i + 1], c));
 }
 
 // out_kind 1: the exact int32 sums of this thread's kCols columns gj0.. of
@@ -1014,7 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t aphase = 0;
     bool ok = true;
     uint4* stash = reinterpret_cast<uint4*>(smem + kStages * kStageBytes + kBarBytes) + (threadIdx.x - 128);
-    const uint32_t out_stage = smem_u32(smem + kStages * kStageBytes + kBarBytes) + static_cast<uint32_t>(ew) * kStageOutBytes;
+    const uint32_t out_stage =
+        smem_u32(smem + kStages * kStageBytes + kBarBytes) + static_cast<uint32_t>(ew) * kStageOutBytes;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(half * kCols);
     auto release = [&](int b) { mbar_arrive(acce0 + 8 * b); };
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
