@@ -16,21 +16,24 @@ cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64
   constexpr int G = 1;
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-#define OZK_CRT_LAUNCH(KIND)                                                                                      \
-  do {                                                                                                            \
-    if (X)                                                                                                        \
-      crt_kernel<NL, KIND, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K); \
-    else                                                                                                          \
-      crt_kernel<NL, KIND, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K); \
+  const RowDiv rd = row_div((N + 4 * G - 1) / (4 * G));
+#define OZK_CRT_LAUNCH(KIND)                                                                            \
+  do {                                                                                                  \
+    if (X)                                                                                              \
+      crt_kernel<NL, KIND, true, G, 0>                                                                  \
+          <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K, rd);           \
+    else                                                                                                \
+      crt_kernel<NL, KIND, false, G, 0>                                                                 \
+          <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K, rd);           \
   } while (0)
   if (in_kind == 0)
     OZK_CRT_LAUNCH(0);
   else if (in_kind == 1)
     OZK_CRT_LAUNCH(1);
   else if (X)
-    crt_pairs_kernel<NL, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K);
+    crt_pairs_kernel<NL, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K, rd);
   else
-    crt_pairs_kernel<NL, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K);
+    crt_pairs_kernel<NL, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K, rd);
 #undef OZK_CRT_LAUNCH
   return cudaGetLastError();
 }

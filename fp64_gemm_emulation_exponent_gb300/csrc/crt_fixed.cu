@@ -18,10 +18,11 @@ cudaError_t launch_fixed(int64_t M, int64_t N, const void* in, int in_kind, int6
   if (in_kind == 2)
     crt_pairs_kernel<crt_limbs(NM), false, 2, NM>
         <<<static_cast<unsigned>((M * ((N + 7) / 8) + 255) / 256), 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C,
-                                                                                      ldc, nullptr, K);
+                                                                                      ldc, nullptr, K,
+                                                                                      row_div((N + 7) / 8));
   else
-    crt_kernel<crt_limbs(NM), 0, false, G, NM>
-        <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K);
+    crt_kernel<crt_limbs(NM), 0, false, G, NM><<<blocks, 256, 0, stream>>>(
+        in, ldi, plane, M, N, 1, s, t, C, ldc, nullptr, K, row_div((N + 4 * G - 1) / (4 * G)));
   return cudaGetLastError();
 }
 
