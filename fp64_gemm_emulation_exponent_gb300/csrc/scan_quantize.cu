@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
     uint64_t m = 0;
     if (sp.a_vec) {  // a_seg is a multiple of 4: every group of 4 starts 32-byte aligned
       const int64_t g1 = k1 >> 2;
-#pragma unroll 2
+#pragma unroll 8  // eight 32-byte loads in flight per lane
       for (int64_t g = (k0 >> 2) + lane; g < g1; g += 32) {
         uint64_t v[4];
         load4_u64(a + 4 * g, v);
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp)
     }
     if (c < sp.N) {
       if (sp.b_vec && c + 3 < sp.N) {
-#pragma unroll 4
+#pragma unroll 8  // eight 32-byte loads in flight per thread (4 measured 10% slower at 4096^3)
         for (int64_t k = k0 + rg; k < k1; k += kRowGroups) {
           uint64_t v[4];
           load4_u64(sp.B + k * sp.ldb + c, v);
