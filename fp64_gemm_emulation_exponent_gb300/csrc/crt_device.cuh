@@ -301,20 +301,18 @@ __device__ __forceinline__ uint32_t div_rows(uint32_t g, const RowDiv& r) {
 // 32-bit sums are exact.  X = S - q P is assembled from the columns (plus
 // q times the 16-bit limbs of 2^(32 NL) - P) into NL 32-bit limbs.
 // NFIX > 0 fixes the moduli count at compile time (it must equal K.n); those
-// kernels are held to four 256-thread blocks per SM up to four limbs and to
-// three beyond.
+// kernels are held to five 256-thread blocks per SM at three limbs (48
+// registers: 8192^2 at 8 moduli 317 -> 304 us against four blocks), four at
+// four limbs (five spilled there: 456 -> 494 us) and three beyond.
 //  IN_KIND 0: uint8 residues, modulus k at in + k * plane, row i at + i * ldi;
 //  IN_KIND 1: int32 partial sums, split sp and modulus k at (sp * n + k) * plane.
 // All residue words are loaded before any arithmetic so that the loads of a
 // thread are in flight together.
 template <int NL, int IN_KIND, bool LIMBS, int G, int NFIX>
-__global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1) crt_kernel(const void* __restrict__ in, int64_t ldi,
-                                                  int64_t plane, int64_t M, int64_t N, int splits,
-                                                  const int32_t* __restrict__ s,
-                                                  const int32_t* __restrict__ t,
-                                                  double* __restrict__ C, int64_t ldc,
-                                                  uint32_t* __restrict__ Xout,
-                                                  const __grid_constant__ CrtConst K, const RowDiv rd) {
+__global__ void __launch_bounds__(256, NFIX ? (NL <= 3 ? 5 : (NL <= 4 ? 4 : 3)) : 1)
+    crt_kernel(const void* __restrict__ in, int64_t ldi, int64_t plane, int64_t M, int64_t N, int splits,
+               const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C, int64_t ldc,
+               uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K, const RowDiv rd) {
   constexpr int W = 4 * G;  // columns per thread
   static_assert(IN_KIND != 2, "pair residues take crt_pairs_kernel");
   // columns of a four-column group accumulated together: four share each
