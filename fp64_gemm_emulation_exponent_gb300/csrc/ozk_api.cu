@@ -16,10 +16,6 @@ namespace ozk {
 namespace {
 
 constexpr int kSplitSms = 152;  // SM count the split-K choice plans for (GB300)
-// K from which the GEMM writes pair residues: below it the byte planes,
-// reduced in fp32 per chunk and stored by TMA, cost less overall (measured
-// from K = 8192 to 16384; at 32768 the pair output is ahead)
-constexpr int64_t kPairOutMinK = 32768;
 constexpr int64_t kMaxDim = INT32_MAX / 2;  // rows/columns the kernels index with int
 
 // ---- small unsigned multi-limb integers for the host-side constants -------
@@ -243,10 +239,14 @@ Layout layout_for(int64_t M, int64_t N, int64_t K, int n) {
   Layout L;
   L.kpad = ozk_kpad(K);
   L.splits = choose_splits(M, N, L.kpad, n, kSplitSms);
-  // one split: byte residues (kind 0), or for long K the uint16 residues of
-  // moduli pairs (kind 2: the GEMM's epilogue does the first CRT step, which
-  // pays only once K amortises the heavier tile tail); split-K: int32 sums
-  L.kind = L.splits > 1 ? 1 : (K >= kPairOutMinK ? 2 : 0);
+  // one split: byte residues (kind 0); split-K: int32 sums (kind 1).  The
+  // uint16 residues of moduli pairs (kind 2, the first CRT step in the GEMM's
+  // epilogue) measured slower end to end at every K once the byte planes were
+  // reduced in fp32 and stored by TMA (e.g. 2048^2 x 32768: 8 moduli 1954 ->
+  // 1798 us, 20 moduli 4470 -> 4296 us with byte planes; 14 moduli within
+  // 0.3% either way), so ozk_dgemm does not use them; the stage entry points
+  // still write and read them.
+  L.kind = L.splits > 1 ? 1 : 0;
   L.ldo = L.kind == 1 ? round_up(N, 4) : round_up(N, 16);
   L.planes = L.kind == 1 ? n * L.splits : (L.kind == 2 ? (n + 1) / 2 : n);
   size_t off = 0;

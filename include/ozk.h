@@ -112,8 +112,8 @@ typedef struct {
   size_t planes_offset;     /* the residue GEMM's output, in the layout of planes_kind */
   int64_t kpad;
   int64_t a_plane, b_plane;
-  int planes_kind;          /* 0: uint8 residues, 1: int32 split-K sums, 2: uint16 pair residues
-                               (the out_kind of ozk_residue_gemm) */
+  int planes_kind;          /* 0: uint8 residues, 1: int32 split-K sums (the out_kind of
+                               ozk_residue_gemm; its kind 2, pair residues, is not chosen here) */
   int64_t planes_ld;        /* row stride of a plane, elements */
   int64_t planes_plane;     /* elements between consecutive planes */
   int splits;               /* K splits (planes_kind 1) */

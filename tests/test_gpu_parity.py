@@ -175,10 +175,9 @@ def test_dgemm_bit_exact(M, N, K, n):
 
 
 @pytest.mark.parametrize("M,N,K,n", [(65, 300, 32800, 13), (130, 90, 32768, 14), (65, 300, 8200, 13)])
-def test_dgemm_bit_exact_pair_residue_path(M, N, K, n):
-    """K of 32768 or more: the GEMM's epilogue writes uint16 residues of
-    moduli pairs (an odd last modulus alone) and the combine starts from
-    them.  K = 8200: byte planes reduced over nine chunks."""
+def test_dgemm_bit_exact_long_k(M, N, K, n):
+    """Long K in one split: byte planes whose 33, 32 or 9 chunks are each cut
+    in fp32 and added before the one reduction, against the oracle."""
     A, B = inputs(M, N, K, seed=M + N + K + n)
     assert same_bits(dgemm(A, B, n), oracle.dgemm(A, B, n))
 
@@ -425,8 +424,8 @@ def test_host_buffers_in_blocks(M, N, K):
     four blocks of whole 256-row or 256-column tiles, copies overlapping the
     stages; ragged last blocks here) with padded host leading dimensions:
     equal to the device path bit for bit, and to the oracle on sampled
-    outputs, block edges included (byte residues at K <= 700, pair residues
-    at K = 32800)."""
+    outputs, block edges included (one chunk per tile at K <= 700, 33 at
+    K = 32800)."""
     A, B = inputs(M, N, K, seed=M + N + K)
     hA = torch.zeros((M, K + 3), dtype=torch.float64).pin_memory()
     hB = torch.zeros((K, N + 5), dtype=torch.float64).pin_memory()
@@ -468,11 +467,11 @@ def test_host_async_calls_in_flight():
         assert same_bits(hC.numpy(), dgemm(A, B, 14))
 
 
-def test_host_async_pair_residue_and_split_k_outputs():
+def test_host_async_long_k_and_split_k_outputs():
     """Back-to-back ozk_dgemm_host_async calls whose later ones find an earlier
-    call still computing (the whole-product schedule), with K >= 32768 (the
-    GEMM writes uint16 pair residues) and K >= 2^17 (int32 split-K partials):
-    every C equals the device path bit for bit."""
+    call still computing (the whole-product schedule), with K = 32800 (byte
+    planes over 33 chunks) and K >= 2^17 (int32 split-K partials): every C
+    equals the device path bit for bit."""
     shapes = [(768, 768, 32800), (768, 392, 32800), (96, 40, 140000), (96, 40, 140000)]
     st = torch.cuda.Stream()
     calls = []
