@@ -22,6 +22,7 @@ constexpr uint64_t kInfBits = 0x7FF0000000000000ull;
 constexpr int kScanThreads = 256;
 constexpr int kQThreads = 256;
 constexpr int kQK = 16;  // K elements per quantisation thread: one 32-byte store per modulus
+constexpr int kMaxBudget = 94;  // |a'| <= 2^94 fits the three-word form
 
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
@@ -257,17 +258,16 @@ __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, const 
 // ---------------------------------------------------------------------------
 // Quantisation.  x = (-1)^neg m 2^e exactly (m < 2^53); with sh = e + s the
 // integer is a' = (-1)^neg round(m 2^sh), rounded to nearest with ties to
-// even (a shift and a rounding increment), |a'| <= 2^beta <= 2^72.  a' is
-// kept offset to a non-negative integer, a'' = a' + 2^(22 NL - 1) < 2^(22 NL),
-// as NL limbs of 22 bits: the two's complement of a' modulo 2^(22 NL) with its
-// top bit flipped.  Then, for every modulus,
-//   a' + h = sum_j l_j (2^22j mod p) + (h - 2^(22 NL - 1))   (mod p),
-// one integer below 2^32 whose canonical residue minus h is the balanced
-// residue.  Three limbs hold every beta <= 64; four the rest.  For beta <= 62
-// (NL = 2 below) a'' = a' + 2^63 fits one 64-bit word, and its eight bytes
-// against (2^8b mod p) give x in two 4-byte dot products (dp4a), x < 2^20.
+// even (a shift and a rounding increment), |a'| <= 2^beta.  a' is kept offset
+// to a non-negative integer, a'' = a' + 2^(32 NL - 1) < 2^(32 NL), as NL
+// 32-bit words: the two's complement of a' modulo 2^(32 NL) with its top bit
+// flipped (NL = 2 for beta <= 62, NL = 3 for beta <= 94, every budget there
+// is).  Then, for every modulus,
+//   a' + h = sum_b byte_b(a'') (2^8b mod p) + (h - 2^(32 NL - 1))   (mod p),
+// with the bytes taken four at a time by 4-byte dot products (dp4a): one
+// integer x < 4 NL * 255 * 254 + 2 p < 2^20, which a multiply-high by
+// ceil(2^32 / p) divides exactly; x mod p minus h is the balanced residue.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kMask22 = (1u << 22) - 1;
 
 template <int NL>
 __device__ __forceinline__ void scale_round(uint64_t bits, int32_t sc, uint32_t (&l)[NL]) {
@@ -299,16 +299,13 @@ __device__ __forceinline__ void scale_round(uint64_t bits, int32_t sc, uint32_t 
     hi = ~hi + (lo == 0 ? 1u : 0u);
     lo = 0ull - lo;
   }
+  static_assert(NL == 2 || NL == 3, "two or three 32-bit words");
+  l[0] = static_cast<uint32_t>(lo);
+  l[1] = static_cast<uint32_t>(lo >> 32);
   if constexpr (NL == 2) {  // |a'| <= 2^62: the low word of the two's complement, + 2^63
-    const uint64_t w = lo ^ (1ull << 63);
-    l[0] = static_cast<uint32_t>(w);
-    l[1] = static_cast<uint32_t>(w >> 32);
-  } else {
-    l[0] = static_cast<uint32_t>(lo) & kMask22;
-    l[1] = static_cast<uint32_t>(lo >> 22) & kMask22;
-    l[2] = (static_cast<uint32_t>(lo >> 44) | (hi << 20)) & kMask22;
-    if constexpr (NL == 4) l[3] = (hi >> 2) & kMask22;
-    l[NL - 1] ^= 1u << 21;  // + 2^(22 NL - 1)
+    l[1] ^= 1u << 31;
+  } else {  // |a'| <= 2^94: the 96-bit two's complement, + 2^95
+    l[2] = hi ^ (1u << 31);
   }
 }
 
@@ -327,32 +324,13 @@ __device__ __forceinline__ uint32_t shifted_residue(const uint32_t (&l)[NL]) {
     return (l[0] ^ 0x80u) & 0xFFu;  // (a' + 128) mod 256 from the low byte
   } else {
     constexpr uint32_t h = (p - 1) / 2;
-    if constexpr (NL == 2) {
-      // x = sum of the bytes of a'' times 2^8b mod p, plus h - 2^63 mod p:
-      // x < 8 * 255 * 254 + 2 p < 2^20, where umulhi by ceil(2^32/p) divides exactly
-      constexpr uint32_t off = (p - pow2_mod(63, p)) % p + h;
-      constexpr uint32_t m32 = static_cast<uint32_t>(((1ull << 32) + p - 1) / p);
-      const uint32_t x = __dp4a(l[1], byte_weights(4, p), __dp4a(l[0], byte_weights(0, p), off));
-      return x - __umulhi(x, m32) * p;
-    }
-    constexpr uint32_t c1 = pow2_mod(22, p), c2 = pow2_mod(44, p);
-    constexpr uint32_t off = (p - pow2_mod(22 * NL - 1, p)) % p + h;
-    if constexpr (NL == 3) {
-      // x < 2^22 (1 + 2 * 254) + 254 + 127 < 2^31: the 2^39 magic divides exactly
-      constexpr uint32_t m39 = static_cast<uint32_t>(((1ull << 39) + p - 1) / p);
-      const uint32_t x = l[0] + off + l[1] * c1 + l[2] * c2;
-      const uint32_t q = __umulhi(x, m39) >> 7;
-      return x - q * p;
-    } else {
-      // x < 2^32; the 2^32 magic quotient is exact or one too large
-      constexpr uint32_t c3 = pow2_mod(66, p);
-      constexpr uint32_t mg = magic_of(p);
-      const uint32_t x = l[0] + off + l[1] * c1 + l[2] * c2 + l[3] * c3;
-      const uint32_t q = __umulhi(x, mg);
-      int32_t r = static_cast<int32_t>(x - q * p);
-      r += r < 0 ? static_cast<int32_t>(p) : 0;
-      return static_cast<uint32_t>(r);
-    }
+    // x = the bytes of a'' against 2^8b mod p, plus h - 2^(32 NL - 1) mod p:
+    // x < 4 NL * 255 * 254 + 2 p < 2^20, where umulhi by ceil(2^32/p) is exact
+    constexpr uint32_t off = (p - pow2_mod(32 * NL - 1, p)) % p + h;
+    constexpr uint32_t m32 = static_cast<uint32_t>(((1ull << 32) + p - 1) / p);
+    uint32_t x = __dp4a(l[1], byte_weights(4, p), __dp4a(l[0], byte_weights(0, p), off));
+    if constexpr (NL == 3) x = __dp4a(l[2], byte_weights(8, p), x);
+    return x - __umulhi(x, m32) * p;
   }
 }
 
@@ -676,14 +654,13 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   const int64_t threads = qp.a_span + qp.b_threads;
   if (threads == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((threads + kQThreads - 1) / kQThreads);
-  // |a'| <= 2^budget: one 64-bit word for a budget of at most 62, three
-  // 22-bit limbs of two's complement up to 64, four beyond
+  // |a'| <= 2^budget: two 32-bit words of two's complement for a budget of
+  // at most 62, three beyond
+  if (budget > kMaxBudget) return cudaErrorInvalidValue;
   if (budget <= 62)
     quantize_kernel<2><<<blocks, kQThreads, 0, stream>>>(qp);
-  else if (budget <= 64)
-    quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
   else
-    quantize_kernel<4><<<blocks, kQThreads, 0, stream>>>(qp);
+    quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
   return cudaGetLastError();
 }
 
@@ -713,12 +690,11 @@ cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const doubl
     else                                                                       \
       quantize_rows_kernel<NL, false><<<blocks, threads, 0, stream>>>(qp, budget, s); \
   } while (0)
+  if (budget > kMaxBudget) return cudaErrorInvalidValue;
   if (budget <= 62)
     OZK_ROWS_LAUNCH(2);
-  else if (budget <= 64)
-    OZK_ROWS_LAUNCH(3);
   else
-    OZK_ROWS_LAUNCH(4);
+    OZK_ROWS_LAUNCH(3);
 #undef OZK_ROWS_LAUNCH
   return cudaGetLastError();
 }

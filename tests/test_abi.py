@@ -110,6 +110,23 @@ def test_workspace_layout_regions_fit_and_do_not_overlap():
         assert info.planes_ld >= N and info.planes_plane >= M * info.planes_ld
 
 
+def test_quantiser_residue_division_is_exact_below_two_to_the_20():
+    """The quantiser forms each residue from x, the bytes of the offset
+    integer (up to twelve) against 2^(8b) mod p plus an offset below 2p:
+    x < 12 * 255 * 254 + 2p < 2^20.  It divides by a multiply-high with
+    ceil(2^32 / p); that quotient is floor(x / p) for every such x and every
+    odd modulus."""
+    import numpy as np
+
+    assert 12 * 255 * 254 + 2 * 256 < 1 << 20
+    x = np.arange(1 << 20, dtype=np.uint64)
+    for p in (int(v) for v in oracle.moduli(ozk.OZK_MAX_MODULI)):
+        if p == 256:
+            continue
+        m32 = np.uint64(((1 << 32) + p - 1) // p)
+        assert np.array_equal((x * m32) >> np.uint64(32), x // np.uint64(p)), p
+
+
 def test_kpad():
     assert [ozk.ozk_kpad(k) for k in [0, 1, 63, 64, 65, 128, 131071]] == [0, 64, 64, 64, 128, 128, 131072]
 

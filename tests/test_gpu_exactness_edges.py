@@ -444,8 +444,8 @@ def quantize_tie_operands(M, N, K, n, seed):
 @pytest.mark.parametrize("n,K", [(8, 300), (14, 1000), (17, 100), (17, 16), (18, 1000), (20, 700)])
 def test_quantize_round_half_to_even(n, K):
     """Scales and every residue slice bit-exact against the oracle when most
-    scaled entries are exact halves: beta 26, 49 and 62 (the one-word
-    integer path of the quantiser), 63 and 64 (three limbs), 72 (four)."""
+    scaled entries are exact halves: beta 26, 49 and 62 (the two-word
+    integer path of the quantiser), 63, 64 and 72 (three words)."""
     M, N = 70, 90
     A, B = quantize_tie_operands(M, N, K, n, seed=n * 100 + K)
     s, t = run_scale(dev(A), dev(B), n)

@@ -120,8 +120,9 @@ def test_stages_other_moduli_counts(n):
 
 @pytest.mark.parametrize("n,K", [(17, 100), (17, 16), (17, 5), (18, 300), (18, 1000), (16, 1), (20, 700)])
 def test_stages_across_the_integer_widths(n, K):
-    """beta 62 (one 64-bit word per scaled element, dp4a residues), 63-64
-    (three 22-bit limbs), 65 and 72 (four limbs): every stage bit-exact."""
+    """beta 62 (two 32-bit words per scaled element), 63, 64, 65 and 72
+    (three words; the integer crosses 2^64 from beta 64): every stage
+    bit-exact."""
     A, B = inputs(70, 90, K, seed=n * 1000 + K, kind="special")
     check_stages(A, B, n)
 
@@ -188,8 +189,7 @@ def test_dgemm_bit_exact_fused_row_scan(M, N, K, n):
     """Enough rows of at most 4096 entries: each row of A is scanned inside its
     own quantisation (one block per row).  Special rows (zero, subnormal,
     2^900, wide range, Inf, NaN) and ragged K against the oracle, all outputs,
-    for each integer width (beta 48: one 64-bit word; 63: three limbs; 71:
-    four)."""
+    for each integer width (beta 48: two 32-bit words; 63 and 71: three)."""
     A, B = inputs(M, N, K, seed=M + N + K, kind="special")
     A[5, K // 3] = np.inf
     A[9, K - 1] = np.nan
