@@ -47,6 +47,7 @@
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -1274,6 +1275,23 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t ldo, int64
 
 }  // namespace
 
+// Split-K choice.  A split multiplies the units (tile, modulus) by s and
+// shortens each unit's K by s, so it fills SMs that one wave would leave idle;
+// it costs the int32 partial sums (4 B per output, modulus and split, written
+// here and read by the combine) and each unit's fixed cost.  The count is the
+// one of least modelled time: waves x (k-blocks per unit + kUnitKBlocks) at
+// kKBlockUs each, at least the HBM time of reading every slice once, plus the
+// partial sums at HBM speed.  The constants are fitted to measurements on a
+// GB300 (CTA pairs, 512^2 x 65536 at 8, 14, 17 and 20 moduli, 1024^2 x 65536,
+// 2048^2 x 32768, 256^2 x 262144, every split count up to 24): the GEMM and
+// combine time of the count chosen is within 0.7% of the best count's over
+// those shapes (the earlier rule, which split only what filled less than one
+// wave and weighed nothing but the wave fill, was 2-31% slower on four of
+// them).
+constexpr double kKBlockUs = 0.30;          // one 64-deep k-block of a 256 x 256 tile on one SM pair
+constexpr double kUnitKBlocks = 32.0;       // a unit's fixed cost, in k-blocks
+constexpr double kHbmBytesPerUs = 6.2e6;    // HBM bytes per microsecond the GEMM streams its slices at
+
 int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   // K of at least kPairMinK runs on CTA pairs (kPairM x BN tiles, one per SM
   // pair); every split keeps at least that much K, so the choice holds
@@ -1285,19 +1303,23 @@ int choose_splits(int64_t M, int64_t N, int64_t kpad, int n, int num_sms) {
   const int64_t kblocks = kpad / kKBlock;  // split shares are whole 64-element blocks
   // K beyond one int32-exact sum (2^14 K < 2^31) needs at least this many splits
   const int64_t min_s = (kblocks + OZK_SPLIT_MAX_K / kKBlock - 1) / (OZK_SPLIT_MAX_K / kKBlock);
-  if (min_s == 1 && (tiles >= num_sms || kblocks < 32)) return 1;
-  auto eff = [&](int64_t s) {
-    const int64_t units = tiles * s;
-    const int64_t waves = (units + num_sms - 1) / num_sms;
-    return static_cast<double>(units) / static_cast<double>(waves * num_sms);
+  if (min_s == 1 && kblocks < 2 * min_blocks) return 1;
+  const double floor_us = 2.0 * n * static_cast<double>(M + N) * static_cast<double>(kpad) / kHbmBytesPerUs;
+  auto cost = [&](int64_t s) {
+    const int64_t waves = (tiles * s + num_sms - 1) / num_sms;
+    const double mma = static_cast<double>(waves) *
+                       (static_cast<double>((kblocks + s - 1) / s) + kUnitKBlocks) * kKBlockUs;
+    const double partial = s > 1 ? 8.0 * s * n * static_cast<double>(M) * static_cast<double>(N) / kHbmBytesPerUs
+                                 : 0.0;
+    return std::max(mma, floor_us) + partial;
   };
   int best = static_cast<int>(min_s);
-  double best_eff = eff(min_s);
+  double best_cost = cost(min_s);
   for (int64_t s = min_s + 1; s <= 64 && kblocks / s >= min_blocks; ++s) {
-    const double e = eff(s);
-    if (e > best_eff + 0.02) {
+    const double c = cost(s);
+    if (c < 0.99 * best_cost) {  // a split must pay for itself by a margin
       best = static_cast<int>(s);
-      best_eff = e;
+      best_cost = c;
     }
   }
   return best;

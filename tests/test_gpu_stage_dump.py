@@ -28,7 +28,7 @@ def region(ws, offset, count, dtype):
 
 
 @pytest.mark.parametrize("M,N,K,n,kind", [(2048, 1024, 2100, 14, 0), (600, 520, 9000, 13, 0),
-                                          (600, 520, 33000, 13, 0),
+                                          (600, 520, 33000, 13, 1),
                                           (96, 80, 140000, 14, 1), (513, 300, 700, 20, 0)])
 def test_stage_buffers_of_one_call(M, N, K, n, kind):
     rng = np.random.default_rng(M + K)
