@@ -110,6 +110,32 @@ def test_workspace_layout_regions_fit_and_do_not_overlap():
         assert info.planes_ld >= N and info.planes_plane >= M * info.planes_ld
 
 
+def test_split_count_keeps_its_constraints():
+    """The K split count of ozk_dgemm's residue GEMM: at least the shares K
+    beyond one int32-exact sum needs, at most 64, every share at least 2048
+    of K (the CTA-pair kernel's minimum) when K is split, int32 partial sums
+    exactly when it is split, and none where whole-K units already fill the
+    GPU (square products)."""
+    shapes = [(M, N, K, n) for (M, N) in [(64, 64), (256, 256), (512, 512), (600, 520), (1024, 1024), (2048, 72),
+                                          (4096, 4096)]
+              for K in [512, 2048, 4096, 33000, 65536, 131072, 300000, 1 << 20] for n in [2, 8, 14, 20]]
+    for (M, N, K, n) in shapes:
+        if ozk.ozk_beta(K, n) < 1:
+            continue
+        info = ozk.ozk_workspace_layout(M, N, K, n)
+        kpad, sp = info.kpad, info.splits
+        assert -(-kpad // ozk.OZK_SPLIT_MAX_K) <= sp <= 64, (M, N, K, n, sp)
+        assert (info.planes_kind == 1) == (sp > 1), (M, N, K, n)
+        if sp > 1:
+            assert kpad // 64 // sp >= 2048 // 64, (M, N, K, n, sp)
+            assert -(-(kpad // 64) // sp) * 64 <= ozk.OZK_SPLIT_MAX_K
+    for (M, N, K) in [(4096, 4096, 4096), (8192, 8192, 8192), (8192, 8192, 512), (2048, 2048, 32768)]:
+        assert ozk.ozk_workspace_layout(M, N, K, 14).splits == 1
+    # the choices measured best on 512^2 x 65536: unsplit where 56 or 68 units
+    # already keep HBM busy, split where 80 units would leave a second wave of 4
+    assert [ozk.ozk_workspace_layout(512, 512, 65536, n).splits for n in (14, 17, 20)] == [1, 1, 4]
+
+
 def test_quantiser_residue_division_is_exact_below_two_to_the_20():
     """The quantiser forms each residue from x, the bytes of the offset
     integer (up to twelve) against 2^(8b) mod p plus an offset below 2p:
