@@ -226,16 +226,23 @@ def run_reference(args, ranks: Ranks):
     n = args.moduli
     A, B = workloads.workload_operands(w)
     # per step: a rows x cols block of C over the full K.  The oracle spreads
-    # rows over its threads, so the block holds whole rounds of rows for every
-    # thread, sized (once, untimed) so that warm-up and timed steps together
-    # take about two minutes
+    # rows over its threads and prepares the block's columns once per call,
+    # so the block holds at least 16 whole rounds of rows for every thread
+    # (the per-call column work then costs what about one round does); it is
+    # sized (once, untimed) so that warm-up and timed steps together take
+    # about two minutes, narrowing the columns first where a step would
+    # otherwise take longer than its share
     threads = max(1, oracle.threads())
-    cols = min(256, w.N)
-    rows = min(w.M, threads)
-    _, dt = oracle_block_rate(A, B, n, rows, cols)
     per_step = min(6.0, 120.0 / max(1, args.steps + args.warmup))
-    rounds = max(1, int(per_step / max(dt, 1e-3)))
-    rows = min(w.M, threads * rounds)
+    cols = min(256, w.N)
+    rows = min(w.M, 16 * threads)
+    _, dt = oracle_block_rate(A, B, n, rows, cols)
+    while dt > per_step and cols > 8:
+        cols //= 2
+        dt /= 2
+    if dt < per_step / 2:
+        rounds = max(1, int(per_step / max(dt, 1e-3)))
+        rows = min(w.M, rows * rounds)
     for _ in range(args.warmup):
         oracle_block_rate(A, B, n, rows, cols)
     t0 = time.perf_counter()
