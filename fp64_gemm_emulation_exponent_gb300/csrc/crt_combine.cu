@@ -17,25 +17,21 @@ cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   const RowDiv rd = row_div((N + 4 * G - 1) / (4 * G));
-#define OZK_CRT_LAUNCH(KIND)                                                                            \
-  do {                                                                                                  \
-    if (X)                                                                                              \
-      crt_kernel<NL, KIND, true, G, 0>                                                                  \
-          <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K, rd);           \
-    else                                                                                                \
-      crt_kernel<NL, KIND, false, G, 0>                                                                 \
-          <<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, splits, s, t, C, ldc, X, K, rd);           \
-  } while (0)
+  const dim3 grid(blocks), block(256);
   if (in_kind == 0)
-    OZK_CRT_LAUNCH(0);
-  else if (in_kind == 1)
-    OZK_CRT_LAUNCH(1);
-  else if (X)
-    crt_pairs_kernel<NL, true, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K, rd);
-  else
-    crt_pairs_kernel<NL, false, G, 0><<<blocks, 256, 0, stream>>>(in, ldi, plane, M, N, s, t, C, ldc, X, K, rd);
-#undef OZK_CRT_LAUNCH
-  return cudaGetLastError();
+    return X ? launch_dependent(crt_kernel<NL, 0, true, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N, splits,
+                                s, t, C, ldc, X, K, rd)
+             : launch_dependent(crt_kernel<NL, 0, false, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N,
+                                splits, s, t, C, ldc, X, K, rd);
+  if (in_kind == 1)
+    return X ? launch_dependent(crt_kernel<NL, 1, true, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N, splits,
+                                s, t, C, ldc, X, K, rd)
+             : launch_dependent(crt_kernel<NL, 1, false, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N,
+                                splits, s, t, C, ldc, X, K, rd);
+  return X ? launch_dependent(crt_pairs_kernel<NL, true, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N, s, t,
+                              C, ldc, X, K, rd)
+           : launch_dependent(crt_pairs_kernel<NL, false, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N, s, t,
+                              C, ldc, X, K, rd);
 }
 
 // The FP64 output from byte or pair residues (what the GEMM path writes) on

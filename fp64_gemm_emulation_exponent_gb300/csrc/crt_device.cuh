@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 3 ? 5 : (NL <= 4 ? 4 : 3)) 
     crt_kernel(const void* __restrict__ in, int64_t ldi, int64_t plane, int64_t M, int64_t N, int splits,
                const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C, int64_t ldc,
                uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K, const RowDiv rd) {
+  grid_dependency_sync();
   constexpr int W = 4 * G;  // columns per thread
   static_assert(IN_KIND != 2, "pair residues take crt_pairs_kernel");
   // columns of a four-column group accumulated together: four share each
@@ -581,6 +582,7 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1)
                      const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C,
                      int64_t ldc, uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K,
                      const RowDiv rd) {
+  grid_dependency_sync();
   constexpr int W = 4 * G;
   constexpr uint32_t kPairLiftMargin = 1u << 20;
   const int64_t groups = (N + W - 1) / W;

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <type_traits>
+#include <utility>
 
 #include "ozk.h"
 
@@ -38,6 +39,34 @@ __host__ __device__ constexpr uint32_t pow2_mod(int e, uint32_t p) {
   uint32_t r = 1u % p;
   for (int i = 0; i < e; ++i) r = (r * 2u) % p;
   return r;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation allowed and starts, in every
+// thread, by waiting for the grid before it in the stream to complete and
+// its writes to be visible (so that completing implies the predecessor's
+// completion, which keeps the order transitive), then lets the grid after
+// it launch: its blocks take the SM room this grid's last blocks leave and
+// wait there, instead of being launched only once this grid has ended.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <int I, int N, typename F>

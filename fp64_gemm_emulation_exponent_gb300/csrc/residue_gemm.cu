@@ -874,6 +874,7 @@ template <bool LONG, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
+  grid_dependency_sync();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
@@ -1050,6 +1051,7 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmO, const GemmParams prm) {
+  grid_dependency_sync();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);  // swizzle-atom aligned tiles
@@ -1434,12 +1436,14 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   if (e != cudaSuccess) return e;
   if (!pairs) {
     const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
-    kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, tmO, prm);
-    return cudaGetLastError();
+    return launch_dependent(kernel, dim3(grid), dim3(kThreads), smem, stream, tmA, tmB, tmO, prm);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   pair_launch_config(&cfg, attr, smem, stream);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dependency_sync
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   // persistent: one CTA pair per co-resident cluster slot, at most one per SM pair
   int64_t npairs = num_sms / 2;
   if (resident < npairs) npairs = resident;

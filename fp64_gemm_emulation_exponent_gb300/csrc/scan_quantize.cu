@@ -129,6 +129,7 @@ __device__ __forceinline__ int max_half_octave(uint64_t amax) {
 
 template <bool NORM>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams sp) {
+  grid_dependency_sync();
   const int64_t bid = blockIdx.x;
   if (bid < sp.a_blocks) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -246,6 +247,7 @@ __device__ __forceinline__ int32_t scale_of(const uint64_t* amax, const uint64_t
 __global__ void finalize_scales_kernel(const uint64_t* __restrict__ amax, const uint64_t* __restrict__ nsum,
                                        int64_t M, int64_t N, int budget, int32_t* __restrict__ s,
                                        int32_t* __restrict__ t) {
+  grid_dependency_sync();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= M + N) return;
   const int32_t r = scale_of(amax, nsum, idx, budget);
@@ -392,6 +394,7 @@ struct QuantParams {
 // 128 rows.  Each thread writes one 32-byte run of every modulus' slice.
 template <int NL>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantParams qp) {
+  grid_dependency_sync();
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kQThreads + threadIdx.x;
   uint64_t v[kQK];
   int64_t row, k0, plane;
@@ -479,6 +482,7 @@ static_assert(kRowsMaxThreads % 32 == 0 && kRowsMaxThreads <= 1024, "whole warps
 template <int NL, bool NORM>
 __global__ void __launch_bounds__(kRowsMaxThreads) quantize_rows_kernel(const QuantParams qp, int budget,
                                                                         int32_t* __restrict__ s_out) {
+  grid_dependency_sync();
   __shared__ uint64_t wmax[kRowsMaxThreads / 32];
   const int64_t row = blockIdx.x;
   const int64_t k0 = static_cast<int64_t>(threadIdx.x) * kQK;
@@ -597,12 +601,13 @@ cudaError_t launch_scan(int64_t M, int64_t N, int64_t K, const double* A, int64_
   }
   const int64_t blocks = sp.a_blocks + b_blocks;
   if (blocks > 0) {
-    scan_kernel<false><<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (nsum) {  // the norm pass, once every maximum is in
-      scan_kernel<true><<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(sp);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_dependent(scan_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kScanThreads), 0, stream,
+                              sp)) != cudaSuccess)
+      return e;
+    if (nsum &&  // the norm pass, once every maximum is in
+        (e = launch_dependent(scan_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kScanThreads), 0, stream,
+                              sp)) != cudaSuccess)
+      return e;
   }
   return cudaSuccess;
 }
@@ -613,9 +618,8 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t K, const double* A, int64
   if (M + N == 0) return cudaSuccess;
   cudaError_t e = launch_scan(M, N, K, A, lda, B, ldb, amax, nsum, stream);
   if (e != cudaSuccess) return e;
-  finalize_scales_kernel<<<static_cast<unsigned>((M + N + 255) / 256), 256, 0, stream>>>(amax, nsum, M, N, budget,
-                                                                                          s, t);
-  return cudaGetLastError();
+  return launch_dependent(finalize_scales_kernel, dim3(static_cast<unsigned>((M + N + 255) / 256)), dim3(256), 0,
+                          stream, amax, nsum, M, N, budget, s, t);
 }
 
 cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const double* A,
@@ -657,11 +661,8 @@ cudaError_t launch_quantize(int64_t M, int64_t N, int64_t K, int64_t kpad, const
   // |a'| <= 2^budget: two 32-bit words of two's complement for a budget of
   // at most 62, three beyond
   if (budget > kMaxBudget) return cudaErrorInvalidValue;
-  if (budget <= 62)
-    quantize_kernel<2><<<blocks, kQThreads, 0, stream>>>(qp);
-  else
-    quantize_kernel<3><<<blocks, kQThreads, 0, stream>>>(qp);
-  return cudaGetLastError();
+  if (budget <= 62) return launch_dependent(quantize_kernel<2>, dim3(blocks), dim3(kQThreads), 0, stream, qp);
+  return launch_dependent(quantize_kernel<3>, dim3(blocks), dim3(kQThreads), 0, stream, qp);
 }
 
 bool quantize_rows_fits(int64_t kpad) { return kpad / kQK <= kRowsMaxThreads; }
@@ -683,20 +684,13 @@ cudaError_t launch_quantize_rows(int64_t M, int64_t K, int64_t kpad, const doubl
   qp.a_vec = (reinterpret_cast<uintptr_t>(A) % 32 == 0) && (lda % 4 == 0);
   const unsigned threads = static_cast<unsigned>((kpad / kQK + 31) / 32 * 32);
   const unsigned blocks = static_cast<unsigned>(M);
-#define OZK_ROWS_LAUNCH(NL)                                                    \
-  do {                                                                         \
-    if (norm)                                                                  \
-      quantize_rows_kernel<NL, true><<<blocks, threads, 0, stream>>>(qp, budget, s);  \
-    else                                                                       \
-      quantize_rows_kernel<NL, false><<<blocks, threads, 0, stream>>>(qp, budget, s); \
-  } while (0)
   if (budget > kMaxBudget) return cudaErrorInvalidValue;
+  const dim3 grid(blocks), block(threads);
   if (budget <= 62)
-    OZK_ROWS_LAUNCH(2);
-  else
-    OZK_ROWS_LAUNCH(3);
-#undef OZK_ROWS_LAUNCH
-  return cudaGetLastError();
+    return norm ? launch_dependent(quantize_rows_kernel<2, true>, grid, block, 0, stream, qp, budget, s)
+                : launch_dependent(quantize_rows_kernel<2, false>, grid, block, 0, stream, qp, budget, s);
+  return norm ? launch_dependent(quantize_rows_kernel<3, true>, grid, block, 0, stream, qp, budget, s)
+              : launch_dependent(quantize_rows_kernel<3, false>, grid, block, 0, stream, qp, budget, s);
 }
 
 }  // namespace ozk
