@@ -593,3 +593,35 @@ def test_deterministic_and_stream_ordered():
     st.synchronize()
     assert torch.equal(C1.view(torch.int64), C2.view(torch.int64))
     assert ozk.ozk_stream_status(st) == 0
+
+
+def test_back_to_back_calls_on_one_workspace():
+    """Kernels launch while the one before them finishes (dependent launches):
+    calls issued back to back on one stream and one caller workspace, with
+    other inputs, shapes and moduli counts (a split-K one among them) and the
+    caller's own work in between, must each see only their own data.  Each
+    result is checked against the oracle at sampled outputs after one final
+    synchronisation."""
+    cases = [(600, 520, 2100, 14, 1), (600, 520, 2100, 14, 2), (256, 300, 40000, 11, 3), (700, 90, 900, 20, 4),
+             (600, 520, 2100, 8, 5)]
+    ops = [inputs(M, N, K, seed=seed) for (M, N, K, n, seed) in cases]
+    need = max(ozk.ozk_workspace_size(M, N, K, n) for (M, N, K, n, _) in cases)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    outs, snaps = [], []
+    with torch.cuda.stream(st):
+        devs = [(dev(A), dev(B)) for (A, B) in ops]
+        st.synchronize()
+        for (M, N, K, n, _), (dA, dB) in zip(cases, devs):
+            C = torch.full((M, N), float("nan"), dtype=torch.float64, device="cuda")
+            ozk.ozk_dgemm_ws(M, N, K, dA, K, dB, N, C, N, n, ws, need, st)
+            snaps.append(C.clone())  # the caller's kernel right behind the call
+            dA.mul_(3.0)  # and one that overwrites an input the call has read
+            outs.append(C)
+    st.synchronize()
+    assert ozk.ozk_stream_status(st) == 0
+    for (M, N, K, n, seed), (A, B), C, S in zip(cases, ops, outs, snaps):
+        ii, jj = sample_pairs(M, N, 160, seed=seed)
+        Co, _, _, _ = oracle.sample(A, B, n, ii, jj)
+        assert same_bits(C.cpu().numpy()[ii, jj], Co), (M, N, K, n)
+        assert torch.equal(C.view(torch.int64), S.view(torch.int64))
