@@ -16,7 +16,7 @@ cudaError_t launch_nl_g(int64_t M, int64_t N, const void* in, int in_kind, int64
   constexpr int G = 1;
   const int64_t threads = M * ((N + 4 * G - 1) / (4 * G));
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  const RowDiv rd = row_div((N + 4 * G - 1) / (4 * G));
+  const FastDiv rd = fast_div((N + 4 * G - 1) / (4 * G));
   const dim3 grid(blocks), block(256);
   if (in_kind == 0)
     return X ? launch_dependent(crt_kernel<NL, 0, true, G, 0>, grid, block, 0, stream, in, ldi, plane, M, N, splits,

@@ -267,25 +267,6 @@ __device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[G]) {
 // point), so such outputs get the exact symmetric lift.
 constexpr uint32_t kLiftMargin = 1u << 13;
 
-// floor(g / d) for every g < 2^31 by one multiply-high, d fixed per launch
-// (the output column groups per row): with l = ceil(log2 d) and
-// m = ceil(2^(31 + l) / d) < 2^32, g m / 2^(31 + l) exceeds g / d by less
-// than g / 2^(31 + l) < 2^-l <= 1/d, which cannot carry it past the next
-// integer, so floor(g / d) = umulhi(g, m) >> (l - 1); d = 1 has s = -1.
-struct RowDiv {
-  uint32_t m;
-  int s;
-};
-inline RowDiv row_div(int64_t d) {
-  if (d <= 1) return {0u, -1};
-  int l = 0;
-  while ((int64_t{1} << l) < d) ++l;
-  const uint64_t num = uint64_t{1} << (31 + l);
-  return {static_cast<uint32_t>((num + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d)), l - 1};
-}
-__device__ __forceinline__ uint32_t div_rows(uint32_t g, const RowDiv& r) {
-  return r.s < 0 ? g : __umulhi(g, r.m) >> r.s;
-}
 
 
 
@@ -312,7 +293,7 @@ template <int NL, int IN_KIND, bool LIMBS, int G, int NFIX>
 __global__ void __launch_bounds__(256, NFIX ? (NL <= 3 ? 5 : (NL <= 4 ? 4 : 3)) : 1)
     crt_kernel(const void* __restrict__ in, int64_t ldi, int64_t plane, int64_t M, int64_t N, int splits,
                const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C, int64_t ldc,
-               uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K, const RowDiv rd) {
+               uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K, const FastDiv rd) {
   grid_dependency_sync();
   constexpr int W = 4 * G;  // columns per thread
   static_assert(IN_KIND != 2, "pair residues take crt_pairs_kernel");
@@ -328,7 +309,7 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 3 ? 5 : (NL <= 4 ? 4 : 3)) 
   int64_t i, jt;
   if (M * groups <= 0x7FFFFFFF) {
     const uint32_t g32 = static_cast<uint32_t>(gid), gr = static_cast<uint32_t>(groups);
-    const uint32_t i32 = div_rows(g32, rd);  // g32 / gr
+    const uint32_t i32 = div_fast(g32, rd);  // g32 / gr
     i = i32;
     jt = static_cast<int64_t>(g32 - i32 * gr) * W;
   } else {
@@ -581,7 +562,7 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1)
     crt_pairs_kernel(const void* __restrict__ in, int64_t ldi, int64_t plane, int64_t M, int64_t N,
                      const int32_t* __restrict__ s, const int32_t* __restrict__ t, double* __restrict__ C,
                      int64_t ldc, uint32_t* __restrict__ Xout, const __grid_constant__ CrtConst K,
-                     const RowDiv rd) {
+                     const FastDiv rd) {
   grid_dependency_sync();
   constexpr int W = 4 * G;
   constexpr uint32_t kPairLiftMargin = 1u << 20;
@@ -591,7 +572,7 @@ __global__ void __launch_bounds__(256, NFIX ? (NL <= 4 ? 4 : 3) : 1)
   int64_t i, jt;
   if (M * groups <= 0x7FFFFFFF) {
     const uint32_t g32 = static_cast<uint32_t>(gid), gr = static_cast<uint32_t>(groups);
-    const uint32_t i32 = div_rows(g32, rd);  // g32 / gr
+    const uint32_t i32 = div_fast(g32, rd);  // g32 / gr
     i = i32;
     jt = static_cast<int64_t>(g32 - i32 * gr) * W;
   } else {

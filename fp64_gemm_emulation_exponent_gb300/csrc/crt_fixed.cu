@@ -18,9 +18,9 @@ cudaError_t launch_fixed(int64_t M, int64_t N, const void* in, int in_kind, int6
   if (in_kind == 2)
     return launch_dependent(crt_pairs_kernel<crt_limbs(NM), false, 2, NM>,
                             dim3(static_cast<unsigned>((M * ((N + 7) / 8) + 255) / 256)), dim3(256), 0, stream, in,
-                            ldi, plane, M, N, s, t, C, ldc, nullptr, K, row_div((N + 7) / 8));
+                            ldi, plane, M, N, s, t, C, ldc, nullptr, K, fast_div((N + 7) / 8));
   return launch_dependent(crt_kernel<crt_limbs(NM), 0, false, G, NM>, dim3(blocks), dim3(256), 0, stream, in, ldi,
-                          plane, M, N, 1, s, t, C, ldc, nullptr, K, row_div((N + 4 * G - 1) / (4 * G)));
+                          plane, M, N, 1, s, t, C, ldc, nullptr, K, fast_div((N + 4 * G - 1) / (4 * G)));
 }
 
 template <int NM>

@@ -69,6 +69,27 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// floor(g / d) for every g < 2^31 by one multiply-high, d fixed per launch
+// (the combine's column groups per row, the GEMM's tile and split counts):
+// with l = ceil(log2 d) and m = ceil(2^(31 + l) / d) < 2^32, g m / 2^(31 + l)
+// exceeds g / d by less than g / 2^(31 + l) < 2^-l <= 1/d, which cannot carry
+// it past the next integer, so floor(g / d) = umulhi(g, m) >> (l - 1); d = 1
+// has s = -1.
+struct FastDiv {
+  uint32_t m;
+  int s;
+};
+inline FastDiv fast_div(int64_t d) {
+  if (d <= 1) return {0u, -1};
+  int l = 0;
+  while ((int64_t{1} << l) < d) ++l;
+  const uint64_t num = uint64_t{1} << (31 + l);
+  return {static_cast<uint32_t>((num + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d)), l - 1};
+}
+__device__ __forceinline__ uint32_t div_fast(uint32_t g, const FastDiv& r) {
+  return r.s < 0 ? g : __umulhi(g, r.m) >> r.s;
+}
+
 template <int I, int N, typename F>
 __host__ __device__ __forceinline__ void static_for(F&& f) {
   if constexpr (I < N) {

@@ -189,6 +189,9 @@ struct GemmParams {
   int mod_units;           // n, or ceil(n/2) pairs of moduli for out_kind 2
   int64_t ldo, out_plane;  // row stride and per-(split, modulus) plane stride, in elements
   void* out;
+  // the unit decode's divisors: tiles per modulus and split, tiles per group
+  // of tile rows, tile rows of the last (shorter) group, splits
+  FastDiv div_tiles, div_group, div_tail, div_splits;
 };
 
 // ---------------------------------------------------------------------------
@@ -484,20 +487,47 @@ struct Unit {
 // sweeping every column tile of B (the whole slice, 134 MB per modulus at
 // N = K = 8192) once per couple of tile rows.
 constexpr int kGroupM = 8;
+static_assert((kGroupM & (kGroupM - 1)) == 0, "a whole group's tile row and column by mask and shift");
 
-template <bool PAIRS>
+// Every role of every CTA decodes each of its units.  In the single-CTA
+// kernel, whose units are short (a 128 x 256 tile over at most 1024 of K),
+// the divisions are multiplies by the reciprocals the host computed for the
+// launch (a run-time divide is a long dependent chain): 8192^2 x 512 at 14
+// moduli 618 -> 601 us.  The CTA-pair kernel's units are long, and there the
+// reciprocals held in its control warps' 56 registers spilled more and cost
+// 0.3% at 4096^3, so it divides.
+template <bool PAIRS, bool FAST>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& prm) {
   Unit r;
-  const int tiles = prm.tiles_m * prm.tiles_n;
-  const int idx = u % tiles;
-  u /= tiles;
-  const int first = idx / (kGroupM * prm.tiles_n) * kGroupM;  // first tile row of the group
-  const int gm = min(prm.tiles_m - first, kGroupM);            // tile rows in the group
-  const int in = idx - first * prm.tiles_n;
-  r.mt = first + in % gm;
-  r.nt = in / gm;
-  r.sk = u % prm.splits;
-  r.q = u / prm.splits;
+  if constexpr (!FAST) {
+    const int tiles = prm.tiles_m * prm.tiles_n;
+    const int idx = u % tiles;
+    u /= tiles;
+    const int first = idx / (kGroupM * prm.tiles_n) * kGroupM;  // first tile row of the group
+    const int gm = min(prm.tiles_m - first, kGroupM);            // tile rows in the group
+    const int in = idx - first * prm.tiles_n;
+    r.mt = first + in % gm;
+    r.nt = in / gm;
+    r.sk = u % prm.splits;
+    r.q = u / prm.splits;
+  } else {
+    const uint32_t tiles = static_cast<uint32_t>(prm.tiles_m * prm.tiles_n);
+    const uint32_t uq = div_fast(static_cast<uint32_t>(u), prm.div_tiles);
+    const uint32_t idx = static_cast<uint32_t>(u) - uq * tiles;
+    const int first = static_cast<int>(div_fast(idx, prm.div_group)) * kGroupM;  // first tile row of the group
+    const uint32_t in = idx - static_cast<uint32_t>(first * prm.tiles_n);
+    if (prm.tiles_m - first >= kGroupM) {  // kGroupM tile rows in the group
+      r.mt = first + static_cast<int>(in & (kGroupM - 1));
+      r.nt = static_cast<int>(in / kGroupM);
+    } else {  // the last group, tiles_m mod kGroupM rows
+      const uint32_t nt = div_fast(in, prm.div_tail);
+      r.mt = first + static_cast<int>(in - nt * static_cast<uint32_t>(prm.tiles_m - first));
+      r.nt = static_cast<int>(nt);
+    }
+    const uint32_t q = div_fast(uq, prm.div_splits);
+    r.sk = static_cast<int>(uq - q * static_cast<uint32_t>(prm.splits));
+    r.q = static_cast<int>(q);
+  }
   if (PAIRS) {  // out_kind 2
     r.p = 2 * r.q;
     r.passes = min(2, prm.n - r.p);
@@ -927,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<KIND == 2>(u, prm);
+        const Unit w = decode_unit<KIND == 2, true>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
@@ -970,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<KIND == 2>(u, prm);
+        const Unit w = decode_unit<KIND == 2, true>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kChunkKB) {
           const int c1 = min(w.kb1, c0 + kChunkKB);
@@ -1022,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(half * kCols);
     auto release = [&](int b) { mbar_arrive(acce0 + 8 * b); };
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<KIND == 2>(u, prm);
+      const Unit w = decode_unit<KIND == 2, true>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kChunkKB - 1) / kChunkKB;
       const int64_t row0 = static_cast<int64_t>(w.mt) * BM + quad * 32;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
@@ -1111,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kPairStages; ++s) issued_parity[s] = -1;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit<KIND == 2>(u, prm);
+        const Unit w = decode_unit<KIND == 2, false>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag, prm.timeout_ns)) {
@@ -1148,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int u = pair; u < units && ok; u += npairs) {
-        const Unit w = decode_unit<KIND == 2>(u, prm);
+        const Unit w = decode_unit<KIND == 2, false>(u, prm);
         for (int ps = 0; ps < w.passes && ok; ++ps)
         for (int c0 = w.kb0; c0 < w.kb1 && ok; c0 += kPairChunkKB) {
           const int c1 = min(w.kb1, c0 + kPairChunkKB);
@@ -1200,7 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(half * kCols);
     auto release = [&](int b) { mbar_arrive_cluster(cluster_addr(acce0 + 8 * b, 0)); };
     for (int u = pair; u < units && ok; u += npairs) {
-      const Unit w = decode_unit<KIND == 2>(u, prm);
+      const Unit w = decode_unit<KIND == 2, false>(u, prm);
       const int nchunks = (w.kb1 - w.kb0 + kPairChunkKB - 1) / kPairChunkKB;
       const int64_t row0 = static_cast<int64_t>(w.mt) * kPairM + static_cast<int64_t>(rank) * BM + quad * 32;
       const int64_t gj0 = static_cast<int64_t>(w.nt) * BN + half * kCols;
@@ -1411,6 +1441,10 @@ cudaError_t launch_gemm(int64_t M, int64_t N, int64_t kpad, const uint16_t* a_sl
   // single CTAs otherwise
   const bool pairs = static_cast<int64_t>(prm.kb_per_split) * BK >= kPairMinK;
   prm.tiles_m = static_cast<int>(pairs ? (M + kPairM - 1) / kPairM : (M + BM - 1) / BM);
+  prm.div_tiles = fast_div(static_cast<int64_t>(prm.tiles_m) * prm.tiles_n);
+  prm.div_group = fast_div(static_cast<int64_t>(kGroupM) * prm.tiles_n);
+  prm.div_tail = fast_div(prm.tiles_m % kGroupM);
+  prm.div_splits = fast_div(splits);
   CUtensorMap tmA, tmB;
   if (!make_slice_map(&tmA, a_slices, M, kpad, a_plane, n, BM) ||
       !make_slice_map(&tmB, b_slices, N, kpad, b_plane, n, pairs ? kBHalf : BN))
