@@ -441,11 +441,11 @@ def quantize_tie_operands(M, N, K, n, seed):
     return lines(M, K), np.ascontiguousarray(lines(N, K).T)
 
 
-@pytest.mark.parametrize("n,K", [(8, 300), (14, 1000), (17, 100), (17, 16), (18, 1000), (20, 700)])
+@pytest.mark.parametrize("n,K", [(8, 300), (14, 1000), (17, 100), (17, 16), (18, 1000), (20, 700), (20, 64)])
 def test_quantize_round_half_to_even(n, K):
     """Scales and every residue slice bit-exact against the oracle when most
     scaled entries are exact halves: beta 26, 49 and 62 (the two-word
-    integer path of the quantiser), 63, 64 and 72 (three words)."""
+    integer path of the quantiser), 63, 64, 72 and 74 (three words)."""
     M, N = 70, 90
     A, B = quantize_tie_operands(M, N, K, n, seed=n * 100 + K)
     s, t = run_scale(dev(A), dev(B), n)

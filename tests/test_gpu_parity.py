@@ -118,11 +118,12 @@ def test_stages_other_moduli_counts(n):
     check_stages(A, B, n)
 
 
-@pytest.mark.parametrize("n,K", [(17, 100), (17, 16), (17, 5), (18, 300), (18, 1000), (16, 1), (20, 700)])
+@pytest.mark.parametrize("n,K", [(17, 100), (17, 16), (17, 5), (18, 300), (18, 1000), (16, 1), (20, 700), (20, 2),
+                                 (20, 1)])
 def test_stages_across_the_integer_widths(n, K):
-    """beta 62 (two 32-bit words per scaled element), 63, 64, 65 and 72
-    (three words; the integer crosses 2^64 from beta 64): every stage
-    bit-exact."""
+    """beta 62 (two 32-bit words per scaled element), 63, 64, 65, 72, 76 and
+    77, the largest budget of any moduli count (three words; the integer
+    crosses 2^64 from beta 64): every stage bit-exact."""
     A, B = inputs(70, 90, K, seed=n * 1000 + K, kind="special")
     check_stages(A, B, n)
 
