@@ -17,7 +17,13 @@
  *    14 gives about a 53-bit product, 8 about 26 bits per operand.
  *  - Device pointers belong to the caller; the library never frees them.
  *  - ozk_stream_t is a cudaStream_t (NULL = legacy default stream).  Work is
- *    stream-ordered and asynchronous unless stated otherwise.
+ *    stream-ordered and asynchronous unless stated otherwise.  The library's
+ *    kernels allow programmatic dependent launch: each waits for the work
+ *    before it, and lets the kernel after it launch early.  A caller kernel
+ *    launched after a call with programmatic stream serialisation allowed
+ *    must itself wait (griddepcontrol.wait, cudaGridDependencySynchronize)
+ *    before it reads the call's results; ordinary launches, copies and
+ *    events are ordered as usual.
  *  - Argument errors are returned synchronously before anything is launched.
  *    Launch failures return OZK_ERR_CUDA.  Faults detected inside a kernel
  *    (a pipeline wait that ran out) are latched on the device and reported by
